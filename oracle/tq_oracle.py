@@ -1,0 +1,583 @@
+"""fp64 CPU oracle for the rotation-quantised KV cache and compressed-domain
+decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It shares no code with
+the CUDA library (``rotated_bit_kv_gb300``), and the library never imports it.
+
+The oracle is deliberately plain and slow: dense matrices instead of butterflies,
+closed-form Beta-density integrals instead of tables, one function per step of
+the method, in the order the pages give them.  Sources, by page title:
+
+* [TQ-MNN]  "TurboQuant: ... MNN runs it on the phone" (zhaode.wang):
+  §2.1 the three-step encoder (norm, rotate, per-coordinate codebook search);
+  §2.2 the coordinate density after a random rotation, f(t) ~ (1-t^2)^((d-3)/2);
+  §2.3 the Lloyd-Max codebook (centroid / midpoint conditions) and the
+       MSE <= 2.7/4^b bound;
+  §3.1 Hadamard with a +-1 sign flip in place of a random orthogonal matrix,
+       32-wide blocks with their own norm;
+  §3.3 8 three-bit indices in 3 bytes, two four-bit indices per byte,
+       rotated-domain K dot and V accumulation, in-place quantisation on write;
+  §3.4 codebook search as a count of boundary comparisons (strict greater-than).
+* [RotaryQuant] "RotaryQuant: Fitting 120B MoE Models on Consumer Hardware via
+  Fused Compressed-Space Attention" (papernotes.org):
+  Key design 2: R = R_SO(4) o H_d with v -> q_L v conj(q_R) per 4-dim block;
+  Key design 3: <Rq, Rk> = q^T k, o~ = sum_j a_j v~_j = R o, one inverse rotation.
+* [Block-GTQ] "RoPE-Aware Bit Allocation for KV-Cache Quantization" (aitrends.kr):
+  block energy s_i, objective J(b) = sum_i s_i 4^(-b_i), greedy allocation by
+  Delta_i = (3/4) s_i 4^(-b_i), same-width grouping, key-axis split with
+  log-sum-exp merge.
+
+Readings where the pages are silent or ambiguous (each also listed in the design doc):
+* density exponent (d-3)/2 (the §2.2 formula; the intuition paragraph's
+  (d-2)/2 omits the Jacobian of the slice);
+* the codebook dimension d is the width of the normalised block (128, 32, or a
+  mixed-rate group's width);
+* y = H . D . x (sign flip first); SO(4) variant y = S . H . x with no sign flip;
+* search ties go to the lower cell (strict >, as the NEON compare-count does);
+  the decision is taken in fp32: fp32(y) against fp32 boundaries;
+* 3-bit packing is LSB first: index i of a vector occupies bits [3i, 3i+3) of
+  the little-endian byte stream, so each 3-byte group holds 8 whole indices;
+* the stored norm is ||x|| as is (no re-normalisation by ||Q(y)||), rounded to
+  the norm dtype; a zero vector stores norm 0 and index 2^(b-1)-1 everywhere;
+* mixed-rate keys: RoPE block i is coordinates (2i, 2i+1); each same-width group
+  is encoded by one TQ-MSE encoder with its own random orthogonal matrix, its
+  own norm and the codebook for its own width; groups are laid out in ascending
+  bit width, one index per nibble;
+* attention scale 1/sqrt(head_dim); greedy ties go to the lowest block index.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import List, Sequence, Tuple
+
+import numpy as np
+from scipy.special import betainc, beta as beta_fn
+
+# ============================================================================
+# 1. Coordinate density and the Lloyd-Max codebook  [TQ-MNN §2.2, §2.3]
+# ============================================================================
+
+
+def density_exponent(d: int) -> float:
+    """a in f(t) = (1 - t^2)^a / Z on [-1, 1] for one coordinate of a uniformly
+    random point on the unit sphere in R^d  [TQ-MNN §2.2]."""
+    return (d - 3) / 2.0
+
+
+def _Z(d: int) -> float:
+    a = density_exponent(d)
+    return beta_fn(0.5, a + 1.0)
+
+
+def coord_cdf(t, d: int):
+    """P(T <= t).  T^2 ~ Beta(1/2, a+1), so P(|T| <= x) = I_{x^2}(1/2, a+1)."""
+    t = np.asarray(t, dtype=np.float64)
+    a = density_exponent(d)
+    return 0.5 + 0.5 * np.sign(t) * betainc(0.5, a + 1.0, np.minimum(t * t, 1.0))
+
+
+def coord_tail(t, d: int):
+    """P(T > t) for t >= 0, computed without cancellation: 1/2 I_{1-t^2}(a+1, 1/2)."""
+    t = np.asarray(t, dtype=np.float64)
+    a = density_exponent(d)
+    return 0.5 * betainc(a + 1.0, 0.5, np.maximum(1.0 - t * t, 0.0))
+
+
+def cell_probability(lo, hi, d: int):
+    """P(lo < T <= hi), using the tail form on the positive side."""
+    lo = np.asarray(lo, dtype=np.float64)
+    hi = np.asarray(hi, dtype=np.float64)
+    pos = lo >= 0
+    neg = hi <= 0
+    out = coord_cdf(hi, d) - coord_cdf(lo, d)
+    out = np.where(pos, coord_tail(np.abs(lo), d) - coord_tail(np.abs(hi), d), out)
+    out = np.where(neg, coord_tail(np.abs(hi), d) - coord_tail(np.abs(lo), d), out)
+    return out
+
+
+def first_moment_antiderivative(t, d: int):
+    """F1(t) with F1' = t f(t):  F1(t) = -(1 - t^2)^(a+1) / (2 (a+1) Z)."""
+    t = np.asarray(t, dtype=np.float64)
+    a = density_exponent(d)
+    return -np.power(np.maximum(1.0 - t * t, 0.0), a + 1.0) / (2.0 * (a + 1.0) * _Z(d))
+
+
+def cell_first_moment(lo, hi, d: int):
+    """integral over (lo, hi] of t f(t) dt."""
+    return first_moment_antiderivative(hi, d) - first_moment_antiderivative(lo, d)
+
+
+def cell_second_moment(lo, hi, d: int):
+    """integral over (lo, hi] of t^2 f(t) dt.  With u = t^2, the integral over
+    [0, x] is 1/2 B(3/2, a+1) I_{x^2}(3/2, a+1) / Z; odd extension by sign."""
+    a = density_exponent(d)
+    Z = _Z(d)
+
+    def G(t):
+        t = np.asarray(t, dtype=np.float64)
+        return np.sign(t) * 0.5 * beta_fn(1.5, a + 1.0) * betainc(1.5, a + 1.0, np.minimum(t * t, 1.0)) / Z
+
+    return G(hi) - G(lo)
+
+
+@dataclass
+class Codebook:
+    d: int
+    bits: int
+    centroids: np.ndarray    # ascending, 2^bits entries (fp64)
+    boundaries: np.ndarray   # 2^bits - 1 midpoints (fp64)
+    iterations: int
+
+
+def lloyd_max_codebook(d: int, bits: int, tol: float = 1e-15, max_iter: int = 2_000_000) -> Codebook:
+    """1-D continuous k-means on f(t) with 2^bits cells  [TQ-MNN §2.3]:
+    boundaries are midpoints of neighbouring centroids; each centroid is the
+    conditional mean of its cell; iterate until the centroids stop moving."""
+    if d < 2:
+        raise ValueError("codebook dimension must be >= 2")
+    K = 1 << bits
+    # initial centroids: the density's own quantiles at (k + 1/2) / K
+    from scipy.special import betaincinv
+    a = density_exponent(d)
+    p = (np.arange(K) + 0.5) / K
+    mag = np.sqrt(betaincinv(0.5, a + 1.0, np.abs(2.0 * p - 1.0)))
+    c = np.sign(p - 0.5) * mag
+    for it in range(1, max_iter + 1):
+        b = 0.5 * (c[:-1] + c[1:])
+        lo = np.concatenate(([-1.0], b))
+        hi = np.concatenate((b, [1.0]))
+        c_new = cell_first_moment(lo, hi, d) / cell_probability(lo, hi, d)
+        if np.max(np.abs(c_new - c)) < tol:
+            c = c_new
+            break
+        c = c_new
+    else:
+        raise RuntimeError(f"Lloyd-Max did not converge for d={d}, bits={bits}")
+    return Codebook(d, bits, c, 0.5 * (c[:-1] + c[1:]), it)
+
+
+def codebook_mse(cb: Codebook) -> float:
+    """E[(T - Q(T))^2] per coordinate (closed form from cell moments)."""
+    lo = np.concatenate(([-1.0], cb.boundaries))
+    hi = np.concatenate((cb.boundaries, [1.0]))
+    P = cell_probability(lo, hi, cb.d)
+    M1 = cell_first_moment(lo, hi, cb.d)
+    M2 = cell_second_moment(lo, hi, cb.d)
+    return float(np.sum(M2 - 2.0 * cb.centroids * M1 + cb.centroids ** 2 * P))
+
+
+_CB_CACHE = {}
+
+
+def codebook(d: int, bits: int) -> Codebook:
+    key = (d, bits)
+    if key not in _CB_CACHE:
+        _CB_CACHE[key] = lloyd_max_codebook(d, bits)
+    return _CB_CACHE[key]
+
+
+# ============================================================================
+# 2. Rotations  [TQ-MNN §3.1; RotaryQuant Key design 2; Block-GTQ grouping]
+# ============================================================================
+
+
+def hadamard(n: int) -> np.ndarray:
+    """Normalised Walsh-Hadamard matrix in natural (Sylvester) order, built by
+    the doubling recursion H_2n = [[H, H], [H, -H]] / sqrt(2)."""
+    if n < 1 or n & (n - 1):
+        raise ValueError("n must be a power of two")
+    H = np.ones((1, 1))
+    while H.shape[0] < n:
+        H = np.block([[H, H], [H, -H]]) / math.sqrt(2.0)
+    return H
+
+
+def quat_mul(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """Hamilton product of quaternions (w, x, y, z)."""
+    pw, px, py, pz = p
+    qw, qx, qy, qz = q
+    return np.array([
+        pw * qw - px * qx - py * qy - pz * qz,
+        pw * qx + px * qw + py * qz - pz * qy,
+        pw * qy - px * qz + py * qw + pz * qx,
+        pw * qz + px * qy - py * qx + pz * qw,
+    ])
+
+
+def quat_conj(q: np.ndarray) -> np.ndarray:
+    return np.array([q[0], -q[1], -q[2], -q[3]])
+
+
+def so4_block_matrix(qL: np.ndarray, qR: np.ndarray) -> np.ndarray:
+    """4x4 matrix of v -> q_L v conj(q_R), v = (w, x, y, z) read as w + xi + yj + zk
+    [RotaryQuant, Key design 2].  Built column by column from the Hamilton
+    product of the basis quaternions."""
+    qRc = quat_conj(np.asarray(qR, dtype=np.float64))
+    qL = np.asarray(qL, dtype=np.float64)
+    M = np.zeros((4, 4))
+    for j in range(4):
+        e = np.zeros(4)
+        e[j] = 1.0
+        M[:, j] = quat_mul(quat_mul(qL, e), qRc)
+    return M
+
+
+def block_diag(blocks: Sequence[np.ndarray]) -> np.ndarray:
+    n = sum(b.shape[0] for b in blocks)
+    out = np.zeros((n, n))
+    o = 0
+    for b in blocks:
+        k = b.shape[0]
+        out[o:o + k, o:o + k] = b
+        o += k
+    return out
+
+
+@dataclass
+class Segment:
+    """A contiguous run of rotated coordinates that shares one norm and one
+    codebook: positions [start, start+length) of the code record."""
+    start: int
+    length: int
+    cb_dim: int
+    bits: int
+    norm_slot: int
+
+
+@dataclass
+class HeadSpec:
+    """Everything the encoder needs for one KV head: the dense rotation R
+    (rotated = R @ x, in code-record order), its segments, and the coordinate
+    sets whose norms each segment stores (norm over x restricted to them)."""
+    R: np.ndarray
+    segments: List[Segment]
+    seg_coords: List[np.ndarray]
+    n_norm_slots: int
+    nibble_codes: bool        # codes stored one per nibble (4-bit or mixed)
+
+
+def spec_wht128(signs: np.ndarray, bits: int) -> HeadSpec:
+    """y = H_128 D x, one norm  [TQ-MNN §3.1]."""
+    d = signs.shape[0]
+    R = hadamard(d) @ np.diag(signs.astype(np.float64))
+    return HeadSpec(R, [Segment(0, d, d, bits, 0)], [np.arange(d)], 1, bits == 4)
+
+
+def spec_wht32(signs: np.ndarray, bits: int) -> HeadSpec:
+    """Four independent 32-point sign-flipped WHTs, one norm per block
+    [TQ-MNN §3.1 block_size = 32]; block k uses signs[32k:32k+32]."""
+    d = signs.shape[0]
+    H = hadamard(32)
+    blocks = [H @ np.diag(signs[32 * k:32 * k + 32].astype(np.float64)) for k in range(d // 32)]
+    segs = [Segment(32 * k, 32, 32, bits, k) for k in range(d // 32)]
+    coords = [np.arange(32 * k, 32 * k + 32) for k in range(d // 32)]
+    return HeadSpec(block_diag(blocks), segs, coords, d // 32, bits == 4)
+
+
+def spec_so4_wht128(quats: np.ndarray, bits: int) -> HeadSpec:
+    """R = R_SO(4) o H_d  [RotaryQuant, Key design 2]: y = S H x, S block
+    diagonal with one q_L v conj(q_R) map per 4-dim block, no sign flip."""
+    d = quats.shape[0] * 4
+    S = block_diag([so4_block_matrix(quats[i, 0], quats[i, 1]) for i in range(d // 4)])
+    return HeadSpec(S @ hadamard(d), [Segment(0, d, d, bits, 0)], [np.arange(d)], 1, bits == 4)
+
+
+def group_layout(block_bits: Sequence[int], b_min: int = 1, b_max: int = 4):
+    """Same-width grouping of RoPE blocks  [Block-GTQ, physical encoding]:
+    for each width b (ascending) with at least one block, the coordinates
+    (2i, 2i+1) of its blocks in ascending i.  Returns [(b, coords)]."""
+    block_bits = np.asarray(block_bits)
+    out = []
+    for b in range(b_min, b_max + 1):
+        blocks = np.nonzero(block_bits == b)[0]
+        if blocks.size:
+            coords = np.stack([2 * blocks, 2 * blocks + 1], axis=1).reshape(-1)
+            out.append((b, coords))
+    return out
+
+
+def spec_group_dense(block_bits: Sequence[int], mats: dict) -> HeadSpec:
+    """Mixed-rate keys: each same-width group is one TQ-MSE encoder with a
+    random orthogonal matrix Pi_b of its own width, its own norm and the
+    codebook for (n_b, b)  [Block-GTQ; TQ-MNN §2.1].  `mats[b]` is Pi_b."""
+    layout = group_layout(block_bits)
+    d = 2 * len(block_bits)
+    R = np.zeros((d, d))
+    segs, coords = [], []
+    o = 0
+    for b, cs in layout:
+        n = cs.size
+        P = np.asarray(mats[b], dtype=np.float64)
+        assert P.shape == (n, n)
+        R[o:o + n, cs] = P
+        segs.append(Segment(o, n, n, b, b - 1))
+        coords.append(cs)
+        o += n
+    return HeadSpec(R, segs, coords, 4, True)
+
+
+# ============================================================================
+# 3. Quantise and pack  [TQ-MNN §2.1, §3.3, §3.4]
+# ============================================================================
+
+
+def round_norm(n: np.ndarray, norm_dtype: str) -> np.ndarray:
+    if norm_dtype == "f16":
+        return n.astype(np.float16)
+    return n.astype(np.float32)
+
+
+def codebook_search(y: np.ndarray, cb: Codebook) -> np.ndarray:
+    """idx = #{k : y > beta_k}: the count of boundaries strictly below y
+    [TQ-MNN §3.4], so a coordinate on a boundary takes the lower cell.  The
+    comparison is made in fp32 (fp32(y) against fp32 boundaries)."""
+    b32 = cb.boundaries.astype(np.float32)
+    y32 = np.asarray(y).astype(np.float32)
+    return np.sum(y32[..., None] > b32, axis=-1).astype(np.int64)
+
+
+def quantize(x: np.ndarray, spec: HeadSpec, norm_dtype: str):
+    """Encode vectors x [N][d] (exact fp64 values of the inputs).
+
+    Per segment: n = ||x_seg||; y = (R x)_seg / n; idx = #{k : y > beta_k}
+    with the decision in fp32.  Returns (idx [N][d] int, stored norms
+    [N][slots], y [N][d] fp64)."""
+    x = np.asarray(x, dtype=np.float64)
+    N, d = x.shape
+    rot = x @ spec.R.T
+    idx = np.zeros((N, d), dtype=np.int64)
+    y = np.zeros((N, d))
+    norms = np.zeros((N, spec.n_norm_slots))
+    for seg, cs in zip(spec.segments, spec.seg_coords):
+        n = np.sqrt(np.sum(x[:, cs] ** 2, axis=1))
+        sl = slice(seg.start, seg.start + seg.length)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            ys = np.where(n[:, None] > 0, rot[:, sl] / n[:, None], 0.0)
+        y[:, sl] = ys
+        idx[:, sl] = codebook_search(ys, codebook(seg.cb_dim, seg.bits))
+        norms[:, seg.norm_slot] = n
+    return idx, round_norm(norms, norm_dtype), y
+
+
+def pack_3bit(idx: np.ndarray) -> np.ndarray:
+    """8 three-bit indices per 3 bytes: for group g, w = sum_i idx[8g+i] << 3i,
+    stored little-endian as w & 255, (w >> 8) & 255, (w >> 16) & 255."""
+    idx = np.asarray(idx, dtype=np.int64)
+    N, d = idx.shape
+    assert d % 8 == 0 and idx.min() >= 0 and idx.max() < 8
+    g = idx.reshape(N, d // 8, 8)
+    w = np.zeros((N, d // 8), dtype=np.int64)
+    for i in range(8):
+        w |= g[:, :, i] << (3 * i)
+    out = np.stack([w & 255, (w >> 8) & 255, (w >> 16) & 255], axis=2)
+    return out.reshape(N, 3 * d // 8).astype(np.uint8)
+
+
+def unpack_3bit(b: np.ndarray, d: int) -> np.ndarray:
+    b = np.asarray(b, dtype=np.int64).reshape(b.shape[0], d // 8, 3)
+    w = b[:, :, 0] | (b[:, :, 1] << 8) | (b[:, :, 2] << 16)
+    return np.stack([(w >> (3 * i)) & 7 for i in range(8)], axis=2).reshape(b.shape[0], d)
+
+
+def pack_4bit(idx: np.ndarray) -> np.ndarray:
+    """Two indices per byte: byte j = idx[2j] | idx[2j+1] << 4."""
+    idx = np.asarray(idx, dtype=np.int64)
+    assert idx.min() >= 0 and idx.max() < 16
+    return (idx[:, 0::2] | (idx[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_4bit(b: np.ndarray, d: int) -> np.ndarray:
+    b = np.asarray(b, dtype=np.int64)
+    out = np.zeros((b.shape[0], d), dtype=np.int64)
+    out[:, 0::2] = b & 15
+    out[:, 1::2] = b >> 4
+    return out
+
+
+def pack(idx: np.ndarray, spec: HeadSpec) -> np.ndarray:
+    return pack_4bit(idx) if spec.nibble_codes else pack_3bit(idx)
+
+
+def unpack(codes: np.ndarray, spec: HeadSpec, d: int) -> np.ndarray:
+    return unpack_4bit(codes, d) if spec.nibble_codes else unpack_3bit(codes, d)
+
+
+def dequantize_rotated(idx: np.ndarray, norms: np.ndarray, spec: HeadSpec) -> np.ndarray:
+    """v~ = n_seg * C_seg[idx] in the rotated domain (no inverse rotation)."""
+    N, d = idx.shape
+    out = np.zeros((N, d))
+    nrm = np.asarray(norms, dtype=np.float64)
+    for seg in spec.segments:
+        sl = slice(seg.start, seg.start + seg.length)
+        C = codebook(seg.cb_dim, seg.bits).centroids
+        out[:, sl] = nrm[:, seg.norm_slot][:, None] * C[idx[:, sl]]
+    return out
+
+
+def dequantize(idx: np.ndarray, norms: np.ndarray, spec: HeadSpec) -> np.ndarray:
+    """Reverse of the encoder [TQ-MNN §2.1]: codebook lookup -> inverse
+    rotation -> times the norm."""
+    return dequantize_rotated(idx, norms, spec) @ spec.R
+
+
+# ============================================================================
+# 4. Block energy and greedy bit allocation  [Block-GTQ]
+# ============================================================================
+
+
+def block_energy(q_cal: np.ndarray, k_cal: np.ndarray) -> np.ndarray:
+    """s_i = 1/2 (E_{t, g in G(h)} ||q^(i)||^2 + E_t ||k^(i)||^2), block i =
+    coordinates (2i, 2i+1).  q_cal [T][G][d] holds the query heads that read
+    this KV head; k_cal [T][d]."""
+    q = np.asarray(q_cal, dtype=np.float64)
+    k = np.asarray(k_cal, dtype=np.float64)
+    d = k.shape[-1]
+    qb = (q.reshape(q.shape[0], q.shape[1], d // 2, 2) ** 2).sum(-1)   # [T][G][L]
+    kb = (k.reshape(k.shape[0], d // 2, 2) ** 2).sum(-1)                # [T][L]
+    return 0.5 * (qb.mean(axis=(0, 1)) + kb.mean(axis=0))
+
+
+def greedy_bit_alloc(s: Sequence[float], b_min: int, b_max: int, B_total: int) -> np.ndarray:
+    """Minimise J(b) = sum_i s_i 4^(-b_i) s.t. b_min <= b_i <= b_max,
+    sum_i b_i = B_total: start at b_min, then repeatedly add one bit to the
+    block with the largest marginal gain Delta_i = (3/4) s_i 4^(-b_i) among
+    blocks below b_max (ties -> lowest index)."""
+    s = np.asarray(s, dtype=np.float64)
+    L = s.size
+    if B_total < L * b_min or B_total > L * b_max or b_min > b_max:
+        raise ValueError("infeasible bit budget")
+    b = np.full(L, b_min, dtype=np.int64)
+    for _ in range(B_total - L * b_min):
+        best, best_gain = -1, -np.inf
+        for i in range(L):
+            if b[i] < b_max:
+                gain = 0.75 * s[i] * 4.0 ** (-b[i])
+                if gain > best_gain:
+                    best, best_gain = i, gain
+        b[best] += 1
+    return b
+
+
+def allocation_objective(s, b) -> float:
+    return float(np.sum(np.asarray(s, dtype=np.float64) * 4.0 ** (-np.asarray(b, dtype=np.float64))))
+
+
+# ============================================================================
+# 5. Decode attention on the packed cache  [RotaryQuant Key design 3;
+#    TQ-MNN §3.3; Block-GTQ key-axis split]
+# ============================================================================
+
+
+def attend_rotated(q: np.ndarray, k_idx, k_norm, k_spec: HeadSpec, v_idx, v_norm, v_spec: HeadSpec,
+                   seq_len: int) -> np.ndarray:
+    """One (batch, KV head): q [G][d] (exact fp64 of the stored query).
+
+    q~ = R_K q; s_j = <q~, k~_j> / sqrt(d) with k~_j = n_j C[idx_j] per segment;
+    a = softmax over j < seq_len; o~ = sum_j a_j v~_j; o = R_V^T o~."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    L = int(seq_len)
+    if L <= 0:
+        return np.zeros_like(q)
+    qt = q @ k_spec.R.T                                   # [G][d]
+    Kt = dequantize_rotated(k_idx[:L], k_norm[:L], k_spec)
+    Vt = dequantize_rotated(v_idx[:L], v_norm[:L], v_spec)
+    s = qt @ Kt.T / math.sqrt(d)                          # [G][L]
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    a = p / p.sum(axis=1, keepdims=True)
+    ot = a @ Vt                                           # rotated-domain output
+    return ot @ v_spec.R                                  # R^T applied: o = R^T o~
+
+
+def attend_dequantized(q, k_idx, k_norm, k_spec, v_idx, v_norm, v_spec, seq_len) -> np.ndarray:
+    """The same attention computed the conventional way: dequantise every key
+    and value back to the original domain, then attend with the raw q."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    L = int(seq_len)
+    if L <= 0:
+        return np.zeros_like(q)
+    K = dequantize(k_idx[:L], k_norm[:L], k_spec)
+    V = dequantize(v_idx[:L], v_norm[:L], v_spec)
+    s = q @ K.T / math.sqrt(d)
+    a = np.exp(s - s.max(axis=1, keepdims=True))
+    a /= a.sum(axis=1, keepdims=True)
+    return a @ V
+
+
+def attend_exact(q, K, V, seq_len) -> np.ndarray:
+    """Unquantised fp64 attention (for the reported quantisation-error statistic)."""
+    q = np.asarray(q, dtype=np.float64)
+    L = int(seq_len)
+    s = q @ np.asarray(K[:L], dtype=np.float64).T / math.sqrt(q.shape[-1])
+    a = np.exp(s - s.max(axis=1, keepdims=True))
+    a /= a.sum(axis=1, keepdims=True)
+    return a @ np.asarray(V[:L], dtype=np.float64)
+
+
+def split_partials(q, k_idx, k_norm, k_spec, v_idx, v_norm, v_spec, bounds: Sequence[Tuple[int, int]]):
+    """Per key-axis section [lo, hi): (m, l, o~_unnormalised) with
+    m = max_j s_j, l = sum_j exp(s_j - m), o~ = sum_j exp(s_j - m) v~_j.
+    An empty section yields (-inf, 0, 0)."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    qt = q @ k_spec.R.T
+    out = []
+    for lo, hi in bounds:
+        if hi <= lo:
+            out.append((np.full(q.shape[0], -np.inf), np.zeros(q.shape[0]), np.zeros_like(q)))
+            continue
+        Kt = dequantize_rotated(k_idx[lo:hi], k_norm[lo:hi], k_spec)
+        Vt = dequantize_rotated(v_idx[lo:hi], v_norm[lo:hi], v_spec)
+        s = qt @ Kt.T / math.sqrt(d)
+        m = s.max(axis=1)
+        p = np.exp(s - m[:, None])
+        out.append((m, p.sum(axis=1), p @ Vt))
+    return out
+
+
+def lse_merge(partials, v_spec: HeadSpec) -> np.ndarray:
+    """Log-sum-exp merge of key-axis sections, then the single inverse rotation:
+    M = max m_s; l = sum_s e^(m_s - M) l_s; o~ = sum_s e^(m_s - M) o~_s / l;
+    o = R_V^T o~.  Sections with m = -inf contribute nothing."""
+    ms = np.stack([p[0] for p in partials])            # [S][G]
+    M = ms.max(axis=0)
+    w = np.where(np.isfinite(ms), np.exp(ms - M[None]), 0.0)
+    l = sum(w[i] * partials[i][1] for i in range(len(partials)))
+    ot = sum(w[i][:, None] * partials[i][2] for i in range(len(partials)))
+    return (ot / l[:, None]) @ v_spec.R
+
+
+# ============================================================================
+# 6. Whole-cache helpers (loops over (batch, KV head); no reordering)
+# ============================================================================
+
+
+def head_specs(wl, inputs, block_bits=None, mats=None):
+    """(k_spec, v_spec) per KV head for a workload description."""
+    from workloads import ROT_WHT128, ROT_WHT32, ROT_SO4_WHT128
+    specs = []
+    for h in range(wl.n_kv_heads):
+        if wl.rot == ROT_WHT128:
+            v = spec_wht128(inputs.signs[h], wl.v_bits)
+            k = spec_wht128(inputs.signs[h], wl.k_bits)
+        elif wl.rot == ROT_WHT32:
+            v = spec_wht32(inputs.signs[h], wl.v_bits)
+            k = spec_wht32(inputs.signs[h], wl.k_bits)
+        elif wl.rot == ROT_SO4_WHT128:
+            v = spec_so4_wht128(inputs.quats[h], wl.v_bits)
+            k = spec_so4_wht128(inputs.quats[h], wl.k_bits)
+        else:
+            raise ValueError(wl.rot)
+        if wl.mixed_k:
+            k = spec_group_dense(block_bits[h], mats[h])
+        specs.append((k, v))
+    return specs
+
+
+def norm_dtype_name(wl) -> str:
+    from workloads import F16
+    return "f16" if wl.norm_dtype == F16 else "f32"
