@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step of the rotation-quantised packed KV cache on
+the Llama-3.1-8B-shaped decode workload: batch 32, 32 query heads, 8 KV heads,
+head_dim 128, T = 8192 cached tokens per sequence, bf16 q/K/V, 3-bit K and V,
+128-point sign-flipped WHT, fp16 norms.
+
+A step is one pass of the whole hot path: quantise-and-append the new token's
+K and V for every sequence (write side) and decode attention for every query
+head over T tokens on the packed codes (read side).
+
+Prints one JSON line.  `value` is the algorithmic HBM throughput of the step
+(codes + norms read, q read, out written, appended bytes) in GB/s, summed over
+ranks; `us_per_step` is the device time per step.  The roofline block reports
+the decode kernel alone against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  (N > 1 under torch.distributed.run: independent replicas, one per GPU)
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "packed 3-bit KV decode attention: µs/step and HBM GB/s as % of GB300 peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(wl: W.Workload, T: int, desc) -> dict:
+    B, Hkv, Hq, d = wl.batch, wl.n_kv_heads, wl.n_q_heads, wl.head_dim
+    per_tok = desc.k_code_bytes + desc.v_code_bytes + (desc.k_norm_slots + desc.v_norm_slots) * desc.norm_bytes
+    in_b = 4 if wl.in_dtype == W.F32 else 2
+    decode = B * T * Hkv * per_tok + B * Hq * d * in_b + B * Hq * d * 4
+    append = B * Hkv * 2 * d * in_b + B * Hkv * per_tok
+    return {"decode": decode, "append": append, "step": decode + append}
+
+
+def workload_name(wl, T):
+    return (f"llama8b_decode: batch {wl.batch}, {wl.n_q_heads} q heads / {wl.n_kv_heads} KV heads, d=128, "
+            f"T={T}, bf16 q/K/V, 3-bit K and V, 128-point sign-flipped WHT, fp16 norms")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (started before, stopped after)."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        self.proc = None
+        vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+        gpu_index = vis[local_rank].strip() if local_rank < len(vis) else str(local_rank)
+        self.path = os.path.join("/tmp", f"tq_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("tq_decode.cu", "tq_device.cuh", "tq_internal.h"):
+        with open(os.path.join(ROOT, "rotated_bit_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_llama8b_T8192.md")
+    if not os.path.exists(p):
+        return None
+    src, traffic = None, None
+    for line in open(p):
+        if line.startswith("kernel_source_sha256_16:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if src == kernel_source_hash() else None
+
+
+# ----------------------------------------------------------------------------
+# CPU leg: the oracle as it stands, on a bounded sample of the same step
+class OracleLeg:
+    """The oracle as it stands, timed on a bounded sample of the step: for a few
+    (batch, KV head) pairs, encode the new token's K and V and run attention
+    over T cached tokens (the cache itself is encoded once, untimed)."""
+
+    def __init__(self, wl, T, n_pairs):
+        from gpu_harness import Setup, oracle_encode
+        from oracle import tq_oracle as O
+        self.O = O
+        self.wl, self.T = wl.with_(batch=1), T
+        self.inp = W.make_inputs(self.wl, seq_len=T)
+        self.specs = O.head_specs(self.wl, self.inp)
+        self.st = Setup(self.wl, self.inp, None, None, self.specs, None, None)
+        self.heads = list(range(min(n_pairs, wl.n_kv_heads)))
+        self.encs = {h: (oracle_encode(self.st, "k", 0, h), oracle_encode(self.st, "v", 0, h)) for h in self.heads}
+
+    def seconds_per_pair(self, reps=1):
+        from gpu_harness import oracle_attention
+        O, wl, T, inp = self.O, self.wl, self.T, self.inp
+        t0 = time.perf_counter()
+        n = 0
+        for _ in range(reps):
+            for h in self.heads:
+                x = W.as_float64(inp.K[0, T - 1:T, h], wl.in_dtype)
+                O.quantize(x, self.specs[h][0], O.norm_dtype_name(wl))
+                x = W.as_float64(inp.V[0, T - 1:T, h], wl.in_dtype)
+                O.quantize(x, self.specs[h][1], O.norm_dtype_name(wl))
+                ek, ev = self.encs[h]
+                oracle_attention(self.st, ek, ev, 0, h, T)
+                n += 1
+        return (time.perf_counter() - t0) / n
+
+
+def cpu_cores():
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(v):
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+def run_reference(args, wl, T, rank, world):
+    if rank != 0:
+        return
+    from rotated_bit_kv_gb300 import tq_cache_desc
+    d = tq_cache_desc()
+    d.k_code_bytes = d.v_code_bytes = 48
+    d.k_norm_slots = d.v_norm_slots = 1
+    d.norm_bytes = 2
+    sb = step_bytes(wl, T, d)
+    pairs_total = wl.batch * wl.n_kv_heads
+    leg = OracleLeg(wl, T, n_pairs=1)
+    for _ in range(args.warmup):
+        leg.seconds_per_pair()
+    times = []
+    for _ in range(args.steps):
+        times.append(leg.seconds_per_pair() * pairs_total)
+    step_s = statistics.mean(times)
+    val = sb["step"] / step_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "us_per_step": step_s * 1e6,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(wl, T), "parallelism": "replicas"},
+        "cpu_baseline": {"kind": "oracle", "value": val, "unit": "GB/s", "cores": cpu_cores(),
+                         "sample": f"per step: oracle encode of the new token + attention over T={T} for one "
+                                   f"(batch, KV head), scaled linearly to all {pairs_total} pairs"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+def run_ours(args, wl, T, rank, world, local_rank):
+    import torch
+
+    import rotated_bit_kv_gb300 as tq
+    from gpu_harness import make_setup, to_torch_input
+
+    tq.build()
+    lib = tq.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    inp = W.make_inputs(wl, seq_len=T)
+    st = make_setup(tq, wl, inp, T)
+    desc = st.desc
+    # two cache copies alternated between steps: each step reads ~210 MB, more
+    # than L2, and never the copy the previous step read
+    caches = [tq.PackedKVCache(desc, st.blob, device=dev) for _ in range(2)]
+    K = to_torch_input(torch, inp.K, wl.in_dtype, dev)
+    V = to_torch_input(torch, inp.V, wl.in_dtype, dev)
+    zero = torch.zeros(wl.batch, dtype=torch.int32, device=dev)
+    for c in caches:
+        c.append(K, V, zero)
+    torch.cuda.synchronize()
+    k_new = K[:, T - 1:T].contiguous()
+    v_new = V[:, T - 1:T].contiguous()
+    del K, V
+    q = to_torch_input(torch, inp.q, wl.in_dtype, dev)
+    start = torch.full((wl.batch,), T - 1, dtype=torch.int32, device=dev)
+    seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
+    out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    splits, vmode = tq.tq_decode_plan(desc, T)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    in_code = tq._dtype_code(q)
+    dref = ctypes.byref(desc)
+    pref = [ctypes.byref(c.ptrs) for c in caches]
+
+    def step(i, ev=None, qd=q, kd=k_new, vd=v_new, sd=start, ld=seq, od=out):
+        c = caches[i & 1]
+        st_ = lib.tq_quantize_append(dref, pref[i & 1], kd.data_ptr(), vd.data_ptr(), in_code, sd.data_ptr(), 1,
+                                     c.status.data_ptr(), sptr)
+        if ev is not None:
+            ev[0].record(stream)
+        st2 = lib.tq_decode_attention(dref, pref[i & 1], qd.data_ptr(), in_code, ld.data_ptr(), T, od.data_ptr(),
+                                      c.workspace.data_ptr(), c.workspace.numel(), c.status.data_ptr(), sptr)
+        if ev is not None:
+            ev[1].record(stream)
+        if st_ or st2:
+            raise RuntimeError(f"library error {st_} {st2}")
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_a.record(stream)
+    for i in range(args.steps):
+        step(i, kev[i])
+    t_b.record(stream)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = max_over_ranks(t_a.elapsed_time(t_b))
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    for c in caches:
+        if int(c.status.item()) != 0:
+            raise RuntimeError(f"device status {int(c.status.item())}")
+
+    # end to end through the C ABI with host buffers: pinned H2D of the step's
+    # inputs (q, new K/V token, positions, lengths) and D2H of the output
+    hq = q.cpu().pin_memory()
+    hk = k_new.cpu().pin_memory()
+    hv = v_new.cpu().pin_memory()
+    hs = start.cpu().pin_memory()
+    hl = seq.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv, ds, dl = (torch.empty_like(x) for x in (q, k_new, v_new, start, seq))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hs, hl))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step(i):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        step(i, None, dq, dk, dv, ds, dl, out)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_a.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e_b.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e_a.elapsed_time(e_b))
+
+    sb = step_bytes(wl, T, desc)
+    step_ms = elapsed_ms / args.steps
+    value = world * sb["step"] / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = sb["decode"] / (dec_ms * 1e-3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "us_per_step": step_ms * 1e3,
+        "pct_of_peak": 100.0 * (value / world) / peak, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_name(wl, T), "batch": wl.batch, "seq_len": T,
+                   "parallelism": "replicas" if world == 1 else f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.0f MB read per step vs 129 MB L2); two cache copies "
+                         "alternated between steps" % (sb["decode"] / 1e6),
+                   "decode_plan": {"splits": splits, "v_mode": vmode}},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(), "kernel": "decode attention",
+                     "us_per_launch": dec_ms * 1e3, "algorithmic_bytes_per_launch": sb["decode"],
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy kernel; spec ~7900)"},
+        "e2e": {"value": world * sb["step"] / (e2e_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+                "us_per_step": e2e_ms / args.steps * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        leg = OracleLeg(wl, T, n_pairs=2)
+        npairs = len(leg.heads)
+        dt = leg.seconds_per_pair(reps=4)
+        pairs_total = wl.batch * wl.n_kv_heads
+        cpu_step = dt * pairs_total
+        line["cpu_baseline"] = {
+            "kind": "oracle", "value": sb["step"] / cpu_step / 1e9, "unit": "GB/s", "cores": cpu_cores(),
+            "sample": f"oracle (fp64 NumPy) encode of the new token + attention over T={T} for {npairs} (batch, KV "
+                      f"head) pairs x4, scaled linearly to all {pairs_total} pairs"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seq-len", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = W.llama8b_decode(seq_len=args.seq_len)
+    if args.impl == "reference":
+        run_reference(args, wl, args.seq_len, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, wl, args.seq_len, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

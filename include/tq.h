@@ -1,0 +1,282 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) rotation-quantised KV cache library.
+ *
+ * The library implements one data-parallel hot path, in two halves:
+ *
+ *   write side  (tq_quantize_append): per K/V vector, L2 norm -> orthogonal
+ *               rotation -> per-coordinate Lloyd-Max codebook search -> 3/4-bit
+ *               packing into a caller-owned device cache;
+ *   read side   (tq_decode_attention): rotate q once, QK dot products on the
+ *               packed codes by codebook lookup, online softmax, V accumulation
+ *               in the rotated domain, log-sum-exp merge of key-axis splits, one
+ *               inverse rotation of the output.
+ *
+ * Sources, by page title (sections as printed on each page):
+ *   [TQ-MNN]      "TurboQuant: ... MNN runs it on the phone" (zhaode.wang blog)
+ *   [RotaryQuant] "RotaryQuant: Fitting 120B MoE Models on Consumer Hardware via
+ *                 Fused Compressed-Space Attention" (papernotes.org)
+ *   [Block-GTQ]   "RoPE-Aware Bit Allocation for KV-Cache Quantization" (aitrends.kr)
+ *
+ * Conventions shared by every entry point
+ *   - head_dim is 128.  q head g reads KV head g / (n_q_heads / n_kv_heads).
+ *   - Every pointer named d_* (and every pointer inside tq_cache_ptrs, q, out,
+ *     workspace) is DEVICE memory owned by the caller; the library never
+ *     allocates, frees or retains a pointer past the call.  Host pointers are
+ *     read during the call only.
+ *   - Device entry points are asynchronous and stream ordered on `stream` (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream).  They
+ *     return TQ_OK after a successful launch; argument errors that the host can
+ *     see are returned before anything is launched.  Conditions only the device
+ *     can see (a sequence length above the cache capacity, a write position
+ *     outside the cache) are clamped or skipped, never trapped, and OR a
+ *     TQ_DEV_* bit into *d_status when d_status is not NULL.
+ *   - The library keeps no global mutable state; calls on different streams
+ *     with disjoint buffers are independent.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+typedef int32_t tq_status;
+#define TQ_OK                  0
+#define TQ_ERR_INVALID_ARG     1  /* bad shape, pointer, enum or size          */
+#define TQ_ERR_UNSUPPORTED     2  /* valid but not built (e.g. head_dim != 128) */
+#define TQ_ERR_CUDA            3  /* a CUDA runtime call or launch failed       */
+#define TQ_ERR_NO_CONVERGENCE  4  /* the Lloyd-Max iteration did not converge   */
+#define TQ_ERR_WORKSPACE       5  /* workspace missing or smaller than required */
+
+/* bits OR-ed into the caller's device status word */
+#define TQ_DEV_SEQ_OVER_CAPACITY  1  /* seq_len > t_capacity: clamped          */
+#define TQ_DEV_SEQ_OVER_MAX       2  /* seq_len > max_seq_len: clamped         */
+#define TQ_DEV_BAD_POSITION       4  /* append position outside [0, capacity): skipped */
+
+/* ---------------------------------------------------------------- enums */
+#define TQ_F32   0
+#define TQ_F16   1
+#define TQ_BF16  2
+
+/* Rotation kinds.  R is orthogonal; rotated = R x.
+ *   WHT128      R = H_128 D, D = diag(+-1 signs)      [TQ-MNN §3.1]
+ *   WHT32       R = diag(H_32 D_k), k = 0..3, each block with its own norm
+ *                                                      [TQ-MNN §3.1, block_size = 32]
+ *   SO4_WHT128  R = S H_128, S = diag of 32 maps v -> q_L v conj(q_R)
+ *                                                      [RotaryQuant, Key design 2]
+ * Mixed-rate keys (k_mixed = 1) replace K's rotation by one random orthogonal
+ * matrix per same-width group of RoPE blocks [Block-GTQ, physical encoding and
+ * grouping]; V keeps `rot`. */
+#define TQ_ROT_WHT128      0
+#define TQ_ROT_WHT32       1
+#define TQ_ROT_SO4_WHT128  2
+
+/* parts of the cache, for tq_cache_bytes */
+#define TQ_PART_K_CODES  0
+#define TQ_PART_K_NORMS  1
+#define TQ_PART_V_CODES  2
+#define TQ_PART_V_NORMS  3
+#define TQ_PART_PARAMS   4
+
+/* V-accumulation strategies of the decode kernel [RotaryQuant, Key design 3:
+ * token ("word") parallel below a crossover length, dimension parallel above] */
+#define TQ_VMODE_AUTO            -1
+#define TQ_VMODE_TOKEN_PARALLEL   0
+#define TQ_VMODE_DIM_PARALLEL     1
+#define TQ_VMODE_TENSOR           2  /* dimension parallel on tensor cores */
+
+#define TQ_HEAD_DIM     128
+#define TQ_MAX_GROUP     16   /* maximum n_q_heads / n_kv_heads */
+#define TQ_MAX_SPLITS  1024   /* maximum key-axis splits per (batch, KV head) */
+
+/* ---------------------------------------------------------------- layout */
+/* Cache descriptor.  Filled by tq_cache_desc_init; treat as read-only.
+ *
+ * Device layout of the cache (all token-major per (batch, KV head)):
+ *   k_codes [batch][n_kv_heads][t_capacity][k_code_bytes]   uint8
+ *   k_norms [batch][n_kv_heads][t_capacity][k_norms]        norm_dtype
+ *   v_codes [batch][n_kv_heads][t_capacity][v_code_bytes]   uint8
+ *   v_norms [batch][n_kv_heads][t_capacity][v_norms]        norm_dtype
+ * A code record holds the 128 indices of one vector in rotated-coordinate
+ * order: 3-bit indices LSB first (index i at bits [3i, 3i+3) of the
+ * little-endian byte stream: 8 indices per 3 bytes, 48 B) or 4-bit indices
+ * two per byte (index 2j in the low nibble of byte j, 64 B) [TQ-MNN §3.3].
+ * Mixed-rate keys use the 4-bit container for every width (one index per
+ * nibble) with the groups in ascending bit width [Block-GTQ, packed cache].
+ * Norm slots: 1 (WHT128, SO4_WHT128), 4 (WHT32: one per 32-dim block) or 4
+ * (mixed-rate keys: slot b-1 holds the norm of the b-bit group, 0 if empty). */
+typedef struct tq_cache_desc {
+    int32_t head_dim;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t batch;
+    int32_t t_capacity;
+    int32_t rot;            /* TQ_ROT_* */
+    int32_t k_bits;         /* 3 or 4 (ignored when k_mixed) */
+    int32_t v_bits;         /* 3 or 4 */
+    int32_t norm_dtype;     /* TQ_F16 or TQ_F32 */
+    int32_t k_mixed;        /* 0 or 1 */
+    /* derived */
+    int32_t group;          /* n_q_heads / n_kv_heads */
+    int32_t k_code_bytes;
+    int32_t v_code_bytes;
+    int32_t k_norm_slots;
+    int32_t v_norm_slots;
+    int32_t norm_bytes;     /* 2 or 4 */
+    int64_t params_bytes;   /* size of the parameter blob (tq_params_build) */
+} tq_cache_desc;
+
+/* Device pointers of one cache (caller owned; see layout above).  `params` is
+ * a device copy of the blob written by tq_params_build; it must be 16-byte
+ * aligned. */
+typedef struct tq_cache_ptrs {
+    void* k_codes;
+    void* k_norms;
+    void* v_codes;
+    void* v_norms;
+    const void* params;
+} tq_cache_ptrs;
+
+/* ---------------------------------------------------------------- host API */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tq_status_string(tq_status s);
+
+/* Lloyd-Max codebook for one coordinate of a uniformly random point on the unit
+ * sphere in R^block_dim, density f(t) ~ (1 - t^2)^((block_dim-3)/2) on [-1, 1]
+ * [TQ-MNN §2.2], with 2^bits cells: each centroid is the conditional mean of
+ * its cell, each boundary the midpoint of its neighbours [TQ-MNN §2.3].
+ * Solved in fp64 on the host, returned rounded to fp32.
+ *   block_dim   2..4096 (128, 32, or a mixed-rate group width)
+ *   bits        1..4
+ *   centroids   host, 2^bits floats, ascending
+ *   boundaries  host, 2^bits - 1 floats (midpoints of the fp64 centroids)
+ * Errors: TQ_ERR_INVALID_ARG (range, NULL), TQ_ERR_NO_CONVERGENCE. */
+tq_status tq_codebook(int32_t block_dim, int32_t bits, float* centroids, float* boundaries);
+
+/* Block energy of each two-dimensional RoPE block i (coordinates 2i, 2i+1) for
+ * one KV head [Block-GTQ, block energy]:
+ *   s_i = 1/2 ( mean_{t, g} ||q_{g,t}^(i)||^2 + mean_t ||k_t^(i)||^2 ),
+ * over a calibration prefix of T tokens; g runs over the G query heads that
+ * read this KV head.
+ *   q_cal  host fp32 [T][G][head_dim];  k_cal host fp32 [T][head_dim]
+ *   s_out  host fp64 [head_dim / 2]
+ * Errors: TQ_ERR_INVALID_ARG. */
+tq_status tq_block_energy(const float* q_cal, const float* k_cal, int32_t T, int32_t G,
+                          int32_t head_dim, double* s_out);
+
+/* Greedy integer bit allocation [Block-GTQ, greedy allocation]: minimise
+ * J(b) = sum_i s_i 4^(-b_i) subject to b_min <= b_i <= b_max and
+ * sum_i b_i = B_total.  Every block starts at b_min; each remaining bit goes to
+ * the block with the largest marginal gain (3/4) s_i 4^(-b_i) among blocks below
+ * b_max (ties to the lowest index).
+ *   s      host fp64 [L] (s_i >= 0);  b_out host int32 [L]
+ * Errors: TQ_ERR_INVALID_ARG (NULL, L < 1, b_min > b_max, infeasible B_total). */
+tq_status tq_block_bit_alloc(const double* s, int32_t L, int32_t b_min, int32_t b_max,
+                             int32_t B_total, int32_t* b_out);
+
+/* Fill a cache descriptor and validate the shape.
+ * Errors: TQ_ERR_INVALID_ARG (non-positive sizes, n_q_heads not a multiple of
+ * n_kv_heads, bad enum), TQ_ERR_UNSUPPORTED (head_dim != 128, group >
+ * TQ_MAX_GROUP, bits outside {3, 4}, WHT32 or SO4 combined with k_mixed). */
+tq_status tq_cache_desc_init(tq_cache_desc* desc, int32_t head_dim, int32_t n_q_heads,
+                             int32_t n_kv_heads, int32_t batch, int32_t t_capacity,
+                             int32_t rot, int32_t k_bits, int32_t v_bits,
+                             int32_t norm_dtype, int32_t k_mixed);
+
+/* Bytes of one part of the cache (TQ_PART_*); 0 for an unknown part. */
+size_t tq_cache_bytes(const tq_cache_desc* desc, int32_t part);
+
+/* Build the parameter blob (rotation parameters and codebooks, per KV head)
+ * into host memory of desc->params_bytes bytes; the caller copies it to a
+ * 16-byte aligned device buffer and passes it as tq_cache_ptrs.params.  The
+ * random quantities of the method are inputs, drawn by the caller:
+ *   signs        host fp32 [n_kv][128], each +1 or -1 (WHT128, WHT32, and the
+ *                V rotation of mixed-rate caches); may be NULL for SO4_WHT128
+ *   quats        host fp32 [n_kv][32][2][4]: (q_L, q_R) unit quaternions
+ *                (w, x, y, z) per 4-dim block; required for SO4_WHT128
+ *   k_block_bits host int32 [n_kv][64]: bits of each RoPE block, 1..4; required
+ *                iff k_mixed
+ *   k_group_mats host fp32: for each KV head, for each width b = 1..4 whose
+ *                group is non-empty (n_b = 2 * #blocks), the n_b x n_b
+ *                row-major orthogonal matrix Pi_b, concatenated; required iff
+ *                k_mixed
+ * Codebooks are solved here (tq_codebook) for every (width, bits) in use.
+ * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_NO_CONVERGENCE. */
+tq_status tq_params_build(const tq_cache_desc* desc, const float* signs, const float* quats,
+                          const int32_t* k_block_bits, const float* k_group_mats,
+                          void* host_blob);
+
+/* ---------------------------------------------------------------- device API */
+
+/* Quantise and append n_new tokens of K and V per sequence [TQ-MNN §2.1 and
+ * §3.3 "in-place quantisation on write"; Block-GTQ: a whole prompt in one
+ * call].  For every (b, t, h) and both K and V: n = ||x|| per norm segment,
+ * y = R x / n, idx = #{k : y > boundary_k} (fp32 compares, ties to the lower
+ * cell) [TQ-MNN §3.4], pack, store the norm rounded to norm_dtype.
+ *   K, V         device [batch][n_new][n_kv_heads][128] of in_dtype
+ *   in_dtype     TQ_F32, TQ_F16 or TQ_BF16
+ *   d_start_pos  device int32 [batch]: token t goes to slot d_start_pos[b] + t;
+ *                slots outside [0, t_capacity) are skipped and flagged
+ *   n_new        >= 0 (0 is a no-op)
+ *   d_status     device int32 or NULL
+ * Errors: TQ_ERR_INVALID_ARG (NULL, misaligned, bad dtype), TQ_ERR_CUDA. */
+tq_status tq_quantize_append(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
+                             const void* K, const void* V, int32_t in_dtype,
+                             const int32_t* d_start_pos, int32_t n_new,
+                             int32_t* d_status, void* stream);
+
+/* Workspace bytes tq_decode_attention needs for at most max_splits key-axis
+ * splits: partial (m, l, o~) per (batch, q head, split) plus one ticket per
+ * (batch, KV head).  The ticket words must be zero before the first call on a
+ * workspace (e.g. a cudaMemset of the whole buffer); every call leaves them
+ * zero again. */
+size_t tq_decode_workspace_bytes(const tq_cache_desc* desc, int32_t max_splits);
+
+/* One decode step of attention on the packed cache [RotaryQuant, Key design 3;
+ * TQ-MNN §3.3 K path and V path; Block-GTQ key-axis split with log-sum-exp
+ * merge].  For each batch b and q head g of KV head h:
+ *   q~ = R_K q;  s_j = sum_seg n_{j,seg} <q~_seg, C_seg[idx_{j,seg}]> / sqrt(128)
+ *   a = softmax(s) over j < seq_len_b;  o~ = sum_j a_j v~_j;  o = R_V^T o~.
+ *   q            device [batch][n_q_heads][128] of q_dtype (TQ_F32/F16/BF16)
+ *   d_seq_lens   device int32 [batch]; clamped to [0, min(t_capacity,
+ *                max_seq_len)] with TQ_DEV_* flags; seq_len 0 gives o = 0
+ *   max_seq_len  host upper bound of d_seq_lens, 1..t_capacity; sizes the
+ *                key-axis splits and picks the V-accumulation mode
+ *   out          device fp32 [batch][n_q_heads][128]
+ *   workspace    device, >= tq_decode_workspace_bytes(desc, splits used); the
+ *                splits used are at most TQ_MAX_SPLITS and at most
+ *                ceil(max_seq_len / 64)
+ *   d_status     device int32 or NULL
+ * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_decode_attention(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
+                              const void* q, int32_t q_dtype, const int32_t* d_seq_lens,
+                              int32_t max_seq_len, float* out, void* workspace,
+                              size_t workspace_bytes, int32_t* d_status, void* stream);
+
+/* tq_decode_attention with explicit choices, for tests and tuning:
+ *   v_mode    TQ_VMODE_* (AUTO picks token parallel below the crossover length,
+ *             the tensor-core path where the format supports it, otherwise
+ *             dimension parallel)
+ *   n_splits  key-axis splits per (batch, KV head), 1..TQ_MAX_SPLITS, or 0 for
+ *             the automatic choice
+ * Errors: as tq_decode_attention; TQ_ERR_UNSUPPORTED if v_mode is TENSOR and
+ * the cache format has no tensor-core kernel. */
+tq_status tq_decode_attention_ex(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
+                                 const void* q, int32_t q_dtype, const int32_t* d_seq_lens,
+                                 int32_t max_seq_len, float* out, void* workspace,
+                                 size_t workspace_bytes, int32_t* d_status, void* stream,
+                                 int32_t v_mode, int32_t n_splits);
+
+/* The splits and V mode tq_decode_attention would use (host only). */
+tq_status tq_decode_plan(const tq_cache_desc* desc, int32_t max_seq_len, int32_t v_mode,
+                         int32_t n_splits, int32_t* splits_out, int32_t* v_mode_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H_ */

@@ -1,0 +1,673 @@
+// Read side: decode attention computed on the packed codes.
+//
+// [RotaryQuant] Key design 3: rotate q once (<Rq, Rk> = q^T k), QK dot products
+// and V accumulation on the packed codes in on-chip registers, one inverse
+// rotation of the output (o~ = R o); V accumulation token ("word") parallel for
+// short contexts, dimension parallel for long ones.  [TQ-MNN] §3.3: K path in
+// the rotated domain (q rotated once per head, unpack + codebook lookup +
+// multiply-add per key), V path accumulated in the rotated domain with one
+// inverse WHT.  [Block-GTQ]: long contexts split along the key axis, sections
+// merged by log-sum-exp.
+//
+// Grid: (split, KV head, batch); 128 threads.  Each CTA rotates the G query
+// heads of its KV head into shared memory, streams its section of the cache,
+// and leaves a partial (m, l, o~) per query head.  The last CTA of a (batch,
+// KV head) to finish -- found with an atomic ticket, no spinning -- merges the
+// sections and applies R_V^T.
+#include <stdlib.h>
+
+#include "tq_device.cuh"
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
+constexpr int kPartStride = 132;                      // 128 (o~) + m + l, 16-byte rows
+
+struct DecodeArgs {
+    const uint8_t* k_codes;
+    const void* k_norms;
+    const uint8_t* v_codes;
+    const void* v_norms;
+    const tq_head_params* params;
+    const float* kmat;
+    const void* q;
+    const int32_t* seq_lens;
+    float* out;
+    float* ws_part;
+    int32_t* tickets;
+    int32_t* status;
+    int B, Hq, Hkv, G, Tcap, max_seq, n_splits, split_len, q_dtype, norm_f16, rot, k_mixed;
+};
+
+template <int F> struct Fmt {
+    static constexpr bool three = (F == TQ_FMT_ONE3 || F == TQ_FMT_BLK3);
+    static constexpr int bytes = three ? 48 : 64;
+    static constexpr int words = bytes / 4;
+    static constexpr int nslots = (F == TQ_FMT_ONE3 || F == TQ_FMT_ONE4) ? 1 : 4;
+    static constexpr bool blk = (F == TQ_FMT_BLK3 || F == TQ_FMT_BLK4);
+    static constexpr bool mix = (F == TQ_FMT_MIX4);
+};
+
+// index of code c (compile-time in unrolled loops) from a record in registers
+template <bool THREE>
+__device__ __forceinline__ uint32_t code_at(const uint32_t* w, int c) {
+    if (THREE) {
+        const int bit = 3 * c, wi = bit >> 5, sh = bit & 31;
+        if (sh <= 29) return (w[wi] >> sh) & 7u;
+        return __funnelshift_r(w[wi], w[wi + 1], sh) & 7u;
+    }
+    return (w[c >> 3] >> (4 * (c & 7))) & 15u;
+}
+
+template <int F>
+__device__ __forceinline__ void load_record(const uint8_t* base, size_t tok, uint32_t* w) {
+    const uint4* p = reinterpret_cast<const uint4*>(base + tok * Fmt<F>::bytes);
+#pragma unroll
+    for (int i = 0; i < Fmt<F>::words / 4; ++i) {
+        uint4 u = __ldg(p + i);
+        w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+    }
+}
+
+template <int F>
+__device__ __forceinline__ void load_norms(const void* base, size_t tok, int norm_f16, float* n) {
+    if (Fmt<F>::nslots == 1) {
+        n[0] = tq::load_norm(base, tok, norm_f16);
+    } else if (norm_f16) {
+        uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(base) + tok * 4));
+        float2 a = __half22float2(*reinterpret_cast<__half2*>(&u.x));
+        float2 b = __half22float2(*reinterpret_cast<__half2*>(&u.y));
+        n[0] = a.x; n[1] = a.y; n[2] = b.x; n[3] = b.y;
+    } else {
+        float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + tok * 4));
+        n[0] = f.x; n[1] = f.y; n[2] = f.z; n[3] = f.w;
+    }
+}
+
+template <int GP>
+__device__ __forceinline__ void load_row(const float* row, float* q) {
+    if (GP % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < GP / 4; ++i) {
+            float4 v = reinterpret_cast<const float4*>(row)[i];
+            q[4 * i] = v.x; q[4 * i + 1] = v.y; q[4 * i + 2] = v.z; q[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < GP; ++i) q[i] = row[i];
+    }
+}
+
+// s_g = sum over segments of n_seg * sum_c q~_g[c] C_seg[idx_c]   (log2 units:
+// q~ already carries log2(e) / sqrt(d))
+template <int GP, int KF>
+__device__ __forceinline__ void qk_token(const uint32_t* rec, const float* nrm, const float (*qt)[GP],
+                                         const float (*kcb)[16], const uint8_t* kseg_of, float* sc) {
+    using K = Fmt<KF>;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) sc[g] = 0.f;
+    if (K::mix) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+            const int s = kseg_of[c];
+            float n = nrm[0];
+            n = s == 1 ? nrm[1] : n;
+            n = s == 2 ? nrm[2] : n;
+            n = s == 3 ? nrm[3] : n;
+            const float v = kcb[s][code_at<false>(rec, c)] * n;
+            float q[GP];
+            load_row<GP>(qt[c], q);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) sc[g] = fmaf(v, q[g], sc[g]);
+        }
+    } else {
+        constexpr int nseg = K::blk ? 4 : 1;
+        constexpr int len = 128 / nseg;
+#pragma unroll
+        for (int s = 0; s < nseg; ++s) {
+            float part[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) part[g] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < len; ++cc) {
+                const int c = s * len + cc;
+                const float v = kcb[s][code_at<K::three>(rec, c)];
+                float q[GP];
+                load_row<GP>(qt[c], q);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) part[g] = fmaf(v, q[g], part[g]);
+            }
+#pragma unroll
+            for (int g = 0; g < GP; ++g) sc[g] = fmaf(nrm[s], part[g], sc[g]);
+        }
+    }
+}
+
+template <int GP, int KF, int VF>
+struct Smem {
+    alignas(16) float qt[128][GP];
+    alignas(16) float kcb[4][16];
+    alignas(16) float vcb[4][16];
+    alignas(16) float xs[4][128];     // per-warp staging for the dense key rotation of q
+    alignas(16) float red[4][GP];
+    alignas(16) float red2[4][GP];
+    alignas(16) uint8_t kseg_of[128];
+    int is_last;
+};
+
+// Prologue shared by both modes: codebooks, q~ = R_K q (scaled to log2 units).
+template <int GP, int KF, int VF>
+__device__ __forceinline__ void prologue(const DecodeArgs& a, const tq_head_params& P, Smem<GP, KF, VF>& S,
+                                         int b, int h) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 64) {
+        S.kcb[tid >> 4][tid & 15] = P.k_cent[tid >> 4][tid & 15];
+        S.vcb[tid >> 4][tid & 15] = P.v_cent[tid >> 4][tid & 15];
+    }
+    if (Fmt<KF>::mix) {
+        int s = 0;
+        while (s < 3 && tid >= P.k_seg_start[s + 1]) ++s;
+        S.kseg_of[tid] = (uint8_t)s;
+    }
+    for (int g = warp; g < GP; g += 4) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (g < a.G) {
+            const size_t elem = ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128 + 4 * lane;
+            tq::load4(a.q, elem, a.q_dtype, v);
+            if (Fmt<KF>::mix) {
+                float* xs = S.xs[warp];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xs[4 * lane + i] = v[i];
+                __syncwarp();
+                tq::rotate_forward_dense(P, a.kmat + (size_t)h * 128 * 128, xs, v);
+                __syncwarp();
+            } else {
+                tq::rotate_forward(a.rot, P, v);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S.qt[4 * lane + i][g] = v[i] * (kLog2e * kInvSqrtD);
+    }
+}
+
+// Clamp the sequence length and flag what was clamped.
+__device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
+    int L = a.seq_lens[b];
+    int flags = 0;
+    if (L > a.Tcap) { flags |= TQ_DEV_SEQ_OVER_CAPACITY; L = a.Tcap; }
+    if (L > a.max_seq) { flags |= TQ_DEV_SEQ_OVER_MAX; L = a.max_seq; }
+    if (L < 0) L = 0;
+    if (flags && a.status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.status, flags);  // once per batch
+    return L;
+}
+
+// Epilogue: `ot[g][c]` holds this CTA's unnormalised o~, (m[g], l[g]) its
+// softmax state (identical in every thread).  Either finalise directly (one
+// split) or publish the partial and let the last CTA merge.
+template <int GP>
+__device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const float* m,
+                         const float* l, int* is_last, int b, int h, int s) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (a.n_splits > 1) {
+        float* part = a.ws_part + ((((size_t)b * a.Hkv + h) * a.n_splits + s) * GP) * kPartStride;
+        for (int i = tid; i < GP * 128; i += kThreads) part[(i >> 7) * kPartStride + (i & 127)] = ot[i >> 7][i & 127];
+        if (tid < GP) {
+            part[tid * kPartStride + 128] = m[tid];
+            part[tid * kPartStride + 129] = l[tid];
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const int ticket = atomicAdd(a.tickets + (size_t)b * a.Hkv + h, 1);
+            *is_last = ticket == a.n_splits - 1;
+        }
+        __syncthreads();
+        if (!*is_last) return;
+        __threadfence();
+        // log-sum-exp merge over the splits  [Block-GTQ]
+        const float* base = a.ws_part + (((size_t)b * a.Hkv + h) * a.n_splits * GP) * kPartStride;
+        for (int g = 0; g < GP; ++g) {
+            float M = -INFINITY;
+            for (int t = 0; t < a.n_splits; ++t) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
+            float lsum = 0.f, o = 0.f;
+            if (M != -INFINITY) {
+                for (int t = 0; t < a.n_splits; ++t) {
+                    const float* pr = base + ((size_t)t * GP + g) * kPartStride;
+                    const float mt = __ldcg(pr + 128);
+                    if (mt == -INFINITY) continue;
+                    const float w = exp2f(mt - M);
+                    lsum = fmaf(w, __ldcg(pr + 129), lsum);
+                    o = fmaf(w, __ldcg(pr + tid), o);
+                }
+            }
+            __syncthreads();
+            ot[g][tid] = lsum > 0.f ? o / lsum : 0.f;
+        }
+        if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
+        __syncthreads();
+    } else {
+        for (int i = tid; i < GP * 128; i += kThreads) {
+            const int g = i >> 7;
+            ot[g][i & 127] = l[g] > 0.f ? ot[g][i & 127] / l[g] : 0.f;
+        }
+        __syncthreads();
+    }
+    // o = R_V^T o~, once per query head  [RotaryQuant Key design 3, Kernel D]
+    for (int g = warp; g < a.G; g += 4) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ot[g][4 * lane + i];
+        tq::rotate_inverse(a.rot, P, v);
+        float4* o4 = reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128) + lane;
+        *o4 = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dimension-parallel V accumulation: per tile of 128 tokens, thread t computes
+// the logits of token t (token parallel QK); the tile's V codes are staged in
+// shared memory and thread c accumulates dimension c of o~ for every head.
+template <int GP, int KF, int VF>
+struct SmemDP {
+    Smem<GP, KF, VF> s;
+    alignas(16) float psm[128][GP];
+    alignas(16) float vns[128][4];
+    alignas(16) uint32_t vtile[128 * Fmt<VF>::words];
+    alignas(16) float ot[GP][128];
+};
+
+template <int GP, int KF, int VF>
+__global__ void __launch_bounds__(kThreads) decode_dp(DecodeArgs a) {
+    using KFm = Fmt<KF>;
+    using VFm = Fmt<VF>;
+    __shared__ __align__(16) SmemDP<GP, KF, VF> S;
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const tq_head_params& P = a.params[h];
+    const int L = clamp_len(a, b);
+    const int t0 = s * a.split_len;
+    const int t1 = min(t0 + a.split_len, L);
+    prologue<GP, KF, VF>(a, P, S.s, b, h);
+    __syncthreads();
+
+    const size_t head_tok = ((size_t)b * a.Hkv + h) * a.Tcap;
+    float m_run[GP], l_part[GP], acc[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) { m_run[g] = -INFINITY; l_part[g] = 0.f; acc[g] = 0.f; }
+    const int c = tid;
+    const int vseg = VFm::blk ? (c >> 5) : 0;
+    const int vbit = VFm::three ? 3 * c : 4 * c;
+    const int vwi = vbit >> 5, vsh = vbit & 31;
+    const int vwi1 = vwi + 1 < VFm::words ? vwi + 1 : vwi;
+
+    for (int tile = t0; tile < t1; tile += kThreads) {
+        const int nvalid = min(kThreads, t1 - tile);
+        const int j = tile + tid;
+        const bool valid = tid < nvalid;
+        float sc[GP];
+        float vn[4] = {1.f, 1.f, 1.f, 1.f};
+        if (valid) {
+            uint32_t rec[KFm::words];
+            float kn[4];
+            load_record<KF>(a.k_codes, head_tok + j, rec);
+            load_norms<KF>(a.k_norms, head_tok + j, a.norm_f16, kn);
+            qk_token<GP, KF>(rec, kn, S.s.qt, S.s.kcb, S.s.kseg_of, sc);
+            load_norms<VF>(a.v_norms, head_tok + j, a.norm_f16, vn);
+        } else {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) sc[g] = -INFINITY;
+        }
+        // stage the tile's V codes (contiguous records), 16-byte copies
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(a.v_codes + (head_tok + tile) * VFm::bytes);
+            uint4* dst = reinterpret_cast<uint4*>(S.vtile);
+            const int n16 = nvalid * (VFm::bytes / 16);
+            for (int i = tid; i < n16; i += kThreads) dst[i] = __ldg(src + i);
+        }
+        // tile max per head
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float wm = tq::warp_max(sc[g]);
+            if (lane == 0) S.s.red[warp][g] = wm;
+        }
+        __syncthreads();
+        float corr[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float tm = fmaxf(fmaxf(S.s.red[0][g], S.s.red[1][g]), fmaxf(S.s.red[2][g], S.s.red[3][g]));
+            const float mn = fmaxf(m_run[g], tm);
+            corr[g] = m_run[g] == -INFINITY ? 0.f : exp2f(m_run[g] - mn);
+            const float p = valid ? exp2f(sc[g] - mn) : 0.f;
+            l_part[g] = fmaf(l_part[g], corr[g], p);
+            m_run[g] = mn;
+            S.psm[tid][g] = VFm::nslots == 1 ? p * vn[0] : p;
+        }
+        if (VFm::nslots == 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) S.vns[tid][k] = vn[k];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int g = 0; g < GP; ++g) acc[g] *= corr[g];
+        const float* cb = S.s.vcb[vseg];
+        for (int jj = 0; jj < nvalid; ++jj) {
+            const uint32_t* vr = S.vtile + jj * VFm::words;
+            uint32_t idx;
+            if (VFm::three) idx = __funnelshift_r(vr[vwi], vr[vwi1], vsh) & 7u;
+            else idx = (vr[vwi] >> vsh) & 15u;
+            float v = cb[idx];
+            if (VFm::nslots == 4) v *= S.vns[jj][vseg];
+            float p[GP];
+            load_row<GP>(S.psm[jj], p);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) acc[g] = fmaf(p[g], v, acc[g]);
+        }
+        __syncthreads();
+    }
+    // l = sum over threads of l_part
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        const float ws = tq::warp_sum(l_part[g]);
+        if (lane == 0) S.s.red2[warp][g] = ws;
+    }
+#pragma unroll
+    for (int g = 0; g < GP; ++g) S.ot[g][c] = acc[g];
+    __syncthreads();
+    float lt[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) lt[g] = S.s.red2[0][g] + S.s.red2[1][g] + S.s.red2[2][g] + S.s.red2[3][g];
+    epilogue<GP>(a, P, S.ot, m_run, lt, &S.s.is_last, b, h, s);
+}
+
+// ---------------------------------------------------------------------------
+// Token-parallel V accumulation: each warp streams its own tokens (token j of
+// the section goes to warp (j / 32) % 4, lane j % 32) with its own online
+// softmax state; lane t adds p * v~ of its token into the warp's accumulator
+// at positions staggered by lane (conflict-free, no atomics).  Warps merge by
+// log-sum-exp once, at the end.  No CTA-wide barrier inside the loop.
+template <int GP, int VF>
+struct VRow { static constexpr int stride = (Fmt<VF>::words + 4) | 1; };
+
+template <int GP, int KF, int VF>
+struct SmemTP {
+    Smem<GP, KF, VF> s;
+    alignas(16) uint32_t vrec[4][32][VRow<GP, VF>::stride];
+    alignas(16) float oacc[4][128][GP];
+    alignas(16) float wm[4][GP];
+    alignas(16) float wl[4][GP];
+    alignas(16) float ot[GP][128];
+};
+
+template <int GP, int KF, int VF>
+__global__ void __launch_bounds__(kThreads) decode_tp(DecodeArgs a) {
+    using KFm = Fmt<KF>;
+    using VFm = Fmt<VF>;
+    __shared__ __align__(16) SmemTP<GP, KF, VF> S;
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const tq_head_params& P = a.params[h];
+    const int L = clamp_len(a, b);
+    const int t0 = s * a.split_len;
+    const int t1 = min(t0 + a.split_len, L);
+    prologue<GP, KF, VF>(a, P, S.s, b, h);
+    for (int i = lane; i < 128 * GP; i += 32) (&S.oacc[warp][0][0])[i] = 0.f;
+    __syncthreads();
+
+    const size_t head_tok = ((size_t)b * a.Hkv + h) * a.Tcap;
+    float m_run[GP], l_part[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) { m_run[g] = -INFINITY; l_part[g] = 0.f; }
+    uint32_t* myrow = S.vrec[warp][lane];
+    float(*oacc)[GP] = S.oacc[warp];
+
+    for (int base = t0 + warp * 32; base < t1; base += 4 * 32) {
+        const int j = base + lane;
+        const bool valid = j < t1;
+        float sc[GP];
+        if (valid) {
+            uint32_t rec[KFm::words];
+            float kn[4];
+            load_record<KF>(a.k_codes, head_tok + j, rec);
+            load_norms<KF>(a.k_norms, head_tok + j, a.norm_f16, kn);
+            qk_token<GP, KF>(rec, kn, S.s.qt, S.s.kcb, S.s.kseg_of, sc);
+            uint32_t vr[VFm::words];
+            float vn[4] = {1.f, 1.f, 1.f, 1.f};
+            load_record<VF>(a.v_codes, head_tok + j, vr);
+            load_norms<VF>(a.v_norms, head_tok + j, a.norm_f16, vn);
+#pragma unroll
+            for (int i = 0; i < VFm::words; ++i) myrow[i] = vr[i];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) myrow[VFm::words + k] = __float_as_uint(vn[k]);
+        } else {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) sc[g] = -INFINITY;
+            // an idle lane contributes exact zeros (code 0 times norm 0, p = 0)
+#pragma unroll
+            for (int i = 0; i < VFm::words + 4; ++i) myrow[i] = 0u;
+        }
+        float p[GP], corr[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float mn = fmaxf(m_run[g], tq::warp_max(sc[g]));
+            corr[g] = m_run[g] == -INFINITY ? 0.f : exp2f(m_run[g] - mn);
+            p[g] = valid ? exp2f(sc[g] - mn) : 0.f;
+            l_part[g] = fmaf(l_part[g], corr[g], p[g]);
+            m_run[g] = mn;
+        }
+        __syncwarp();
+        // rescale this warp's accumulator (lane-strided rows)
+        for (int r = lane; r < 128; r += 32) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) oacc[r][g] *= corr[g];
+        }
+        __syncwarp();
+        {
+            // every lane runs the same 128 steps; at step k lane l updates row
+            // (k + l) mod 128, so the 32 rows touched in one step are distinct
+            // and the barrier per step keeps steps from overlapping
+            const float vn0 = __uint_as_float(myrow[VFm::words]);
+            float pv[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) pv[g] = VFm::nslots == 1 ? p[g] * vn0 : p[g];
+            for (int k = 0; k < 128; ++k) {
+                const int cpos = (k + lane) & 127;
+                uint32_t idx;
+                if (VFm::three) {
+                    const int bit = 3 * cpos, wi = bit >> 5, sh = bit & 31;
+                    const int wi1 = wi + 1 < VFm::words ? wi + 1 : wi;
+                    idx = __funnelshift_r(myrow[wi], myrow[wi1], sh) & 7u;
+                } else {
+                    idx = (myrow[cpos >> 3] >> (4 * (cpos & 7))) & 15u;
+                }
+                const int sg = VFm::blk ? (cpos >> 5) : 0;
+                float v = S.s.vcb[sg][idx];
+                if (VFm::nslots == 4) v *= __uint_as_float(myrow[VFm::words + sg]);
+                float o[GP];
+                load_row<GP>(oacc[cpos], o);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) o[g] = fmaf(pv[g], v, o[g]);
+                if (GP % 4 == 0) {
+#pragma unroll
+                    for (int i = 0; i < GP / 4; ++i)
+                        reinterpret_cast<float4*>(oacc[cpos])[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) oacc[cpos][g] = o[g];
+                }
+                __syncwarp();
+            }
+        }
+        __syncwarp();
+    }
+    // warp states -> CTA state (log-sum-exp over the four warps)
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        const float lw = tq::warp_sum(l_part[g]);
+        if (lane == 0) { S.wm[warp][g] = m_run[g]; S.wl[warp][g] = lw; }
+    }
+    __syncthreads();
+    float M[GP], Lt[GP], w[4][GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        M[g] = fmaxf(fmaxf(S.wm[0][g], S.wm[1][g]), fmaxf(S.wm[2][g], S.wm[3][g]));
+        Lt[g] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w[k][g] = (M[g] == -INFINITY || S.wm[k][g] == -INFINITY) ? 0.f : exp2f(S.wm[k][g] - M[g]);
+            Lt[g] = fmaf(w[k][g], S.wl[k][g], Lt[g]);
+        }
+    }
+    const int c = tid;
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+        S.ot[g][c] = w[0][g] * S.oacc[0][c][g] + w[1][g] * S.oacc[1][c][g] + w[2][g] * S.oacc[2][c][g] +
+                     w[3][g] * S.oacc[3][c][g];
+    __syncthreads();
+    epilogue<GP>(a, P, S.ot, M, Lt, &S.s.is_last, b, h, s);
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+typedef void (*KernelFn)(DecodeArgs);
+
+template <int GP, int KF, int VF>
+KernelFn pick_mode(int mode) {
+    if constexpr (GP <= 8) {
+        if (mode == TQ_VMODE_TOKEN_PARALLEL) return decode_tp<GP, KF, VF>;
+    }
+    return decode_dp<GP, KF, VF>;
+}
+
+template <int GP>
+KernelFn pick_fmt(int kf, int vf, int mode) {
+    if (kf == TQ_FMT_ONE3 && vf == TQ_FMT_ONE3) return pick_mode<GP, TQ_FMT_ONE3, TQ_FMT_ONE3>(mode);
+    if (kf == TQ_FMT_ONE4 && vf == TQ_FMT_ONE4) return pick_mode<GP, TQ_FMT_ONE4, TQ_FMT_ONE4>(mode);
+    if (kf == TQ_FMT_BLK3 && vf == TQ_FMT_BLK3) return pick_mode<GP, TQ_FMT_BLK3, TQ_FMT_BLK3>(mode);
+    if (kf == TQ_FMT_BLK4 && vf == TQ_FMT_BLK4) return pick_mode<GP, TQ_FMT_BLK4, TQ_FMT_BLK4>(mode);
+    if (kf == TQ_FMT_MIX4 && vf == TQ_FMT_ONE3) return pick_mode<GP, TQ_FMT_MIX4, TQ_FMT_ONE3>(mode);
+    if (kf == TQ_FMT_MIX4 && vf == TQ_FMT_ONE4) return pick_mode<GP, TQ_FMT_MIX4, TQ_FMT_ONE4>(mode);
+    return nullptr;
+}
+
+KernelFn pick_kernel(int G, int kf, int vf, int mode, int* GP) {
+    if (G <= 1) { *GP = 1; return pick_fmt<1>(kf, vf, mode); }
+    if (G <= 4) { *GP = 4; return pick_fmt<4>(kf, vf, mode); }
+    if (G <= 8) { *GP = 8; return pick_fmt<8>(kf, vf, mode); }
+    *GP = 16;
+    return pick_fmt<16>(kf, vf, mode);
+}
+
+int padded_group(int G) { return G <= 1 ? 1 : G <= 4 ? 4 : G <= 8 ? 8 : 16; }
+
+bool aligned(const void* p, size_t n) { return ((uintptr_t)p % n) == 0; }
+
+constexpr int kSMs = 152;
+
+}  // namespace
+
+extern "C" {
+
+size_t tq_decode_workspace_bytes(const tq_cache_desc* d, int32_t max_splits) {
+    if (!d || d->head_dim != TQ_HEAD_DIM || max_splits < 1) return 0;
+    if (max_splits > TQ_MAX_SPLITS) max_splits = TQ_MAX_SPLITS;
+    const size_t pairs = (size_t)d->batch * d->n_kv_heads;
+    const size_t part = pairs * (size_t)max_splits * padded_group(d->group) * kPartStride * sizeof(float);
+    const size_t tick = ((pairs * sizeof(int32_t)) + 255) & ~(size_t)255;
+    return tick + part;
+}
+
+tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_mode, int32_t n_splits,
+                         int32_t* splits_out, int32_t* v_mode_out) {
+    if (!d || d->head_dim != TQ_HEAD_DIM || max_seq_len < 1 || max_seq_len > d->t_capacity) return TQ_ERR_INVALID_ARG;
+    if (v_mode < TQ_VMODE_AUTO || v_mode > TQ_VMODE_TENSOR) return TQ_ERR_INVALID_ARG;
+    if (n_splits < 0 || n_splits > TQ_MAX_SPLITS) return TQ_ERR_INVALID_ARG;
+    int mode = v_mode;
+    if (mode == TQ_VMODE_AUTO) mode = max_seq_len < tq_v_crossover() ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
+    if (mode == TQ_VMODE_TENSOR) return TQ_ERR_UNSUPPORTED;
+    int splits = n_splits;
+    if (splits == 0) {
+        // fill the GPU: about four resident 128-thread CTAs per SM, sections of
+        // at least 64 tokens
+        const long long pairs = (long long)d->batch * d->n_kv_heads;
+        const long long target = 4LL * kSMs;
+        long long sp = (target + pairs - 1) / pairs;
+        const long long cap = (max_seq_len + 63) / 64;
+        if (sp > cap) sp = cap;
+        if (sp < 1) sp = 1;
+        if (sp > TQ_MAX_SPLITS) sp = TQ_MAX_SPLITS;
+        splits = (int)sp;
+    }
+    if (splits_out) *splits_out = splits;
+    if (v_mode_out) *v_mode_out = mode;
+    return TQ_OK;
+}
+
+tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,
+                                 const int32_t* d_seq_lens, int32_t max_seq_len, float* out, void* workspace,
+                                 size_t workspace_bytes, int32_t* d_status, void* stream, int32_t v_mode,
+                                 int32_t n_splits) {
+    if (!d || !c || d->head_dim != TQ_HEAD_DIM) return TQ_ERR_INVALID_ARG;
+    if (!q || !d_seq_lens || !out || !c->k_codes || !c->k_norms || !c->v_codes || !c->v_norms || !c->params)
+        return TQ_ERR_INVALID_ARG;
+    if (q_dtype != TQ_F32 && q_dtype != TQ_F16 && q_dtype != TQ_BF16) return TQ_ERR_INVALID_ARG;
+    const size_t qa = q_dtype == TQ_F32 ? 16 : 8;
+    if (!aligned(q, qa) || !aligned(out, 16) || !aligned(c->k_codes, 16) || !aligned(c->v_codes, 16) ||
+        !aligned(c->params, 16) || !aligned(c->k_norms, 16) || !aligned(c->v_norms, 16))
+        return TQ_ERR_INVALID_ARG;
+    int splits = 0, mode = 0;
+    tq_status st = tq_decode_plan(d, max_seq_len, v_mode, n_splits, &splits, &mode);
+    if (st != TQ_OK) return st;
+    const int kf = tq_k_fmt(d), vf = tq_v_fmt(d);
+    int GP = 1;
+    KernelFn fn = pick_kernel(d->group, kf, vf, mode, &GP);
+    if (!fn) return TQ_ERR_UNSUPPORTED;
+    DecodeArgs a;
+    a.k_codes = static_cast<const uint8_t*>(c->k_codes);
+    a.k_norms = c->k_norms;
+    a.v_codes = static_cast<const uint8_t*>(c->v_codes);
+    a.v_norms = c->v_norms;
+    a.params = static_cast<const tq_head_params*>(c->params);
+    a.kmat = reinterpret_cast<const float*>(static_cast<const char*>(c->params) +
+                                            (size_t)d->n_kv_heads * sizeof(tq_head_params));
+    a.q = q;
+    a.seq_lens = d_seq_lens;
+    a.out = out;
+    a.status = d_status;
+    a.tickets = nullptr;
+    a.ws_part = nullptr;
+    if (splits > 1) {
+        const size_t need = tq_decode_workspace_bytes(d, splits);
+        if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TQ_ERR_WORKSPACE;
+        const size_t pairs = (size_t)d->batch * d->n_kv_heads;
+        const size_t tick = ((pairs * sizeof(int32_t)) + 255) & ~(size_t)255;
+        a.tickets = static_cast<int32_t*>(workspace);
+        a.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + tick);
+    }
+    a.B = d->batch;
+    a.Hq = d->n_q_heads;
+    a.Hkv = d->n_kv_heads;
+    a.G = d->group;
+    a.Tcap = d->t_capacity;
+    a.max_seq = max_seq_len;
+    a.n_splits = splits;
+    a.split_len = (max_seq_len + splits - 1) / splits;
+    a.q_dtype = q_dtype;
+    a.norm_f16 = d->norm_dtype == TQ_F16;
+    a.rot = d->rot;
+    a.k_mixed = d->k_mixed;
+    dim3 grid(splits, d->n_kv_heads, d->batch);
+    if (d->batch > 65535 || d->n_kv_heads > 65535) return TQ_ERR_INVALID_ARG;
+    fn<<<grid, kThreads, 0, (cudaStream_t)stream>>>(a);
+    return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+tq_status tq_decode_attention(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,
+                              const int32_t* d_seq_lens, int32_t max_seq_len, float* out, void* workspace,
+                              size_t workspace_bytes, int32_t* d_status, void* stream) {
+    return tq_decode_attention_ex(d, c, q, q_dtype, d_seq_lens, max_seq_len, out, workspace, workspace_bytes,
+                                  d_status, stream, TQ_VMODE_AUTO, 0);
+}
+
+}  // extern "C"

@@ -27,3 +27,12 @@ def read_golden_kv(name):
             k, *v = line.split()
             out[k] = v
     return out
+
+
+@pytest.fixture(scope="session")
+def tqlib():
+    """The built library (compiled here if missing or stale)."""
+    import rotated_bit_kv_gb300 as tq
+    tq.build()
+    tq.lib()
+    return tq

@@ -1,0 +1,277 @@
+"""GPU parity of the CUDA path against the fp64 oracle, through the C ABI.
+
+Write side: the kernel's packed codes must equal the oracle's except at
+coordinates whose normalised rotated value lies within 1e-5 of a decision
+boundary; those mismatches must be at most 1e-4 of all codes.  Stored norms
+must be equal or adjacent fp16 values (fp32: within 4e-7 relative).
+
+Read side: the oracle's packed cache is uploaded into the device cache and the
+kernel's attention output must be within max-abs 2e-3 * max|o| of the
+oracle's attention on that same cache."""
+import numpy as np
+import pytest
+
+import workloads as W
+from gpu_harness import (ATT_TOL, MAX_MISMATCH_FRAC, att_error, compare_codes, compare_norms, make_setup,
+                         oracle_attention, oracle_encode, to_torch_input)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def tq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import rotated_bit_kv_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+def _workload(name):
+    return {
+        "tiny": W.tiny_single_head(),
+        "llama8b": W.llama8b_decode(),
+        "block32_tq3": W.block32(3),
+        "block32_tq4": W.block32(4),
+        "so4": W.so4_wht(),
+        "mixed": W.mixed_rate_long(),
+    }[name]
+
+
+SMALL = {  # (batch, T) element-wise cases: several tiles and a ragged tail
+    "tiny": (1, 256),
+    "llama8b": (3, 333),
+    "block32_tq3": (2, 333),
+    "block32_tq4": (2, 333),
+    "so4": (1, 333),
+    "mixed": (1, 700),
+}
+
+
+def _encode_on_gpu(tq, name, B, T, cap_extra=5, seq_lens=None):
+    wl = _workload(name).with_(batch=B)
+    inp = W.make_inputs(wl, seq_len=T, seq_lens=seq_lens)
+    st = make_setup(tq, wl, inp, T + cap_extra)
+    cache = tq.PackedKVCache(st.desc, st.blob)
+    K = to_torch_input(torch, inp.K, wl.in_dtype)
+    V = to_torch_input(torch, inp.V, wl.in_dtype)
+    start = torch.zeros(B, dtype=torch.int32, device="cuda")
+    cache.append(K, V, start)
+    torch.cuda.synchronize()
+    return st, cache
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_quantize_append_matches_oracle(tq, name):
+    B, T = SMALL[name]
+    st, cache = _encode_on_gpu(tq, name, B, T)
+    assert int(cache.status.item()) == 0
+    kc = cache.codes_view("k").cpu().numpy()
+    vc = cache.codes_view("v").cpu().numpy()
+    kn = cache.norms_view("k").cpu().numpy()
+    vn = cache.norms_view("v").cpu().numpy()
+    tot = bad = 0
+    for b in range(B):
+        for h in range(st.wl.n_kv_heads):
+            for which, codes, norms in (("k", kc, kn), ("v", vc, vn)):
+                enc = oracle_encode(st, which, b, h)
+                spec = st.specs[h][0 if which == "k" else 1]
+                nbad, n, fw, fws, ok = compare_codes(codes[b, h, :T], enc, spec)
+                assert ok, f"{which} b={b} h={h}: a mismatch outside the near-boundary window"
+                bad += nbad
+                tot += n
+                assert compare_norms(norms[b, h, :T], enc), f"{which} norms b={b} h={h}"
+                # slots beyond T stay untouched (zero)
+                assert not codes[b, h, T:].any()
+    assert bad / tot <= MAX_MISMATCH_FRAC, (bad, tot)
+
+
+def _upload_oracle_cache(tq, st, cache, B, T):
+    """Write the oracle's records into the device cache; returns the encodings."""
+    encs = {}
+    kcv, vcv = cache.codes_view("k"), cache.codes_view("v")
+    knv, vnv = cache.norms_view("k"), cache.norms_view("v")
+    for b in range(B):
+        for h in range(st.wl.n_kv_heads):
+            ek = oracle_encode(st, "k", b, h, 0, T)
+            ev = oracle_encode(st, "v", b, h, 0, T)
+            kcv[b, h, :T] = torch.from_numpy(ek.codes)
+            vcv[b, h, :T] = torch.from_numpy(ev.codes)
+            knv[b, h, :T] = torch.from_numpy(ek.norms)
+            vnv[b, h, :T] = torch.from_numpy(ev.norms)
+            encs[(b, h)] = (ek, ev)
+    torch.cuda.synchronize()
+    return encs
+
+
+def _check_decode(tq, st, cache, encs, q, seq_lens, max_seq, v_mode, n_splits, pairs=None):
+    out = cache.decode(q, seq_lens, max_seq, v_mode=v_mode, n_splits=n_splits)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    G = st.wl.group
+    errs, scales = [], []
+    L = seq_lens.cpu().numpy()
+    pairs = pairs or list(encs)
+    for (b, h) in pairs:
+        ek, ev = encs[(b, h)]
+        ref = oracle_attention(st, ek, ev, b, h, int(min(L[b], max_seq)))
+        e, s = att_error(o[b, h * G:(h + 1) * G], ref)
+        errs.append(e)
+        scales.append(s)
+    err, scale = max(errs), max(scales)
+    assert err <= ATT_TOL * scale, (err, scale)
+    return err, scale
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+@pytest.mark.parametrize("n_splits", [1, 3, 0])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_matches_oracle(tq, name, v_mode, n_splits):
+    B, T = SMALL[name]
+    seq_lens = W.ragged_lengths(B, T, 3) if B > 1 else None
+    st, cache = _encode_on_gpu(tq, name, B, T, seq_lens=seq_lens)
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.from_numpy(st.inp.seq_lens).cuda()
+    _check_decode(tq, st, cache, encs, q, sl, T, v_mode, n_splits)
+    assert int(cache.status.item()) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 31, 127, 128, 129, 511, 512])
+def test_decode_short_and_tile_edges(tq, T):
+    st, cache = _encode_on_gpu(tq, "so4", 1, T)
+    encs = _upload_oracle_cache(tq, st, cache, 1, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.full((1,), T, dtype=torch.int32, device="cuda")
+    for v_mode in (0, 1, -1):
+        _check_decode(tq, st, cache, encs, q, sl, T, v_mode, 0)
+
+
+def test_v_mode_switch_at_crossover(tq):
+    st, _ = _encode_on_gpu(tq, "so4", 1, 8)
+    lo = tq.tq_decode_plan(st.desc, 511)[1]
+    hi = tq.tq_decode_plan(st.desc, 512)[1]
+    assert lo == tq.TQ_VMODE_TOKEN_PARALLEL and hi == tq.TQ_VMODE_DIM_PARALLEL
+
+
+def test_seq_len_zero_and_clamping(tq):
+    B, T = 3, 200
+    st, cache = _encode_on_gpu(tq, "llama8b", B, T, cap_extra=0)
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    # batch 0 empty, batch 1 over capacity (clamped to T), batch 2 normal
+    sl = torch.tensor([0, T + 50, 77], dtype=torch.int32, device="cuda")
+    out = cache.decode(q, sl, T)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 0)
+    st_word = int(cache.status.item())
+    assert st_word & tq.TQ_DEV_SEQ_OVER_CAPACITY
+    G = st.wl.group
+    for b, L in ((1, T), (2, 77)):
+        for h in range(st.wl.n_kv_heads):
+            ek, ev = encs[(b, h)]
+            ref = oracle_attention(st, ek, ev, b, h, L)
+            e, s = att_error(o[b, h * G:(h + 1) * G], ref)
+            assert e <= ATT_TOL * s
+
+
+def test_append_positions_and_incremental(tq):
+    """Appending token by token at increasing positions gives the same cache
+    as one whole-prompt call; positions outside the capacity are skipped and
+    flagged."""
+    B, T = 2, 40
+    st, cache = _encode_on_gpu(tq, "llama8b", B, T)
+    whole_k = cache.codes_view("k").clone()
+    whole_kn = cache.norms_view("k").clone()
+    cache2 = tq.PackedKVCache(st.desc, st.blob)
+    K = to_torch_input(torch, st.inp.K, st.wl.in_dtype)
+    V = to_torch_input(torch, st.inp.V, st.wl.in_dtype)
+    for t in range(0, T, 7):
+        n = min(7, T - t)
+        cache2.append(K[:, t:t + n].contiguous(), V[:, t:t + n].contiguous(),
+                      torch.full((B,), t, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(cache2.codes_view("k"), whole_k)
+    assert torch.equal(cache2.norms_view("k"), whole_kn)
+    assert int(cache2.status.item()) == 0
+    # out-of-range start position: skipped and flagged; n_new = 0 is a no-op
+    before = cache2.codes_view("v").clone()
+    cache2.append(K[:, :3].contiguous(), V[:, :3].contiguous(),
+                  torch.tensor([st.desc.t_capacity - 1, -5], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(cache2.status.item()) & tq.TQ_DEV_BAD_POSITION
+    after = cache2.codes_view("v")
+    cap = st.desc.t_capacity
+    assert torch.equal(after[1], before[1])             # batch 1 entirely skipped
+    assert torch.equal(after[0, :, :cap - 1], before[0, :, :cap - 1])
+    tq.tq_quantize_append(st.desc, cache2.ptrs, K[:, :0].contiguous(), V[:, :0].contiguous(),
+                          torch.zeros(B, dtype=torch.int32, device="cuda"), 0)
+
+
+def test_argument_errors(tq):
+    st, cache = _encode_on_gpu(tq, "tiny", 1, 8)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.full((1,), 8, dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(tq.TQError) as e:          # max_seq above capacity
+        tq.tq_decode_attention(st.desc, cache.ptrs, q, sl, 10 ** 6, out, cache.workspace)
+    assert e.value.status == tq.TQ_ERR_INVALID_ARG
+    small_ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tq.TQError) as e:          # workspace too small for 4 splits
+        tq.tq_decode_attention_ex(st.desc, cache.ptrs, q, sl, 8, out, small_ws, None, None, 1, 4)
+    assert e.value.status == tq.TQ_ERR_WORKSPACE
+    with pytest.raises(tq.TQError):               # misaligned output
+        tq.tq_decode_attention(st.desc, cache.ptrs, q, sl, 8, out.view(-1)[1:].view(1, 1, 127)[:, :, :], cache.workspace)
+
+
+# --------------------------------------------------------------------------
+# full sizes, in the launch configuration the benchmark times (automatic plan)
+FULL = {
+    "llama8b": (W.llama8b_decode(), [(0, 0), (13, 5), (31, 7)]),
+    "block32_tq4": (W.block32(4), [(0, 0), (7, 7)]),
+    "so4_32k": (W.so4_wht(seq_len=32768), [(0, 0), (0, 3)]),
+    "mixed_131k": (W.mixed_rate_long(131072), [(0, 0), (0, 1)]),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled(tq, name):
+    wl, pairs = FULL[name]
+    T, B = wl.seq_len, wl.batch
+    inp = W.make_inputs(wl)
+    st = make_setup(tq, wl, inp, T)
+    cache = tq.PackedKVCache(st.desc, st.blob)
+    K = to_torch_input(torch, inp.K, wl.in_dtype)
+    V = to_torch_input(torch, inp.V, wl.in_dtype)
+    cache.append(K, V, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    del K, V
+    # write side on the sampled pairs
+    kc, vc = cache.codes_view("k"), cache.codes_view("v")
+    encs = {}
+    bad = tot = 0
+    for (b, h) in pairs:
+        ek = oracle_encode(st, "k", b, h)
+        ev = oracle_encode(st, "v", b, h)
+        for enc, codes, which in ((ek, kc, 0), (ev, vc, 1)):
+            nb, n, _, _, ok = compare_codes(codes[b, h].cpu().numpy(), enc, st.specs[h][which])
+            assert ok
+            bad += nb
+            tot += n
+        encs[(b, h)] = (ek, ev)
+    assert bad / tot <= MAX_MISMATCH_FRAC
+    # read side: the sampled pairs carry the oracle's records
+    knv, vnv = cache.norms_view("k"), cache.norms_view("v")
+    for (b, h), (ek, ev) in encs.items():
+        kc[b, h] = torch.from_numpy(ek.codes)
+        vc[b, h] = torch.from_numpy(ev.codes)
+        knv[b, h] = torch.from_numpy(ek.norms)
+        vnv[b, h] = torch.from_numpy(ev.norms)
+    q = to_torch_input(torch, inp.q, wl.in_dtype)
+    sl = torch.from_numpy(inp.seq_lens).cuda()
+    _check_decode(tq, st, cache, encs, q, sl, T, -1, 0, pairs=pairs)
+    assert int(cache.status.item()) == 0
