@@ -73,16 +73,28 @@ class ClockSampler:
 
     def __init__(self, local_rank: int):
         self.proc = None
-        vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
-        gpu_index = vis[local_rank].strip() if local_rank < len(vis) else str(local_rank)
         self.path = os.path.join("/tmp", f"tq_clocks_{os.getpid()}.csv")
         try:
+            gpu_index = self._index_of(local_rank)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    @staticmethod
+    def _index_of(local_rank: int) -> str:
+        """nvidia-smi index of the CUDA device this rank uses, matched by UUID."""
+        import torch
+        uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+        out = subprocess.run(["nvidia-smi", "--query-gpu=index,uuid", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=30).stdout
+        rows = [r.split(",") for r in out.strip().splitlines() if "," in r]
+        for idx, u in rows:
+            if uuid.replace("GPU-", "") in u:
+                return idx.strip()
+        return rows[0][0].strip() if len(rows) == 1 else str(local_rank)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -370,12 +382,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seq-len", type=int, default=8192)
+    ap.add_argument("--batch", type=int, default=32, help="smaller batches are for profiling captures only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    wl = W.llama8b_decode(seq_len=args.seq_len)
+    wl = W.llama8b_decode(seq_len=args.seq_len, batch=args.batch)
     if args.impl == "reference":
         run_reference(args, wl, args.seq_len, rank, world)
         return

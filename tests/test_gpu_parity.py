@@ -151,7 +151,7 @@ def test_decode_short_and_tile_edges(tq, T):
 
 
 def test_v_mode_switch_at_crossover(tq):
-    st, _ = _encode_on_gpu(tq, "so4", 1, 8)
+    st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=600)
     lo = tq.tq_decode_plan(st.desc, 511)[1]
     hi = tq.tq_decode_plan(st.desc, 512)[1]
     assert lo == tq.TQ_VMODE_TOKEN_PARALLEL and hi == tq.TQ_VMODE_DIM_PARALLEL
@@ -224,8 +224,10 @@ def test_argument_errors(tq):
     with pytest.raises(tq.TQError) as e:          # workspace too small for 4 splits
         tq.tq_decode_attention_ex(st.desc, cache.ptrs, q, sl, 8, out, small_ws, None, None, 1, 4)
     assert e.value.status == tq.TQ_ERR_WORKSPACE
-    with pytest.raises(tq.TQError):               # misaligned output
-        tq.tq_decode_attention(st.desc, cache.ptrs, q, sl, 8, out.view(-1)[1:].view(1, 1, 127)[:, :, :], cache.workspace)
+    big = torch.empty(128 + 4, dtype=torch.float32, device="cuda")
+    with pytest.raises(tq.TQError) as e:          # output not 16-byte aligned
+        tq.tq_decode_attention(st.desc, cache.ptrs, q, sl, 8, big[1:129].view(1, 1, 128), cache.workspace)
+    assert e.value.status == tq.TQ_ERR_INVALID_ARG
 
 
 # --------------------------------------------------------------------------
