@@ -272,6 +272,34 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* desc, const tq_cache_ptrs*
                                  size_t workspace_bytes, int32_t* d_status, void* stream,
                                  int32_t v_mode, int32_t n_splits);
 
+/* tq_decode_attention for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this entry point; it exists for callers that
+ * must not call cudaMalloc: code running inside another framework's memory
+ * pool, plugins that are given only their input and output buffers, and paths
+ * where an allocation would synchronise the device.  The split-K scratch (the
+ * per-split partials and the per-(batch, KV head) tickets) is a fixed 8 MiB
+ * array inside the library's device image, held by every GPU that loads the
+ * library until the process exits; nothing is allocated or freed.
+ *   Arguments as tq_decode_attention, without the workspace; the plan is the
+ *   automatic one (same splits and V mode as tq_decode_attention).
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call zeroes the ticket words on `stream` before the kernel; the
+ *   partials are overwritten.  All calls share the one array, so calls whose
+ *   kernels can overlap on the GPU (concurrent streams, several host threads)
+ *   race and corrupt each other: order them on one stream.
+ * Errors: as tq_decode_attention; TQ_ERR_WORKSPACE when the plan needs more
+ * scratch than tq_decode_noalloc_max_scratch_bytes() (reduce batch * KV heads
+ * or use tq_decode_attention with a workspace). */
+tq_status tq_decode_attention_noalloc(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
+                                      const void* q, int32_t q_dtype, const int32_t* d_seq_lens,
+                                      int32_t max_seq_len, float* out, int32_t* d_status,
+                                      void* stream);
+
+/* Size in bytes of the fixed scratch array behind tq_decode_attention_noalloc. */
+size_t tq_decode_noalloc_max_scratch_bytes(void);
+
 /* The splits and V mode tq_decode_attention would use (host only). */
 tq_status tq_decode_plan(const tq_cache_desc* desc, int32_t max_seq_len, int32_t v_mode,
                          int32_t n_splits, int32_t* splits_out, int32_t* v_mode_out);

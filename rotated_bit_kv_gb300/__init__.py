@@ -63,6 +63,9 @@ _SIGS = {
     "tq_decode_attention_ex": (_I, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_ptrs), _P, _I, _P,
                                     _I, _P, _P, ctypes.c_size_t, _P, _P, _I, _I]),
     "tq_decode_plan": (_I, [ctypes.POINTER(tq_cache_desc), _I, _I, _I, _P, _P]),
+    "tq_decode_attention_noalloc": (_I, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_ptrs), _P, _I,
+                                         _P, _I, _P, _P, _P]),
+    "tq_decode_noalloc_max_scratch_bytes": (ctypes.c_size_t, []),
 }
 
 
@@ -221,6 +224,20 @@ def tq_decode_attention_ex(desc: tq_cache_desc, cache: tq_cache_ptrs, q, seq_len
                                         _ptr(seq_lens), int(max_seq_len), _ptr(out), _ptr(workspace), nbytes,
                                         _ptr(status), _stream(stream), int(v_mode), int(n_splits)),
            "tq_decode_attention_ex")
+
+
+def tq_decode_noalloc_max_scratch_bytes() -> int:
+    return int(lib().tq_decode_noalloc_max_scratch_bytes())
+
+
+def tq_decode_attention_noalloc(desc: tq_cache_desc, cache: tq_cache_ptrs, q, seq_lens, max_seq_len: int, out,
+                                status=None, stream=None):
+    """Decode attention without a workspace: the split-K scratch is the
+    library's fixed device array (for callers that cannot allocate)."""
+    _require_cuda(q, seq_lens, out, status)
+    _check(lib().tq_decode_attention_noalloc(ctypes.byref(desc), ctypes.byref(cache), _ptr(q), _dtype_code(q),
+                                             _ptr(seq_lens), int(max_seq_len), _ptr(out), _ptr(status),
+                                             _stream(stream)), "tq_decode_attention_noalloc")
 
 
 # ---------------------------------------------------------------- allocation helper

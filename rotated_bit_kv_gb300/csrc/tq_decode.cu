@@ -671,3 +671,64 @@ tq_status tq_decode_attention(const tq_cache_desc* d, const tq_cache_ptrs* c, co
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code that runs inside another
+// framework's memory pool or allocator (and must not allocate behind its
+// back), plugins handed only fixed input/output buffers, and paths where an
+// allocation would synchronise the device.  For them the split-K scratch (the
+// per-split partials and the per-(batch, KV head) tickets) lives in a fixed
+// array in this library's device image instead of a caller-provided buffer.
+// Every GPU that loads the library holds this array until the process exits.
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device, looked up once per
+// device.  In host code the array's name only stands in for the symbol; only
+// the address returned here may be handed to a kernel.
+tq_status scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return TQ_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" size_t tq_decode_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" tq_status tq_decode_attention_noalloc(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q,
+                                                 int32_t q_dtype, const int32_t* d_seq_lens, int32_t max_seq_len,
+                                                 float* out, int32_t* d_status, void* stream) {
+    int32_t splits = 0, mode = 0;
+    tq_status st = tq_decode_plan(d, max_seq_len, TQ_VMODE_AUTO, 0, &splits, &mode);
+    if (st != TQ_OK) return st;
+    if (splits == 1) return tq_decode_attention_ex(d, c, q, q_dtype, d_seq_lens, max_seq_len, out, nullptr, 0,
+                                                   d_status, stream, TQ_VMODE_AUTO, 1);
+    const size_t need = tq_decode_workspace_bytes(d, splits);
+    if (need == 0 || need > kNoAllocScratchBytes) return TQ_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    st = scratch_address(&scratch);
+    if (st != TQ_OK) return st;
+    // the tickets must start at zero; the array keeps whatever the last call left
+    const size_t pairs = (size_t)d->batch * d->n_kv_heads;
+    if (cudaMemsetAsync(scratch, 0, pairs * sizeof(int32_t), (cudaStream_t)stream) != cudaSuccess) return TQ_ERR_CUDA;
+    return tq_decode_attention_ex(d, c, q, q_dtype, d_seq_lens, max_seq_len, out, scratch, kNoAllocScratchBytes,
+                                  d_status, stream, TQ_VMODE_AUTO, splits);
+}
