@@ -78,7 +78,7 @@ class ClockSampler:
             gpu_index = self._index_of(local_rank)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "25"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -132,18 +132,22 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic():
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
-    if it was taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "decode_llama8b_T8192.md")
-    if not os.path.exists(p):
-        return None
-    src, traffic = None, None
-    for line in open(p):
-        if line.startswith("kernel_source_sha256_16:"):
-            src = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
-    return traffic if src == kernel_source_hash() else None
+    """Per-launch DRAM bytes of the decode kernel from a committed ncu summary
+    taken on the current kernel source (else None)."""
+    d = os.path.join(ROOT, "profiles")
+    want = kernel_source_hash()
+    for f in sorted(os.listdir(d)) if os.path.isdir(d) else []:
+        if not f.endswith(".md"):
+            continue
+        src, traffic = None, None
+        for line in open(os.path.join(d, f)):
+            if line.startswith("kernel_source_sha256_16:"):
+                src = line.split(":", 1)[1].strip()
+            if line.startswith("dram_bytes_per_launch:"):
+                traffic = float(line.split(":", 1)[1].strip())
+        if src == want and traffic is not None:
+            return traffic
+    return None
 
 
 # ----------------------------------------------------------------------------
@@ -378,7 +382,7 @@ def run_ours(args, wl, T, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seq-len", type=int, default=8192)
