@@ -16,255 +16,10 @@
 // sections and applies R_V^T.
 #include <stdlib.h>
 
-#include "tq_device.cuh"
+
+#include "tq_decode_common.cuh"
 
 namespace {
-
-constexpr int kThreads = 128;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
-constexpr int kPartStride = 132;                      // 128 (o~) + m + l, 16-byte rows
-
-struct DecodeArgs {
-    const uint8_t* k_codes;
-    const void* k_norms;
-    const uint8_t* v_codes;
-    const void* v_norms;
-    const tq_head_params* params;
-    const float* kmat;
-    const void* q;
-    const int32_t* seq_lens;
-    float* out;
-    float* ws_part;
-    int32_t* tickets;
-    int32_t* status;
-    int B, Hq, Hkv, G, Tcap, max_seq, n_splits, split_len, q_dtype, norm_f16, rot, k_mixed;
-};
-
-template <int F> struct Fmt {
-    static constexpr bool three = (F == TQ_FMT_ONE3 || F == TQ_FMT_BLK3);
-    static constexpr int bytes = three ? 48 : 64;
-    static constexpr int words = bytes / 4;
-    static constexpr int nslots = (F == TQ_FMT_ONE3 || F == TQ_FMT_ONE4) ? 1 : 4;
-    static constexpr bool blk = (F == TQ_FMT_BLK3 || F == TQ_FMT_BLK4);
-    static constexpr bool mix = (F == TQ_FMT_MIX4);
-};
-
-// index of code c (compile-time in unrolled loops) from a record in registers
-template <bool THREE>
-__device__ __forceinline__ uint32_t code_at(const uint32_t* w, int c) {
-    if (THREE) {
-        const int bit = 3 * c, wi = bit >> 5, sh = bit & 31;
-        if (sh <= 29) return (w[wi] >> sh) & 7u;
-        return __funnelshift_r(w[wi], w[wi + 1], sh) & 7u;
-    }
-    return (w[c >> 3] >> (4 * (c & 7))) & 15u;
-}
-
-template <int F>
-__device__ __forceinline__ void load_record(const uint8_t* base, size_t tok, uint32_t* w) {
-    const uint4* p = reinterpret_cast<const uint4*>(base + tok * Fmt<F>::bytes);
-#pragma unroll
-    for (int i = 0; i < Fmt<F>::words / 4; ++i) {
-        uint4 u = __ldg(p + i);
-        w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
-    }
-}
-
-template <int F>
-__device__ __forceinline__ void load_norms(const void* base, size_t tok, int norm_f16, float* n) {
-    if (Fmt<F>::nslots == 1) {
-        n[0] = tq::load_norm(base, tok, norm_f16);
-    } else if (norm_f16) {
-        uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(base) + tok * 4));
-        float2 a = __half22float2(*reinterpret_cast<__half2*>(&u.x));
-        float2 b = __half22float2(*reinterpret_cast<__half2*>(&u.y));
-        n[0] = a.x; n[1] = a.y; n[2] = b.x; n[3] = b.y;
-    } else {
-        float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + tok * 4));
-        n[0] = f.x; n[1] = f.y; n[2] = f.z; n[3] = f.w;
-    }
-}
-
-template <int GP>
-__device__ __forceinline__ void load_row(const float* row, float* q) {
-    if (GP % 4 == 0) {
-#pragma unroll
-        for (int i = 0; i < GP / 4; ++i) {
-            float4 v = reinterpret_cast<const float4*>(row)[i];
-            q[4 * i] = v.x; q[4 * i + 1] = v.y; q[4 * i + 2] = v.z; q[4 * i + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < GP; ++i) q[i] = row[i];
-    }
-}
-
-// s_g = sum over segments of n_seg * sum_c q~_g[c] C_seg[idx_c]   (log2 units:
-// q~ already carries log2(e) / sqrt(d))
-template <int GP, int KF>
-__device__ __forceinline__ void qk_token(const uint32_t* rec, const float* nrm, const float (*qt)[GP],
-                                         const float (*kcb)[16], const uint8_t* kseg_of, float* sc) {
-    using K = Fmt<KF>;
-#pragma unroll
-    for (int g = 0; g < GP; ++g) sc[g] = 0.f;
-    if (K::mix) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-            const int s = kseg_of[c];
-            float n = nrm[0];
-            n = s == 1 ? nrm[1] : n;
-            n = s == 2 ? nrm[2] : n;
-            n = s == 3 ? nrm[3] : n;
-            const float v = kcb[s][code_at<false>(rec, c)] * n;
-            float q[GP];
-            load_row<GP>(qt[c], q);
-#pragma unroll
-            for (int g = 0; g < GP; ++g) sc[g] = fmaf(v, q[g], sc[g]);
-        }
-    } else {
-        constexpr int nseg = K::blk ? 4 : 1;
-        constexpr int len = 128 / nseg;
-#pragma unroll
-        for (int s = 0; s < nseg; ++s) {
-            float part[GP];
-#pragma unroll
-            for (int g = 0; g < GP; ++g) part[g] = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < len; ++cc) {
-                const int c = s * len + cc;
-                const float v = kcb[s][code_at<K::three>(rec, c)];
-                float q[GP];
-                load_row<GP>(qt[c], q);
-#pragma unroll
-                for (int g = 0; g < GP; ++g) part[g] = fmaf(v, q[g], part[g]);
-            }
-#pragma unroll
-            for (int g = 0; g < GP; ++g) sc[g] = fmaf(nrm[s], part[g], sc[g]);
-        }
-    }
-}
-
-template <int GP, int KF, int VF>
-struct Smem {
-    alignas(16) float qt[128][GP];
-    alignas(16) float kcb[4][16];
-    alignas(16) float vcb[4][16];
-    alignas(16) float xs[4][128];     // per-warp staging for the dense key rotation of q
-    alignas(16) float red[4][GP];
-    alignas(16) float red2[4][GP];
-    alignas(16) uint8_t kseg_of[128];
-    int is_last;
-};
-
-// Prologue shared by both modes: codebooks, q~ = R_K q (scaled to log2 units).
-template <int GP, int KF, int VF>
-__device__ __forceinline__ void prologue(const DecodeArgs& a, const tq_head_params& P, Smem<GP, KF, VF>& S,
-                                         int b, int h) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid < 64) {
-        S.kcb[tid >> 4][tid & 15] = P.k_cent[tid >> 4][tid & 15];
-        S.vcb[tid >> 4][tid & 15] = P.v_cent[tid >> 4][tid & 15];
-    }
-    if (Fmt<KF>::mix) {
-        int s = 0;
-        while (s < 3 && tid >= P.k_seg_start[s + 1]) ++s;
-        S.kseg_of[tid] = (uint8_t)s;
-    }
-    for (int g = warp; g < GP; g += 4) {
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (g < a.G) {
-            const size_t elem = ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128 + 4 * lane;
-            tq::load4(a.q, elem, a.q_dtype, v);
-            if (Fmt<KF>::mix) {
-                float* xs = S.xs[warp];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) xs[4 * lane + i] = v[i];
-                __syncwarp();
-                tq::rotate_forward_dense(P, a.kmat + (size_t)h * 128 * 128, xs, v);
-                __syncwarp();
-            } else {
-                tq::rotate_forward(a.rot, P, v);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) S.qt[4 * lane + i][g] = v[i] * (kLog2e * kInvSqrtD);
-    }
-}
-
-// Clamp the sequence length and flag what was clamped.
-__device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
-    int L = a.seq_lens[b];
-    int flags = 0;
-    if (L > a.Tcap) { flags |= TQ_DEV_SEQ_OVER_CAPACITY; L = a.Tcap; }
-    if (L > a.max_seq) { flags |= TQ_DEV_SEQ_OVER_MAX; L = a.max_seq; }
-    if (L < 0) L = 0;
-    if (flags && a.status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.status, flags);  // once per batch
-    return L;
-}
-
-// Epilogue: `ot[g][c]` holds this CTA's unnormalised o~, (m[g], l[g]) its
-// softmax state (identical in every thread).  Either finalise directly (one
-// split) or publish the partial and let the last CTA merge.
-template <int GP>
-__device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const float* m,
-                         const float* l, int* is_last, int b, int h, int s) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (a.n_splits > 1) {
-        float* part = a.ws_part + ((((size_t)b * a.Hkv + h) * a.n_splits + s) * GP) * kPartStride;
-        for (int i = tid; i < GP * 128; i += kThreads) part[(i >> 7) * kPartStride + (i & 127)] = ot[i >> 7][i & 127];
-        if (tid < GP) {
-            part[tid * kPartStride + 128] = m[tid];
-            part[tid * kPartStride + 129] = l[tid];
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int ticket = atomicAdd(a.tickets + (size_t)b * a.Hkv + h, 1);
-            *is_last = ticket == a.n_splits - 1;
-        }
-        __syncthreads();
-        if (!*is_last) return;
-        __threadfence();
-        // log-sum-exp merge over the splits  [Block-GTQ]
-        const float* base = a.ws_part + (((size_t)b * a.Hkv + h) * a.n_splits * GP) * kPartStride;
-        for (int g = 0; g < GP; ++g) {
-            float M = -INFINITY;
-            for (int t = 0; t < a.n_splits; ++t) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
-            float lsum = 0.f, o = 0.f;
-            if (M != -INFINITY) {
-                for (int t = 0; t < a.n_splits; ++t) {
-                    const float* pr = base + ((size_t)t * GP + g) * kPartStride;
-                    const float mt = __ldcg(pr + 128);
-                    if (mt == -INFINITY) continue;
-                    const float w = exp2f(mt - M);
-                    lsum = fmaf(w, __ldcg(pr + 129), lsum);
-                    o = fmaf(w, __ldcg(pr + tid), o);
-                }
-            }
-            __syncthreads();
-            ot[g][tid] = lsum > 0.f ? o / lsum : 0.f;
-        }
-        if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
-        __syncthreads();
-    } else {
-        for (int i = tid; i < GP * 128; i += kThreads) {
-            const int g = i >> 7;
-            ot[g][i & 127] = l[g] > 0.f ? ot[g][i & 127] / l[g] : 0.f;
-        }
-        __syncthreads();
-    }
-    // o = R_V^T o~, once per query head  [RotaryQuant Key design 3, Kernel D]
-    for (int g = warp; g < a.G; g += 4) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = ot[g][4 * lane + i];
-        tq::rotate_inverse(a.rot, P, v);
-        float4* o4 = reinterpret_cast<float4*>(a.out + ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128) + lane;
-        *o4 = make_float4(v[0], v[1], v[2], v[3]);
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Dimension-parallel V accumulation: per tile of 128 tokens, thread t computes
 // the logits of token t (token parallel QK); the tile's V codes are staged in
@@ -583,14 +338,33 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     if (!d || d->head_dim != TQ_HEAD_DIM || max_seq_len < 1 || max_seq_len > d->t_capacity) return TQ_ERR_INVALID_ARG;
     if (v_mode < TQ_VMODE_AUTO || v_mode > TQ_VMODE_TENSOR) return TQ_ERR_INVALID_ARG;
     if (n_splits < 0 || n_splits > TQ_MAX_SPLITS) return TQ_ERR_INVALID_ARG;
+    const bool tc = tq_decode_tc_supported(d);
     int mode = v_mode;
-    if (mode == TQ_VMODE_AUTO) mode = max_seq_len < tq_v_crossover() ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
-    if (mode == TQ_VMODE_TENSOR) return TQ_ERR_UNSUPPORTED;
+    if (mode == TQ_VMODE_AUTO) {
+        if (max_seq_len < tq_v_crossover()) mode = TQ_VMODE_TOKEN_PARALLEL;
+        else mode = tc ? TQ_VMODE_TENSOR : TQ_VMODE_DIM_PARALLEL;
+    }
+    if (mode == TQ_VMODE_TENSOR && !tc) return TQ_ERR_UNSUPPORTED;
     int splits = n_splits;
-    if (splits == 0) {
+    const long long pairs = (long long)d->batch * d->n_kv_heads;
+    if (splits == 0 && mode == TQ_VMODE_TENSOR) {
+        // whole waves of about four resident CTAs per SM; sections of at least
+        // 64 tokens (one 16-token tile per warp)
+        const long long wave = 4LL * kSMs;
+        long long cap = (max_seq_len + 63) / 64;
+        if (cap > TQ_MAX_SPLITS) cap = TQ_MAX_SPLITS;
+        long long best = 1;
+        double best_score = -1.0;
+        for (long long sp = 1; sp <= cap; ++sp) {
+            const double waves = (double)(pairs * sp) / wave;
+            const double full = waves < 1.0 ? waves : waves / ceil(waves);
+            const double score = full - 0.002 * (double)sp;   // mild preference for fewer merges
+            if (score > best_score + 1e-12) { best_score = score; best = sp; }
+        }
+        splits = (int)best;
+    } else if (splits == 0) {
         // fill the GPU: about four resident 128-thread CTAs per SM, sections of
         // at least 64 tokens
-        const long long pairs = (long long)d->batch * d->n_kv_heads;
         const long long target = 4LL * kSMs;
         long long sp = (target + pairs - 1) / pairs;
         const long long cap = (max_seq_len + 63) / 64;
@@ -621,8 +395,11 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     if (st != TQ_OK) return st;
     const int kf = tq_k_fmt(d), vf = tq_v_fmt(d);
     int GP = 1;
-    KernelFn fn = pick_kernel(d->group, kf, vf, mode, &GP);
-    if (!fn) return TQ_ERR_UNSUPPORTED;
+    KernelFn fn = nullptr;
+    if (mode != TQ_VMODE_TENSOR) {
+        fn = pick_kernel(d->group, kf, vf, mode, &GP);
+        if (!fn) return TQ_ERR_UNSUPPORTED;
+    }
     DecodeArgs a;
     a.k_codes = static_cast<const uint8_t*>(c->k_codes);
     a.k_norms = c->k_norms;
@@ -653,12 +430,19 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.max_seq = max_seq_len;
     a.n_splits = splits;
     a.split_len = (max_seq_len + splits - 1) / splits;
+    if (mode == TQ_VMODE_TENSOR) {
+        // sections start on 16-token tiles (16-byte aligned copies of codes and norms)
+        const int al = tq_decode_tc_split_align();
+        a.split_len = (a.split_len + al - 1) / al * al;
+    }
     a.q_dtype = q_dtype;
     a.norm_f16 = d->norm_dtype == TQ_F16;
     a.rot = d->rot;
     a.k_mixed = d->k_mixed;
-    dim3 grid(splits, d->n_kv_heads, d->batch);
     if (d->batch > 65535 || d->n_kv_heads > 65535) return TQ_ERR_INVALID_ARG;
+    if (mode == TQ_VMODE_TENSOR)
+        return tq_decode_tc_launch(d, a, splits, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    dim3 grid(splits, d->n_kv_heads, d->batch);
     fn<<<grid, kThreads, 0, (cudaStream_t)stream>>>(a);
     return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

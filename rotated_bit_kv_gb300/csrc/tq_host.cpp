@@ -121,21 +121,54 @@ tq_status lloyd_max(int d, int bits, double* c) {
     return TQ_ERR_NO_CONVERGENCE;
 }
 
+// fp16 round-to-nearest-even of a positive normal value (11 significant bits).
+double round_half(double x) {
+    int e;
+    const double m = frexp(x, &e);                 // [0.5, 1)
+    return ldexp(nearbyint(ldexp(m, 11)), e - 11);
+}
+
+// Scale s in [1, 2) for which the fp16 roundings of s * c_k (via fp32, as the
+// kernels compute them) have the smallest worst relative error.  Tensor-core
+// kernels keep the codebook as fp16 and fold 1/s into their fp32 norm factors,
+// so the codebook itself enters the products almost exactly.
+float fp16_table_scale(const float* cent, int K) {
+    double best_err = 1e30;
+    float best = 1.0f;
+    for (int i = 0; i < (1 << 16); ++i) {
+        const float sc = (float)(1.0 + i / 65536.0);
+        double err = 0.0;
+        for (int k = 0; k < K; ++k) {
+            const double v = fabs((double)(sc * cent[k]));
+            if (v == 0.0) continue;
+            err = fmax(err, fabs(round_half(v) - v) / v);
+        }
+        if (err < best_err) { best_err = err; best = sc; }
+    }
+    return best;
+}
+
 // Codebooks solved during one tq_params_build call, keyed by (d, bits).
 struct CodebookMemo {
-    struct Entry { int d, bits; float cent[16], bound[16]; };
+    struct Entry { int d, bits; float cent[16], bound[16], hscale; };
     std::vector<Entry> e;
-    tq_status get(int d, int bits, const float** cent, const float** bound) {
+    tq_status get(int d, int bits, const float** cent, const float** bound, float* hscale = nullptr) {
         for (auto& x : e)
-            if (x.d == d && x.bits == bits) { *cent = x.cent; *bound = x.bound; return TQ_OK; }
+            if (x.d == d && x.bits == bits) {
+                *cent = x.cent; *bound = x.bound;
+                if (hscale) *hscale = x.hscale;
+                return TQ_OK;
+            }
         Entry n{};
         n.d = d;
         n.bits = bits;
         tq_status st = tq_codebook(d, bits, n.cent, n.bound);
         if (st != TQ_OK) return st;
+        n.hscale = fp16_table_scale(n.cent, 1 << bits);
         e.push_back(n);
         *cent = e.back().cent;
         *bound = e.back().bound;
+        if (hscale) *hscale = e.back().hscale;
         return TQ_OK;
     }
 };
@@ -301,7 +334,7 @@ tq_status tq_params_build(const tq_cache_desc* d, const float* signs, const floa
         for (int s = 0; s <= 4; ++s) p.v_seg_start[s] = s < vseg ? s * vlen : 128;
         for (int s = 0; s < vseg; ++s) {
             const float *c, *bd;
-            tq_status st = memo.get(vlen, d->v_bits, &c, &bd);
+            tq_status st = memo.get(vlen, d->v_bits, &c, &bd, &p.v_h_scale[s]);
             if (st != TQ_OK) return st;
             p.v_seg_bits[s] = d->v_bits;
             memcpy(p.v_cent[s], c, sizeof(float) * 16);
@@ -314,7 +347,7 @@ tq_status tq_params_build(const tq_cache_desc* d, const float* signs, const floa
             for (int s = 0; s <= 4; ++s) p.k_seg_start[s] = s < kseg ? s * klen : 128;
             for (int s = 0; s < kseg; ++s) {
                 const float *c, *bd;
-                tq_status st = memo.get(klen, d->k_bits, &c, &bd);
+                tq_status st = memo.get(klen, d->k_bits, &c, &bd, &p.k_h_scale[s]);
                 if (st != TQ_OK) return st;
                 p.k_seg_bits[s] = d->k_bits;
                 memcpy(p.k_cent[s], c, sizeof(float) * 16);
@@ -343,7 +376,7 @@ tq_status tq_params_build(const tq_cache_desc* d, const float* signs, const floa
                     }
                 if (n) {
                     const float *c, *bd;
-                    tq_status st = memo.get(n, b, &c, &bd);
+                    tq_status st = memo.get(n, b, &c, &bd, &p.k_h_scale[s]);
                     if (st != TQ_OK) return st;
                     memcpy(p.k_cent[s], c, sizeof(float) * 16);
                     memcpy(p.k_bound[s], bd, sizeof(float) * 16);

@@ -20,7 +20,9 @@ struct alignas(16) tq_head_params {
     int32_t v_seg_start[5];
     int32_t v_seg_bits[4];
     int32_t v_nseg;
-    int32_t pad0[12];
+    float k_h_scale[4];       // fp16 table scale of segment s (see tq_params_build)
+    float v_h_scale[4];
+    int32_t pad0[4];
     float k_cent[4][16];      // ascending centroids of segment s
     float k_bound[4][16];     // 2^bits - 1 boundaries of segment s
     float v_cent[4][16];

@@ -151,10 +151,47 @@ def test_decode_short_and_tile_edges(tq, T):
 
 
 def test_v_mode_switch_at_crossover(tq):
-    st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=600)
-    lo = tq.tq_decode_plan(st.desc, 511)[1]
-    hi = tq.tq_decode_plan(st.desc, 512)[1]
-    assert lo == tq.TQ_VMODE_TOKEN_PARALLEL and hi == tq.TQ_VMODE_DIM_PARALLEL
+    st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=600)          # capacity 608: tensor path available
+    assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
+    assert tq.tq_decode_plan(st.desc, 512)[1] == tq.TQ_VMODE_TENSOR
+    st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=601)          # unaligned capacity: CUDA-core path
+    assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
+    assert tq.tq_decode_plan(st.desc, 512)[1] == tq.TQ_VMODE_DIM_PARALLEL
+    st, _ = _encode_on_gpu(tq, "block32_tq3", 1, 8, cap_extra=600)  # no tensor kernel for this format
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_plan(st.desc, 512, tq.TQ_VMODE_TENSOR)
+    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+
+
+TC_NAMES = ["tiny", "llama8b", "so4"]
+
+
+def _aligned_cap(T):
+    return (T + 5 + 7) // 8 * 8 - T
+
+
+@pytest.mark.parametrize("n_splits", [1, 3, 0])
+@pytest.mark.parametrize("name", TC_NAMES)
+def test_decode_tensor_matches_oracle(tq, name, n_splits):
+    B, T = SMALL[name]
+    seq_lens = W.ragged_lengths(B, T, 4) if B > 1 else None
+    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=_aligned_cap(T), seq_lens=seq_lens)
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.from_numpy(st.inp.seq_lens).cuda()
+    _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, n_splits)
+    assert int(cache.status.item()) == 0
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 64, 100, 512, 1000])
+@pytest.mark.parametrize("name", ["llama8b", "so4"])
+def test_decode_tensor_tile_edges(tq, name, T):
+    st, cache = _encode_on_gpu(tq, name, 1, T, cap_extra=_aligned_cap(T))
+    encs = _upload_oracle_cache(tq, st, cache, 1, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.full((1,), T, dtype=torch.int32, device="cuda")
+    for n_splits in (0, 1, 2):
+        _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, n_splits)
 
 
 def test_seq_len_zero_and_clamping(tq):
