@@ -256,7 +256,7 @@ def run_ours(args, wl, T, rank, world, local_rank):
     start = torch.full((wl.batch,), T - 1, dtype=torch.int32, device=dev)
     seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
     out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
-    splits, vmode = tq.tq_decode_plan(desc, T)
+    splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_AUTO, args.splits)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     in_code = tq._dtype_code(q)
@@ -269,8 +269,9 @@ def run_ours(args, wl, T, rank, world, local_rank):
                                      c.status.data_ptr(), sptr)
         if ev is not None:
             ev[0].record(stream)
-        st2 = lib.tq_decode_attention(dref, pref[i & 1], qd.data_ptr(), in_code, ld.data_ptr(), T, od.data_ptr(),
-                                      c.workspace.data_ptr(), c.workspace.numel(), c.status.data_ptr(), sptr)
+        st2 = lib.tq_decode_attention_ex(dref, pref[i & 1], qd.data_ptr(), in_code, ld.data_ptr(), T, od.data_ptr(),
+                                         c.workspace.data_ptr(), c.workspace.numel(), c.status.data_ptr(), sptr,
+                                         vmode, splits)
         if ev is not None:
             ev[1].record(stream)
         if st_ or st2:
@@ -388,6 +389,7 @@ def main():
     ap.add_argument("--seq-len", type=int, default=8192)
     ap.add_argument("--batch", type=int, default=32, help="smaller batches are for profiling captures only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0, help="key-axis splits (0: the library's plan)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

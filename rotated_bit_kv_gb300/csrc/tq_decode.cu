@@ -348,18 +348,21 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     int splits = n_splits;
     const long long pairs = (long long)d->batch * d->n_kv_heads;
     if (splits == 0 && mode == TQ_VMODE_TENSOR) {
-        // whole waves of about four resident CTAs per SM; sections of at least
-        // 64 tokens (one 16-token tile per warp)
-        const long long wave = 4LL * kSMs;
+        // an SM with at least four CTAs works through them at a fixed rate
+        // (below that its warps cannot hide latency), so the step takes about
+        // max(4, ceil(CTAs / SMs)) x (16-token tiles per warp + about two
+        // tiles of prologue/epilogue); sections of at least 64 tokens
         long long cap = (max_seq_len + 63) / 64;
         if (cap > TQ_MAX_SPLITS) cap = TQ_MAX_SPLITS;
         long long best = 1;
-        double best_score = -1.0;
+        double best_cost = 0.0;
         for (long long sp = 1; sp <= cap; ++sp) {
-            const double waves = (double)(pairs * sp) / wave;
-            const double full = waves < 1.0 ? waves : waves / ceil(waves);
-            const double score = full - 0.002 * (double)sp;   // mild preference for fewer merges
-            if (score > best_score + 1e-12) { best_score = score; best = sp; }
+            const long long sec = (max_seq_len + sp - 1) / sp;
+            const long long per_warp = (sec + 63) / 64;
+            long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
+            if (per_sm < 4) per_sm = 4;
+            const double cost = (double)per_sm * ((double)per_warp + 2.0);
+            if (sp == 1 || cost < best_cost - 1e-9) { best_cost = cost; best = sp; }
         }
         splits = (int)best;
     } else if (splits == 0) {
@@ -439,6 +442,7 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.norm_f16 = d->norm_dtype == TQ_F16;
     a.rot = d->rot;
     a.k_mixed = d->k_mixed;
+    a.fold_mul = 1u << 20;
     if (d->batch > 65535 || d->n_kv_heads > 65535) return TQ_ERR_INVALID_ARG;
     if (mode == TQ_VMODE_TENSOR)
         return tq_decode_tc_launch(d, a, splits, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;

@@ -22,6 +22,7 @@ struct DecodeArgs {
     int32_t* tickets;
     int32_t* status;
     int B, Hq, Hkv, G, Tcap, max_seq, n_splits, split_len, q_dtype, norm_f16, rot, k_mixed;
+    uint32_t fold_mul;   // 1 << 20 (a runtime operand keeps the selector fold on the FMA pipe)
 };
 }  // namespace tq
 
