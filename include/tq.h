@@ -56,6 +56,7 @@ typedef int32_t tq_status;
 #define TQ_DEV_SEQ_OVER_CAPACITY  1  /* seq_len > t_capacity: clamped          */
 #define TQ_DEV_SEQ_OVER_MAX       2  /* seq_len > max_seq_len: clamped         */
 #define TQ_DEV_BAD_POSITION       4  /* append position outside [0, capacity): skipped */
+#define TQ_DEV_WAIT_TIMEOUT       8  /* a bounded wait inside a kernel gave up: the output of that call is invalid */
 
 /* ---------------------------------------------------------------- enums */
 #define TQ_F32   0
@@ -88,6 +89,7 @@ typedef int32_t tq_status;
 #define TQ_VMODE_TOKEN_PARALLEL   0
 #define TQ_VMODE_DIM_PARALLEL     1
 #define TQ_VMODE_TENSOR           2  /* dimension parallel on tensor cores */
+#define TQ_VMODE_TENSOR_STREAMK   3  /* tensor cores, stream-K partition (explicit only) */
 
 #define TQ_HEAD_DIM     128
 #define TQ_MAX_GROUP     16   /* maximum n_q_heads / n_kv_heads */
@@ -232,7 +234,9 @@ tq_status tq_quantize_append(const tq_cache_desc* desc, const tq_cache_ptrs* cac
 
 /* Workspace bytes tq_decode_attention needs for at most max_splits key-axis
  * splits: partial (m, l, o~) per (batch, q head, split) plus one ticket per
- * (batch, KV head).  The ticket words must be zero before the first call on a
+ * (batch, KV head).  For caches the tensor-core kernel supports it also covers
+ * the stream-K partials (at least 1216 + batch * n_kv_heads partial slots), so
+ * max_splits = 1 is enough for the automatic plan.  The ticket words must be zero before the first call on a
  * workspace (e.g. a cudaMemset of the whole buffer); every call leaves them
  * zero again. */
 size_t tq_decode_workspace_bytes(const tq_cache_desc* desc, int32_t max_splits);
@@ -300,7 +304,12 @@ tq_status tq_decode_attention_noalloc(const tq_cache_desc* desc, const tq_cache_
 /* Size in bytes of the fixed scratch array behind tq_decode_attention_noalloc. */
 size_t tq_decode_noalloc_max_scratch_bytes(void);
 
-/* The splits and V mode tq_decode_attention would use (host only). */
+/* The splits and V mode tq_decode_attention would use (host only).
+ * tq_decode_attention_ex with v_mode TQ_VMODE_TENSOR and n_splits == 0 plans
+ * the same splits; the tensor-core kernel also has a "stream-K" partition
+ * (all 16-token tiles of all (batch, KV head) pairs spread evenly over one wave
+ * of persistent CTAs, a pair's pieces merged by the last of them), selected by
+ * v_mode TQ_VMODE_TENSOR_STREAMK; it needs tq_decode_workspace_bytes(desc, 1). */
 tq_status tq_decode_plan(const tq_cache_desc* desc, int32_t max_seq_len, int32_t v_mode,
                          int32_t n_splits, int32_t* splits_out, int32_t* v_mode_out);
 

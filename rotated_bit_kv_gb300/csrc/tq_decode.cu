@@ -320,6 +320,26 @@ bool aligned(const void* p, size_t n) { return ((uintptr_t)p % n) == 0; }
 
 constexpr int kSMs = 152;
 
+// Sections per (batch, KV head) pair for the tensor-core kernel when the
+// stream-K grid is unavailable: an SM with at least four CTAs works through
+// them at a fixed rate, so a step takes about max(4, ceil(CTAs / SMs)) x (tiles
+// per warp + about two tiles of start-up); sections of at least 64 tokens.
+int tc_uniform_splits(long long pairs, int max_seq_len) {
+    long long cap = (max_seq_len + 63) / 64;
+    if (cap > TQ_MAX_SPLITS) cap = TQ_MAX_SPLITS;
+    long long best = 1;
+    double best_cost = 0.0;
+    for (long long sp = 1; sp <= cap; ++sp) {
+        const long long sec = (max_seq_len + sp - 1) / sp;
+        const long long per_warp = (sec + 63) / 64;
+        long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
+        if (per_sm < 4) per_sm = 4;
+        const double cost = (double)per_sm * ((double)per_warp + 2.0);
+        if (sp == 1 || cost < best_cost - 1e-9) { best_cost = cost; best = sp; }
+    }
+    return (int)best;
+}
+
 }  // namespace
 
 extern "C" {
@@ -328,7 +348,12 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc* d, int32_t max_splits) {
     if (!d || d->head_dim != TQ_HEAD_DIM || max_splits < 1) return 0;
     if (max_splits > TQ_MAX_SPLITS) max_splits = TQ_MAX_SPLITS;
     const size_t pairs = (size_t)d->batch * d->n_kv_heads;
-    const size_t part = pairs * (size_t)max_splits * padded_group(d->group) * kPartStride * sizeof(float);
+    size_t slots = pairs * (size_t)max_splits;
+    if (tq_decode_tc_supported(d)) {   // room for the tensor-core kernel's stream-K partials
+        const size_t sk = (size_t)tq_decode_tc_sk_slots(d);
+        if (sk > slots) slots = sk;
+    }
+    const size_t part = slots * padded_group(d->group) * kPartStride * sizeof(float);
     const size_t tick = ((pairs * sizeof(int32_t)) + 255) & ~(size_t)255;
     return tick + part;
 }
@@ -336,7 +361,7 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc* d, int32_t max_splits) {
 tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_mode, int32_t n_splits,
                          int32_t* splits_out, int32_t* v_mode_out) {
     if (!d || d->head_dim != TQ_HEAD_DIM || max_seq_len < 1 || max_seq_len > d->t_capacity) return TQ_ERR_INVALID_ARG;
-    if (v_mode < TQ_VMODE_AUTO || v_mode > TQ_VMODE_TENSOR) return TQ_ERR_INVALID_ARG;
+    if (v_mode < TQ_VMODE_AUTO || v_mode > TQ_VMODE_TENSOR_STREAMK) return TQ_ERR_INVALID_ARG;
     if (n_splits < 0 || n_splits > TQ_MAX_SPLITS) return TQ_ERR_INVALID_ARG;
     const bool tc = tq_decode_tc_supported(d);
     int mode = v_mode;
@@ -344,27 +369,16 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
         if (max_seq_len < tq_v_crossover()) mode = TQ_VMODE_TOKEN_PARALLEL;
         else mode = tc ? TQ_VMODE_TENSOR : TQ_VMODE_DIM_PARALLEL;
     }
-    if (mode == TQ_VMODE_TENSOR && !tc) return TQ_ERR_UNSUPPORTED;
+    if ((mode == TQ_VMODE_TENSOR || mode == TQ_VMODE_TENSOR_STREAMK) && !tc) return TQ_ERR_UNSUPPORTED;
+    if (mode == TQ_VMODE_TENSOR_STREAMK) {   // no per-pair sections
+        if (splits_out) *splits_out = 0;
+        if (v_mode_out) *v_mode_out = mode;
+        return TQ_OK;
+    }
     int splits = n_splits;
     const long long pairs = (long long)d->batch * d->n_kv_heads;
     if (splits == 0 && mode == TQ_VMODE_TENSOR) {
-        // an SM with at least four CTAs works through them at a fixed rate
-        // (below that its warps cannot hide latency), so the step takes about
-        // max(4, ceil(CTAs / SMs)) x (16-token tiles per warp + about two
-        // tiles of prologue/epilogue); sections of at least 64 tokens
-        long long cap = (max_seq_len + 63) / 64;
-        if (cap > TQ_MAX_SPLITS) cap = TQ_MAX_SPLITS;
-        long long best = 1;
-        double best_cost = 0.0;
-        for (long long sp = 1; sp <= cap; ++sp) {
-            const long long sec = (max_seq_len + sp - 1) / sp;
-            const long long per_warp = (sec + 63) / 64;
-            long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
-            if (per_sm < 4) per_sm = 4;
-            const double cost = (double)per_sm * ((double)per_warp + 2.0);
-            if (sp == 1 || cost < best_cost - 1e-9) { best_cost = cost; best = sp; }
-        }
-        splits = (int)best;
+        splits = tc_uniform_splits(pairs, max_seq_len);
     } else if (splits == 0) {
         // fill the GPU: about four resident 128-thread CTAs per SM, sections of
         // at least 64 tokens
@@ -399,9 +413,15 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     const int kf = tq_k_fmt(d), vf = tq_v_fmt(d);
     int GP = 1;
     KernelFn fn = nullptr;
-    if (mode != TQ_VMODE_TENSOR) {
+    if (mode != TQ_VMODE_TENSOR && mode != TQ_VMODE_TENSOR_STREAMK) {
         fn = pick_kernel(d->group, kf, vf, mode, &GP);
         if (!fn) return TQ_ERR_UNSUPPORTED;
+    }
+    int sk_grid = 0;
+    if (mode == TQ_VMODE_TENSOR_STREAMK) {
+        mode = TQ_VMODE_TENSOR;
+        sk_grid = tq_decode_tc_sk_grid(d, max_seq_len);
+        if (sk_grid == 0) splits = tc_uniform_splits((long long)d->batch * d->n_kv_heads, max_seq_len);
     }
     DecodeArgs a;
     a.k_codes = static_cast<const uint8_t*>(c->k_codes);
@@ -417,8 +437,8 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.status = d_status;
     a.tickets = nullptr;
     a.ws_part = nullptr;
-    if (splits > 1) {
-        const size_t need = tq_decode_workspace_bytes(d, splits);
+    if (splits > 1 || sk_grid > 0) {
+        const size_t need = sk_grid > 0 ? tq_decode_workspace_bytes(d, 1) : tq_decode_workspace_bytes(d, splits);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TQ_ERR_WORKSPACE;
         const size_t pairs = (size_t)d->batch * d->n_kv_heads;
         const size_t tick = ((pairs * sizeof(int32_t)) + 255) & ~(size_t)255;
@@ -432,7 +452,7 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.Tcap = d->t_capacity;
     a.max_seq = max_seq_len;
     a.n_splits = splits;
-    a.split_len = (max_seq_len + splits - 1) / splits;
+    a.split_len = splits > 0 ? (max_seq_len + splits - 1) / splits : 0;
     if (mode == TQ_VMODE_TENSOR) {
         // sections start on 16-token tiles (16-byte aligned copies of codes and norms)
         const int al = tq_decode_tc_split_align();
@@ -445,7 +465,7 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.fold_mul = 1u << 20;
     if (d->batch > 65535 || d->n_kv_heads > 65535) return TQ_ERR_INVALID_ARG;
     if (mode == TQ_VMODE_TENSOR)
-        return tq_decode_tc_launch(d, a, splits, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+        return tq_decode_tc_launch(d, a, splits, sk_grid, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
     dim3 grid(splits, d->n_kv_heads, d->batch);
     fn<<<grid, kThreads, 0, (cudaStream_t)stream>>>(a);
     return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -509,7 +529,7 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_cache_desc* d, const t
     if (st != TQ_OK) return st;
     if (splits == 1) return tq_decode_attention_ex(d, c, q, q_dtype, d_seq_lens, max_seq_len, out, nullptr, 0,
                                                    d_status, stream, TQ_VMODE_AUTO, 1);
-    const size_t need = tq_decode_workspace_bytes(d, splits);
+    const size_t need = tq_decode_workspace_bytes(d, splits > 0 ? splits : 1);
     if (need == 0 || need > kNoAllocScratchBytes) return TQ_ERR_WORKSPACE;
     void* scratch = nullptr;
     st = scratch_address(&scratch);

@@ -220,25 +220,35 @@ __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*o
         __syncthreads();
         if (!*is_last) return;
         __threadfence();
-        // log-sum-exp merge over the splits  [Block-GTQ]
+        // log-sum-exp merge over the splits  [Block-GTQ]; the loads of a pass
+        // are independent of each other so that their latencies overlap
         const float* base = a.ws_part + (((size_t)b * a.Hkv + h) * a.n_splits * GP) * kPartStride;
+        float M[GP], lsum[GP], acc[GP];
+#pragma unroll
         for (int g = 0; g < GP; ++g) {
-            float M = -INFINITY;
-            for (int t = 0; t < a.n_splits; ++t) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
-            float lsum = 0.f, o = 0.f;
-            if (M != -INFINITY) {
-                for (int t = 0; t < a.n_splits; ++t) {
-                    const float* pr = base + ((size_t)t * GP + g) * kPartStride;
-                    const float mt = __ldcg(pr + 128);
-                    if (mt == -INFINITY) continue;
-                    const float w = exp2f(mt - M);
-                    lsum = fmaf(w, __ldcg(pr + 129), lsum);
-                    o = fmaf(w, __ldcg(pr + tid), o);
-                }
-            }
-            __syncthreads();
-            ot[g][tid] = lsum > 0.f ? o / lsum : 0.f;
+            M[g] = -INFINITY;
+            lsum[g] = 0.f;
+            acc[g] = 0.f;
         }
+#pragma unroll 4
+        for (int t = 0; t < a.n_splits; ++t) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) M[g] = fmaxf(M[g], __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
+        }
+#pragma unroll 4
+        for (int t = 0; t < a.n_splits; ++t) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                const float* pr = base + ((size_t)t * GP + g) * kPartStride;
+                const float mt = __ldcg(pr + 128), lt = __ldcg(pr + 129), ov = __ldcg(pr + tid);
+                const float w = mt == -INFINITY ? 0.f : exp2f(mt - M[g]);
+                lsum[g] = fmaf(w, lt, lsum[g]);
+                acc[g] = fmaf(w, ov, acc[g]);
+            }
+        }
+        // each thread rewrites only its own coordinate of ot
+#pragma unroll
+        for (int g = 0; g < GP; ++g) ot[g][tid] = lsum[g] > 0.f ? acc[g] / lsum[g] : 0.f;
         if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
         __syncthreads();
     } else {
@@ -265,4 +275,10 @@ __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*o
 // or group size has no tensor-core kernel.
 bool tq_decode_tc_supported(const tq_cache_desc* d);
 int tq_decode_tc_split_align();
-cudaError_t tq_decode_tc_launch(const tq_cache_desc* d, const tq::DecodeArgs& a, int splits, cudaStream_t stream);
+// Stream-K partition: partial slots the workspace must hold, and the grid (one
+// wave of resident CTAs; 0 when the occupancy cannot be read).
+int tq_decode_tc_sk_slots(const tq_cache_desc* d);
+int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len);
+// sk_grid > 0: stream-K over that many CTAs; else `splits` sections per pair.
+cudaError_t tq_decode_tc_launch(const tq_cache_desc* d, const tq::DecodeArgs& a, int splits, int sk_grid,
+                                cudaStream_t stream);

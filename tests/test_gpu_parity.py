@@ -194,6 +194,41 @@ def test_decode_tensor_tile_edges(tq, name, T):
         _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, n_splits)
 
 
+@pytest.mark.parametrize("name", TC_NAMES)
+def test_decode_streamk_matches_oracle(tq, name):
+    """Stream-K partition: every tile of every pair spread over one wave of
+    CTAs; ragged lengths put pair boundaries anywhere inside a CTA's range."""
+    B, T = SMALL[name]
+    B = max(B, 5)
+    seq_lens = W.ragged_lengths(B, T, 6)
+    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=_aligned_cap(T), seq_lens=seq_lens)
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.from_numpy(st.inp.seq_lens).cuda()
+    _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR_STREAMK, 0)
+    assert int(cache.status.item()) == 0
+
+
+def test_decode_streamk_empty_and_clamped(tq):
+    B, T = 4, 200
+    st, cache = _encode_on_gpu(tq, "llama8b", B, T, cap_extra=_aligned_cap(T))
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.tensor([0, T + 50, 0, 77], dtype=torch.int32, device="cuda")
+    out = cache.decode(q, sl, T, v_mode=tq.TQ_VMODE_TENSOR_STREAMK)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 0) and np.all(o[2] == 0)
+    assert int(cache.status.item()) & tq.TQ_DEV_SEQ_OVER_CAPACITY
+    G = st.wl.group
+    for b, L in ((1, T), (3, 77)):
+        for h in range(st.wl.n_kv_heads):
+            ek, ev = encs[(b, h)]
+            ref = oracle_attention(st, ek, ev, b, h, L)
+            e, s = att_error(o[b, h * G:(h + 1) * G], ref)
+            assert e <= ATT_TOL * s
+
+
 def test_seq_len_zero_and_clamping(tq):
     B, T = 3, 200
     st, cache = _encode_on_gpu(tq, "llama8b", B, T, cap_extra=0)
