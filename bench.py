@@ -256,7 +256,8 @@ def run_ours(args, wl, T, rank, world, local_rank):
     start = torch.full((wl.batch,), T - 1, dtype=torch.int32, device=dev)
     seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
     out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
-    splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_AUTO, args.splits)
+    splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_TENSOR_STREAMK if args.streamk else tq.TQ_VMODE_AUTO,
+                                      args.splits)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     in_code = tq._dtype_code(q)
@@ -390,6 +391,7 @@ def main():
     ap.add_argument("--batch", type=int, default=32, help="smaller batches are for profiling captures only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=0, help="key-axis splits (0: the library's plan)")
+    ap.add_argument("--streamk", action="store_true", help="tensor-core kernel with the stream-K partition")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -35,12 +35,21 @@
 
 namespace {
 
+// section kernel: two tiles per softmax step (1) or one (0)
+#ifndef TQ_TC_TWO_TILES
+#define TQ_TC_TWO_TILES 0
+#endif
+// value operands through byte-permute lookups (1) or the shared-memory table (0)
+#ifndef TQ_TC_V_PRMT
+#define TQ_TC_V_PRMT 0
+#endif
+
 constexpr int kTile = 16;
 #ifndef TQ_TC_STAGES
 #define TQ_TC_STAGES 3
 #endif
 #ifndef TQ_TC_MIN_BLOCKS
-#define TQ_TC_MIN_BLOCKS 5
+#define TQ_TC_MIN_BLOCKS (TQ_TC_TWO_TILES ? 4 : 5)
 #endif
 
 constexpr int kStages = TQ_TC_STAGES;   // cp.async ring depth per warp
@@ -65,7 +74,7 @@ struct TcFinal {
 
 struct TcSmem {
     union {
-        TcStage ring[4][kStages];
+        TcStage ring[4][4];   // 4 stages per warp: two tiles processed, two in flight
         TcFinal fin;
     };
     alignas(16) float qts[8][128];
@@ -193,6 +202,67 @@ struct Seg {
     int b, h, L, t_lo, t_hi, slot, first, parts, off;
 };
 
+// ---- byte-permute route (integer pipe instead of shared memory)
+//
+// Two 8-byte pools hold the low and the high bytes of the fp16 codebook (scaled
+// as the table).  In a 48-bit window of 16 codes, code pairs (PP[i], QQ[i]) sit
+// at the same bit offset of two bytes three bytes apart; the same two bytes of a
+// second token's window complete a selector of four 3-bit indices, and two PRMT
+// lookups plus two byte merges give (A@PP, A@QQ) and (B@PP, B@QQ) as fp16x2.
+__host__ __device__ constexpr int pp_of(int i) { return i < 2 ? i : i < 4 ? i + 1 : i < 6 ? i + 2 : i == 6 ? 2 : 5; }
+__host__ __device__ constexpr int qq_of(int i) { return pp_of(i) + 8; }
+
+struct Pools {
+    uint32_t lo0, lo1, hi0, hi1;
+};
+
+__device__ __forceinline__ Pools make_pools(const float* cent, float sc) {
+    uint32_t u[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = __half_as_ushort(__float2half_rn(sc * cent[i]));
+    Pools p;
+    p.lo0 = (u[0] & 255u) | ((u[1] & 255u) << 8) | ((u[2] & 255u) << 16) | ((u[3] & 255u) << 24);
+    p.lo1 = (u[4] & 255u) | ((u[5] & 255u) << 8) | ((u[6] & 255u) << 16) | ((u[7] & 255u) << 24);
+    p.hi0 = (u[0] >> 8) | ((u[1] >> 8) << 8) | ((u[2] >> 8) << 16) | ((u[3] >> 8) << 24);
+    p.hi1 = (u[4] >> 8) | ((u[5] >> 8) << 8) | ((u[6] >> 8) << 16) | ((u[7] >> 8) << 24);
+    return p;
+}
+
+// Five byte-offset views of a 48-bit window starting at bit `base` of (wa, wb).
+struct Win {
+    uint32_t b, f8, f16, s0, s8;
+};
+
+__device__ __forceinline__ Win make_win(uint32_t wa, uint32_t wb, uint32_t base) {
+    Win w;
+    w.b = __funnelshift_rc(wa, wb, base);         // window bytes 0-3
+    w.f8 = __funnelshift_rc(wa, wb, base + 8);    // bytes 1-4
+    w.f16 = __funnelshift_rc(wa, wb, base + 16);  // bytes 2-5
+    w.s0 = __funnelshift_rc(wa, wb, base + 2);    // window >> 2: codes 2, 10 byte-aligned
+    w.s8 = __funnelshift_rc(wa, wb, base + 10);   // window >> 10: codes 5, 13
+    return w;
+}
+
+template <int V>
+__device__ __forceinline__ uint32_t view(const Win& w) {
+    return V == 0 ? w.b : V == 1 ? w.f8 : V == 2 ? w.f16 : V == 3 ? w.s0 : w.s8;
+}
+
+// pattern I of a window pair: X = (A@PP[I], A@QQ[I]), Y = (B@PP[I], B@QQ[I])
+template <int I>
+__device__ __forceinline__ void pattern(const Win& A, const Win& B, const Pools& pl, uint32_t fm, uint32_t& X,
+                                        uint32_t& Y) {
+    constexpr int V = I < 2 ? 0 : I < 4 ? 1 : I < 6 ? 2 : I == 6 ? 3 : 4;
+    constexpr int O = I == 0 ? 0 : I == 1 ? 3 : I == 2 ? 1 : I == 3 ? 4 : I == 4 ? 2 : I == 5 ? 5 : I == 6 ? 4 : 5;
+    const uint32_t H = __byte_perm(view<V>(A), view<V>(B), 0x7430);   // [A.bi, A.bj, B.bi, B.bj]
+    const uint32_t t = (O ? __umulhi(H, 1u << (32 - O)) : H) & 0x07070707u;
+    uint32_t sel;
+    asm("mad.hi.u32 %0, %1, %2, %1;" : "=r"(sel) : "r"(t), "r"(fm));   // t + (t >> 12): nibbles (A@p, B@p, A@q, B@q)
+    const uint32_t rl = __byte_perm(pl.lo0, pl.lo1, sel), rh = __byte_perm(pl.hi0, pl.hi1, sel);
+    X = __byte_perm(rl, rh, 0x6240);
+    Y = __byte_perm(rl, rh, 0x7351);
+}
+
 // ---- one 16-token tile of one warp
 
 struct LaneCtx {
@@ -201,10 +271,14 @@ struct LaneCtx {
     int vw;                               // first word of the lane row's 48-bit value window
     uint32_t vsh;                         // its bit offset in that word
     uint32_t selA0, selB0, selA1, selB1;  // PRMT selectors building the PV operand B
+    Pools pv;                             // value codebook byte pools (byte-permute route)
+    uint32_t fm;                          // 1 << 20
 };
 
-__device__ __forceinline__ LaneCtx lane_ctx() {
+__device__ __forceinline__ LaneCtx lane_ctx(const DecodeArgs& a) {
     LaneCtx lc;
+    lc.pv = make_pools(a.params[0].v_cent[0], a.params[0].v_h_scale[0]);
+    lc.fm = a.fold_mul;
     const int lane = threadIdx.x & 31;
     lc.lane4 = 4u * lane;
     lc.r = lane >> 2;
@@ -254,6 +328,50 @@ __device__ __forceinline__ void load_bq(const float (*qts)[128], const LaneCtx& 
             bq[j][st][1] = pack_h2(qh[d1], qh[d1 + 1]);
         }
     }
+}
+
+// PV for one staged tile with operand B `bp` (k steps u = 0, 1).  Row r / r + 8
+// of m tile mt is a coordinate pair of the lane row's 48-bit window: with the
+// table, fields 2mt / 2mt + 1 (coordinates 16r + 4mt + {0, 1} / {2, 3}); with
+// byte permutes, patterns 2mt / 2mt + 1 (coordinates 16r + PP, QQ of each).
+template <int NT>
+__device__ __forceinline__ void pv_tile(const TcStage& sg, const uint32_t (&bp)[NT][2][2], const uint32_t* tab,
+                                        const LaneCtx& lc, WState<NT>& ws) {
+    const int c = lc.c;
+    unroll<2>([&](auto u_c) {
+        constexpr int u = decltype(u_c)::value;
+        const int ta = 8 * u + 2 * c;
+        const uint32_t* va = reinterpret_cast<const uint32_t*>(sg.v + ta * kRec) + lc.vw;
+        const uint32_t* vb = reinterpret_cast<const uint32_t*>(sg.v + (ta + 1) * kRec) + lc.vw;
+        if constexpr (TQ_TC_V_PRMT) {
+            const Win A = make_win(va[0], va[1], lc.vsh), B = make_win(vb[0], vb[1], lc.vsh);
+            unroll<4>([&](auto mt_c) {
+                constexpr int mt = decltype(mt_c)::value;
+                uint32_t a0, a1, a2, a3;
+                pattern<2 * mt>(A, B, lc.pv, lc.fm, a0, a2);
+                pattern<2 * mt + 1>(A, B, lc.pv, lc.fm, a1, a3);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma16816(ws.o[j][mt], a0, a1, a2, a3, bp[j][u][0], bp[j][u][1]);
+            });
+        } else {
+            const uint32_t LA = __funnelshift_r(va[0], va[1], lc.vsh), HA = va[1] >> lc.vsh;
+            const uint32_t LB = __funnelshift_r(vb[0], vb[1], lc.vsh), HB = vb[1] >> lc.vsh;
+            unroll<4>([&](auto mt_c) {
+                constexpr int mt = decltype(mt_c)::value;
+                const uint32_t a0 = tab_lk(tab, vfield7<2 * mt>(LA, HA), lc.lane4);
+                const uint32_t a1 = tab_lk(tab, vfield7<2 * mt + 1>(LA, HA), lc.lane4);
+                const uint32_t a2 = tab_lk(tab, vfield7<2 * mt>(LB, HB), lc.lane4);
+                const uint32_t a3 = tab_lk(tab, vfield7<2 * mt + 1>(LB, HB), lc.lane4);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma16816(ws.o[j][mt], a0, a1, a2, a3, bp[j][u][0], bp[j][u][1]);
+            });
+        }
+    });
+}
+
+// output coordinate (within the lane row's 16) of o[mt][q]
+__device__ __forceinline__ constexpr int pv_coord(int mt, int q) {
+    return TQ_TC_V_PRMT ? ((q & 1) ? qq_of(2 * mt + (q >> 1)) : pp_of(2 * mt + (q >> 1))) : 4 * mt + q;
 }
 
 // QK, online softmax and PV for one staged tile of `nval` valid tokens.
@@ -340,25 +458,112 @@ __device__ __forceinline__ void tile_step(const TcStage& sg, int nval, const uin
         bp[j][1][1] = movtrans(prmt(X, Y, lc.selB1));
     }
 
-    // ---- PV (coordinate-pair form): row r / r + 8 of m tile mt = pair
-    // 8r + 2mt / 8r + 2mt + 1, i.e. fields 2mt / 2mt + 1 of the lane row's window
-    unroll<2>([&](auto u_c) {
-        constexpr int u = decltype(u_c)::value;
-        const int ta = 8 * u + 2 * c;
-        const uint32_t* va = reinterpret_cast<const uint32_t*>(sg.v + ta * kRec) + lc.vw;
-        const uint32_t* vb = reinterpret_cast<const uint32_t*>(sg.v + (ta + 1) * kRec) + lc.vw;
-        const uint32_t LA = __funnelshift_r(va[0], va[1], lc.vsh), HA = va[1] >> lc.vsh;
-        const uint32_t LB = __funnelshift_r(vb[0], vb[1], lc.vsh), HB = vb[1] >> lc.vsh;
-        unroll<4>([&](auto mt_c) {
-            constexpr int mt = decltype(mt_c)::value;
-            const uint32_t a0 = tab_lk(tab, vfield7<2 * mt>(LA, HA), lane4);
-            const uint32_t a1 = tab_lk(tab, vfield7<2 * mt + 1>(LA, HA), lane4);
-            const uint32_t a2 = tab_lk(tab, vfield7<2 * mt>(LB, HB), lane4);
-            const uint32_t a3 = tab_lk(tab, vfield7<2 * mt + 1>(LB, HB), lane4);
+    pv_tile<NT>(sg, bp, tab, lc, ws);
+}
+
+// Two full tiles at once: the same products, one softmax step over their 32
+// tokens (one max reduction, one rescale), and twice the independent work in
+// flight for the warp.
+template <int NT>
+__device__ __forceinline__ void tile_step2(const TcStage& sa, const TcStage& sb, const uint32_t (&bq)[NT][8][2],
+                                           const uint32_t* tab, const LaneCtx& lc, float kinv, int norm_f16,
+                                           WState<NT>& ws) {
+    constexpr int NC = 4 / NT;
+    const int r = lc.r, c = lc.c;
+    const uint32_t lane4 = lc.lane4;
+    const TcStage* sg[2] = {&sa, &sb};
+
+    // ---- QK for both tiles
+    uint32_t x[2][3], y[2][3];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) mma16816(ws.o[j][mt], a0, a1, a2, a3, bp[j][u][0], bp[j][u][1]);
-        });
+    for (int tt = 0; tt < 2; ++tt) {
+        const uint32_t* kA = reinterpret_cast<const uint32_t*>(sg[tt]->k + r * kRec) + 3 * c;
+        const uint32_t* kB = reinterpret_cast<const uint32_t*>(sg[tt]->k + (r + 8) * kRec) + 3 * c;
+        x[tt][0] = kA[0]; x[tt][1] = kA[1]; x[tt][2] = kA[2];
+        y[tt][0] = kB[0]; y[tt][1] = kB[1]; y[tt][2] = kB[2];
+    }
+    float acc[2][NT][NC][4];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int q = 0; q < NC; ++q) acc[tt][j][q][0] = acc[tt][j][q][1] = acc[tt][j][q][2] = acc[tt][j][q][3] = 0.f;
+    unroll<8>([&](auto st_c) {
+        constexpr int st = decltype(st_c)::value;
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            const uint32_t a0 = tab_lk(tab, kfield7<st>(x[tt][0], x[tt][1], x[tt][2]), lane4);
+            const uint32_t a1 = tab_lk(tab, kfield7<st>(y[tt][0], y[tt][1], y[tt][2]), lane4);
+            const uint32_t a2 = tab_lk(tab, kfield7<st + 8>(x[tt][0], x[tt][1], x[tt][2]), lane4);
+            const uint32_t a3 = tab_lk(tab, kfield7<st + 8>(y[tt][0], y[tt][1], y[tt][2]), lane4);
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+                mma16816(acc[tt][j][st % NC], a0, a1, a2, a3, bq[j][st][0], bq[j][st][1]);
+        }
     });
+
+    // ---- one online-softmax step over both tiles (log2 units)
+    float kn[2][2], vn[2][2];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+        kn[tt][0] = ldnorm(sg[tt]->kn, r, norm_f16) * kinv;
+        kn[tt][1] = ldnorm(sg[tt]->kn, r + 8, norm_f16) * kinv;
+        vn[tt][0] = ldnorm(sg[tt]->vn, r, norm_f16);
+        vn[tt][1] = ldnorm(sg[tt]->vn, r + 8, norm_f16);
+    }
+    uint32_t bp[2][NT][2][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        float sc[2][2];
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            float s0 = acc[tt][j][0][0], s8 = acc[tt][j][0][2];
+#pragma unroll
+            for (int q = 1; q < NC; ++q) {
+                s0 += acc[tt][j][q][0];
+                s8 += acc[tt][j][q][2];
+            }
+            sc[tt][0] = s0 * kn[tt][0];
+            sc[tt][1] = s8 * kn[tt][1];
+        }
+        float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 16));
+        const float mn = mt > ws.m[j] + 4.f ? mt : ws.m[j];
+        const float cf = ex2(ws.m[j] - mn);
+        ws.m[j] = mn;
+        float lsum = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            const float p0 = ex2(sc[tt][0] - mn), p8 = ex2(sc[tt][1] - mn);
+            lsum += p0 + p8;
+            const uint32_t X = pack_h2(p0 * vn[tt][0], p8 * vn[tt][1]);
+            const uint32_t Y = __shfl_xor_sync(TQ_FULL_MASK, X, 4);
+            bp[tt][j][0][0] = movtrans(prmt(X, Y, lc.selA0));
+            bp[tt][j][0][1] = movtrans(prmt(X, Y, lc.selB0));
+            bp[tt][j][1][0] = movtrans(prmt(X, Y, lc.selA1));
+            bp[tt][j][1][1] = movtrans(prmt(X, Y, lc.selB1));
+        }
+        ws.l[j] = fmaf(ws.l[j], cf, lsum);
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+            ws.o[j][m4][0] *= cf; ws.o[j][m4][1] *= cf; ws.o[j][m4][2] *= cf; ws.o[j][m4][3] *= cf;
+        }
+    }
+
+    // ---- PV for both tiles
+    uint32_t bpa[NT][2][2], bpb[NT][2][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            bpa[j][u][0] = bp[0][j][u][0]; bpa[j][u][1] = bp[0][j][u][1];
+            bpb[j][u][0] = bp[1][j][u][0]; bpb[j][u][1] = bp[1][j][u][1];
+        }
+    pv_tile<NT>(sa, bpa, tab, lc, ws);
+    pv_tile<NT>(sb, bpb, tab, lc, ws);
 }
 
 // A warp's state into its merge slot: wo[g][128], wm[g], wl[g] for its heads.
@@ -373,10 +578,11 @@ __device__ __forceinline__ void warp_state_out(WState<NT>& ws, const LaneCtx& lc
             wm[4 * j + lc.c] = ws.m[j];
             wl[4 * j + lc.c] = ws.l[j];
         }
-        float4* dst = reinterpret_cast<float4*>(&wo[4 * j + lc.c][16 * lc.r]);
+        float* dst = &wo[4 * j + lc.c][16 * lc.r];
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
-            dst[mt] = make_float4(ws.o[j][mt][0], ws.o[j][mt][1], ws.o[j][mt][2], ws.o[j][mt][3]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[pv_coord(mt, q)] = ws.o[j][mt][q];
     }
 }
 
@@ -534,7 +740,7 @@ __device__ __forceinline__ void issue_tile(const DecodeArgs& a, uint32_t dst, in
 // ---- explicit splits: one CTA of 4 warps per (section, KV head, batch); its
 // warps take the section's tiles round-robin
 template <int GPE, int EP>
-__global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 4) decode_tc(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 3) decode_tc(DecodeArgs a) {
     constexpr int NT = GPE / 4;
     __shared__ TcSmem S;
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -557,29 +763,57 @@ __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 4) dec
     const int nseg = sg.t_hi - sg.t_lo;
     const int nmine = nseg > warp ? (nseg - warp + 3) / 4 : 0;   // this warp: tiles t_lo + warp + 4i
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(S.ring[warp]);
+    constexpr uint32_t kStageBytes = (uint32_t)sizeof(TcStage);
+    auto tile_of = [&](int i) { return sg.t_lo + warp + 4 * i; };
+    constexpr int kAhead = TQ_TC_TWO_TILES ? 2 : 3;   // tiles in flight beyond those being processed
 #pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) {   // start the stream before the q rotation
-        if (k < nmine) issue_tile(a, ring_s + k * (uint32_t)sizeof(TcStage), b, h, L, sg.t_lo + warp + 4 * k);
+    for (int k = 0; k < kAhead; ++k) {   // start the stream before the q rotation
+        if (k < nmine) issue_tile(a, ring_s + k * kStageBytes, b, h, L, tile_of(k));
         cp_async_commit();
     }
     for (int g = warp; g < GPE; g += 4) rotate_q(a, P, b, h, g, S.qts[g]);
     const float kinv = 1.0f / P.k_h_scale[0], vinv = 1.0f / P.v_h_scale[0];
     __syncthreads();
-    const LaneCtx lc = lane_ctx();
+    const LaneCtx lc = lane_ctx(a);
     uint32_t bq[NT][8][2];
     load_bq<NT>(S.qts, lc, bq);
     WState<NT> ws;
     ws.reset();
-    for (int i = 0; i < nmine; ++i) {
-        if (i + kStages - 1 < nmine)
-            issue_tile(a, ring_s + ((i + kStages - 1) % kStages) * (uint32_t)sizeof(TcStage), b, h, L,
-                       sg.t_lo + warp + 4 * (i + kStages - 1));
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const int nval = min(kTile, L - (sg.t_lo + warp + 4 * i) * kTile);
-        tile_step<NT>(S.ring[warp][i % kStages], nval, bq, S.tab, lc, kinv, a.norm_f16, ws);
-        __syncwarp();
+    if constexpr (TQ_TC_TWO_TILES) {
+        for (int i = 0; i < nmine; i += 2) {
+#pragma unroll
+            for (int k = 2; k < 4; ++k) {
+                if (i + k < nmine) issue_tile(a, ring_s + ((i + k) % 4) * kStageBytes, b, h, L, tile_of(i + k));
+                cp_async_commit();
+            }
+            cp_async_wait<2>();
+            __syncwarp();
+            const int nva = min(kTile, L - tile_of(i) * kTile);
+            const TcStage& sa = S.ring[warp][i % 4];
+            if (i + 1 < nmine) {
+                const int nvb = min(kTile, L - tile_of(i + 1) * kTile);
+                const TcStage& sb = S.ring[warp][(i + 1) % 4];
+                if (nva == kTile && nvb == kTile) {
+                    tile_step2<NT>(sa, sb, bq, S.tab, lc, kinv, a.norm_f16, ws);
+                } else {
+                    tile_step<NT>(sa, nva, bq, S.tab, lc, kinv, a.norm_f16, ws);
+                    tile_step<NT>(sb, nvb, bq, S.tab, lc, kinv, a.norm_f16, ws);
+                }
+            } else {
+                tile_step<NT>(sa, nva, bq, S.tab, lc, kinv, a.norm_f16, ws);
+            }
+            __syncwarp();
+        }
+    } else {
+        for (int i = 0; i < nmine; ++i) {
+            if (i + 3 < nmine) issue_tile(a, ring_s + ((i + 3) % 4) * kStageBytes, b, h, L, tile_of(i + 3));
+            cp_async_commit();
+            cp_async_wait<3>();
+            __syncwarp();
+            tile_step<NT>(S.ring[warp][i % 4], min(kTile, L - tile_of(i) * kTile), bq, S.tab, lc, kinv, a.norm_f16,
+                          ws);
+            __syncwarp();
+        }
     }
     cp_async_wait<0>();
     __syncthreads();   // every warp is done with its ring before it is reused
@@ -594,10 +828,8 @@ __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 4) dec
 // ---- stream-K: one persistent CTA of NW warps per SM
 //
 // The CTA's warps claim the tiles of its range one at a time, in order, so that
-// a warp that runs ahead takes more of them.  When a warp is past a segment it
-// leaves its softmax state in the segment's slot set (two sets, by segment
-// parity) and goes on; the last warp to leave merges the set, finishes the
-// segment and frees the set for the segment after next.
+// a warp that runs ahead takes more of them; at the end of a segment the CTA
+// merges its warps' states (the ring keeps streaming the next segment's tiles).
 template <int GPE>
 constexpr int sk_warps() { return GPE <= 4 ? 16 : 8; }
 
@@ -605,106 +837,21 @@ template <int GPE>
 struct SkSmem {
     static constexpr int NW = sk_warps<GPE>();
     TcStage ring[NW][kStages];
-    float wo[2][NW][GPE][128];
-    float wm[2][NW][8];
-    float wl[2][NW][8];
-    float wt[2][NW][8];        // merge weights 2^(m_w - M)
-    float ot[2][8][128];
-    float mm[2][8], ll[2][8];
+    float wo[NW][GPE][128];
+    float wm[NW][8];
+    float wl[NW][8];
+    float ot[8][128];
+    float mm[8], ll[8];
     float qts[kSkSegs][GPE][128];
     uint32_t tab[64 * 32];
     Seg seg[kSkSegs + 1];
     long long scan[NW];
     long long b_base, next_pos, cur_base;
-    int b_first, cur_b, nseg, round_tiles, claim;
-    int arrived[2];            // warps past the segment using slot set p
-    volatile int freed[2];     // slot set p may take the state of segment freed[p] (and later ones)
+    int b_first, cur_b, nseg, round_tiles, claim, is_last;
 };
 
 template <int GPE>
 constexpr size_t sk_smem_bytes() { return sizeof(SkSmem<GPE>); }
-
-// Merge the NW warp states of one slot set into ot/mm/ll and finish the segment
-// (publish its partial or normalise, then the inverse rotation); one warp.
-template <int GPE, int EP>
-__device__ void sk_merge_finish(const DecodeArgs& a, SkSmem<GPE>& S, int p, const Seg& sg, float vinv) {
-    constexpr int NW = SkSmem<GPE>::NW;
-    const int lane = threadIdx.x & 31;
-    const tq_head_params& P = a.params[sg.h];
-    if (lane < EP) {
-        float M = -INFINITY;
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, S.wm[p][w][lane]);
-        float Lt = 0.f;
-        for (int w = 0; w < NW; ++w) {
-            const float m = S.wm[p][w][lane];
-            const float wt = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
-            S.wt[p][w][lane] = wt;
-            Lt = fmaf(wt, S.wl[p][w][lane], Lt);
-        }
-        S.mm[p][lane] = M;
-        S.ll[p][lane] = Lt;
-    }
-    __syncwarp();
-    for (int i = lane; i < EP * 128; i += 32) {
-        const int g = i >> 7, d = i & 127;
-        float ov = 0.f;
-#pragma unroll 4
-        for (int w = 0; w < NW; ++w) ov = fmaf(S.wt[p][w][g], S.wo[p][w][g][d], ov);
-        S.ot[p][g][d] = ov * vinv;   // the value table carried the scale s_V
-    }
-    __syncwarp();
-    float (*ot)[128] = S.ot[p];
-    const int pair = sg.b * a.Hkv + sg.h;
-    if (sg.parts > 1) {
-        float* part = a.ws_part + (size_t)sg.slot * EP * kPartStride;
-        for (int i = lane; i < EP * 128; i += 32) part[(i >> 7) * kPartStride + (i & 127)] = ot[i >> 7][i & 127];
-        if (lane < EP) {
-            part[lane * kPartStride + 128] = S.mm[p][lane];
-            part[lane * kPartStride + 129] = S.ll[p][lane];
-        }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(a.tickets + pair, 1) == sg.parts - 1;
-        if (!__shfl_sync(TQ_FULL_MASK, last, 0)) return;
-        __threadfence();
-        // log-sum-exp merge over the pair's parts  [Block-GTQ]
-        const float* base = a.ws_part + (size_t)sg.first * EP * kPartStride;
-        for (int i = lane; i < EP * 128; i += 32) {
-            const int g = i >> 7, d = i & 127;
-            float M = -INFINITY;
-#pragma unroll 4
-            for (int t = 0; t < sg.parts; ++t) M = fmaxf(M, __ldcg(base + ((size_t)t * EP + g) * kPartStride + 128));
-            float lsum = 0.f, acc = 0.f;
-#pragma unroll 4
-            for (int t = 0; t < sg.parts; ++t) {
-                const float* pr = base + ((size_t)t * EP + g) * kPartStride;
-                const float mt = __ldcg(pr + 128), lt = __ldcg(pr + 129), ov = __ldcg(pr + d);
-                const float w = mt == -INFINITY ? 0.f : exp2f(mt - M);
-                lsum = fmaf(w, lt, lsum);
-                acc = fmaf(w, ov, acc);
-            }
-            ot[g][d] = lsum > 0.f ? acc / lsum : 0.f;
-        }
-        if (lane == 0) a.tickets[pair] = 0;   // ready for the next call
-    } else {
-        for (int i = lane; i < EP * 128; i += 32) {
-            const int g = i >> 7;
-            const float l = S.ll[p][g];
-            ot[g][i & 127] = l > 0.f ? ot[g][i & 127] / l : 0.f;
-        }
-    }
-    __syncwarp();
-    // o = R_V^T o~, once per query head  [RotaryQuant Key design 3, Kernel D]
-    for (int g = 0; g < a.G; ++g) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = ot[g][4 * lane + i];
-        tq::rotate_inverse(a.rot, P, v);
-        float4* o4 = reinterpret_cast<float4*>(a.out + ((size_t)sg.b * a.Hq + (size_t)sg.h * a.G + g) * 128) + lane;
-        *o4 = make_float4(v[0], v[1], v[2], v[3]);
-    }
-}
 
 template <int GPE, int EP>
 __global__ void __launch_bounds__(sk_warps<GPE>() * 32, 1) decode_sk(DecodeArgs a) {
@@ -761,7 +908,7 @@ __global__ void __launch_bounds__(sk_warps<GPE>() * 32, 1) decode_sk(DecodeArgs 
         S.cur_b = S.b_first;
         S.cur_base = S.b_base;
     }
-    const LaneCtx lc = lane_ctx();
+    const LaneCtx lc = lane_ctx(a);
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(S.ring[warp]);
     constexpr uint32_t kStageBytes = (uint32_t)sizeof(TcStage);
 
@@ -807,9 +954,6 @@ __global__ void __launch_bounds__(sk_warps<GPE>() * 32, 1) decode_sk(DecodeArgs 
             S.next_pos = p;
             S.cur_b = b;
             S.cur_base = base;
-            S.arrived[0] = S.arrived[1] = 0;
-            S.freed[0] = 0;   // set p first serves segment p
-            S.freed[1] = 1;
         }
         __syncthreads();
         const int nseg = S.nseg, round_tiles = S.round_tiles;
@@ -865,37 +1009,12 @@ __global__ void __launch_bounds__(sk_warps<GPE>() * 32, 1) decode_sk(DecodeArgs 
                 head = head + 1 == kStages ? 0 : head + 1;
                 __syncwarp();
             }
-            // leave the state in slot set k & 1 once the merge of segment k - 2 freed it
-            const int p = k & 1;
-            if (lane == 0) {
-                int spins = 0;
-                while (S.freed[p] < k) {
-                    __nanosleep(64);
-                    if (++spins > (1 << 24)) {   // never expected; report instead of hanging
-                        if (a.status) atomicOr(a.status, TQ_DEV_WAIT_TIMEOUT);
-                        break;
-                    }
-                }
-            }
-            __syncwarp();
-            __threadfence_block();
-            warp_state_out<NT>(ws, lc, S.wo[p][warp], S.wm[p][warp], S.wl[p][warp]);
-            __threadfence_block();
-            __syncwarp();
-            int arrived = 0;
-            if (lane == 0) arrived = atomicAdd(&S.arrived[p], 1);
-            arrived = __shfl_sync(TQ_FULL_MASK, arrived, 0);
-            if (arrived == NW - 1) {   // last warp past segment k: merge and finish it
-                __threadfence_block();
-                sk_merge_finish<GPE, EP>(a, S, p, sg, vinv);
-                __syncwarp();
-                if (lane == 0) {
-                    S.arrived[p] = 0;
-                    __threadfence_block();
-                    S.freed[p] = k + 2;
-                }
-                __syncwarp();
-            }
+            warp_state_out<NT>(ws, lc, S.wo[warp], S.wm[warp], S.wl[warp]);
+            __syncthreads();
+            merge_warps<EP, NTHR>(NW, &S.wo[0][0][0], GPE * 128, S.wm, S.wl, vinv, S.ot, S.mm, S.ll);
+            __syncthreads();
+            finish_segment<EP, NTHR>(a, P, S.ot, S.mm, S.ll, &S.is_last, sg);
+            __syncthreads();
         }
         cp_async_wait<0>();
     }
