@@ -56,7 +56,6 @@ typedef int32_t tq_status;
 #define TQ_DEV_SEQ_OVER_CAPACITY  1  /* seq_len > t_capacity: clamped          */
 #define TQ_DEV_SEQ_OVER_MAX       2  /* seq_len > max_seq_len: clamped         */
 #define TQ_DEV_BAD_POSITION       4  /* append position outside [0, capacity): skipped */
-#define TQ_DEV_WAIT_TIMEOUT       8  /* a bounded wait inside a kernel gave up: the output of that call is invalid */
 
 /* ---------------------------------------------------------------- enums */
 #define TQ_F32   0
