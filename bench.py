@@ -246,9 +246,19 @@ def run_ours(args, wl, T, rank, world, local_rank):
     K = to_torch_input(torch, inp.K, wl.in_dtype, dev)
     V = to_torch_input(torch, inp.V, wl.in_dtype, dev)
     zero = torch.zeros(wl.batch, dtype=torch.int32, device=dev)
-    for c in caches:
+    pf = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    for i, c in enumerate(caches):
+        if i == 1:
+            pf[0].record()
         c.append(K, V, zero)
+        if i == 1:
+            pf[1].record()
     torch.cuda.synchronize()
+    # whole-prompt append (write side W1-W4 over every token), timed on the second cache
+    pf_us = pf[0].elapsed_time(pf[1]) * 1e3
+    pf_bytes = (K.numel() + V.numel()) * K.element_size() + 2 * wl.batch * wl.n_kv_heads * T * (48 + 2)
+    prefill = {"tokens": wl.batch * T, "us": pf_us, "GB/s": pf_bytes / (pf_us * 1e-6) / 1e9,
+               "bytes": pf_bytes}
     k_new = K[:, T - 1:T].contiguous()
     v_new = V[:, T - 1:T].contiguous()
     del K, V
@@ -367,6 +377,7 @@ def run_ours(args, wl, T, rank, world, local_rank):
                 "us_per_step": e2e_ms / args.steps * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
+        "prefill_append": prefill,
     }
     if world == 1 and not args.no_cpu_baseline:
         leg = OracleLeg(wl, T, n_pairs=2)

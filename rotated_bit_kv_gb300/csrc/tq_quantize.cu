@@ -27,28 +27,40 @@ struct QuantArgs {
 };
 
 constexpr int kWarps = 8;
+constexpr long long kMaxBlocks = 152LL * 8 * 4;   // four waves of 8 resident CTAs per SM
 
-__global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
-    __shared__ float xs_all[kWarps][128];
+// Vector index (warp-uniform): K and V alternate, then KV head, token, batch.
+struct VecId {
+    int which, h, t, b;
+};
+
+__device__ __forceinline__ VecId vec_id(const QuantArgs& a, uint32_t v_all) {
+    VecId id;
+    id.which = (int)(v_all & 1u);
+    const uint32_t v = v_all >> 1;
+    const uint32_t q = v / (uint32_t)a.Hkv;
+    id.h = (int)(v - q * (uint32_t)a.Hkv);
+    const uint32_t bb = q / (uint32_t)a.n_new;
+    id.t = (int)(q - bb * (uint32_t)a.n_new);
+    id.b = (int)bb;
+    return id;
+}
+
+__device__ __forceinline__ size_t input_elem(const QuantArgs& a, const VecId& id) {
+    return (((size_t)id.b * a.n_new + id.t) * a.Hkv + id.h) * 128 + 4 * (threadIdx.x & 31);
+}
+
+// Encode one vector; xin holds this lane's 4 input values.
+__device__ __forceinline__ void encode_vector(const QuantArgs& a, const VecId& id, const float* xin, float* xs) {
     const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
-    const long long warp = (long long)blockIdx.x * kWarps + wib;
-    const long long total = 2LL * a.B * a.n_new * a.Hkv;
-    if (warp >= total) return;
-    const int which = (int)(warp & 1);          // 0 = K, 1 = V
-    const long long v = warp >> 1;
-    const int h = (int)(v % a.Hkv);
-    const int t = (int)((v / a.Hkv) % a.n_new);
-    const int b = (int)(v / ((long long)a.Hkv * a.n_new));
+    const int which = id.which, h = id.h, t = id.t, b = id.b;
     const int slot = a.start_pos[b] + t;
     if (slot < 0 || slot >= a.Tcap) {
         if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
         return;
     }
     const tq_head_params& P = a.params[h];
-    const size_t elem = (((size_t)b * a.n_new + t) * a.Hkv + h) * 128 + 4 * lane;
-    float x[4];
-    tq::load4(a.src[which], elem, a.in_dtype, x);
+    float x[4] = {xin[0], xin[1], xin[2], xin[3]};
 
     const bool mixed = which == 0 && a.k_mixed;
     const int32_t* seg_start = which == 0 ? P.k_seg_start : P.v_seg_start;
@@ -84,7 +96,6 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
             nrm[0] = n;
         }
     } else {
-        float* xs = xs_all[wib];
 #pragma unroll
         for (int i = 0; i < 4; ++i) xs[4 * lane + i] = x[i];
         __syncwarp();
@@ -114,17 +125,33 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
 
     // codebook search: idx = #{k : y > boundary_k}
     uint32_t idx[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int s = segi[i];
+    if (!mixed && seg_bits[segi[0]] <= 4) {
+        // one segment per lane: its boundaries in registers, an unrolled count
+        const int s = segi[0];
         const int nb = (1 << seg_bits[s]) - 1;
-        uint32_t c = 0;
-        for (int k = 0; k < nb; ++k) c += y[i] > bound[s][k] ? 1u : 0u;
-        idx[i] = c;
+        float bd[15];
+#pragma unroll
+        for (int k = 0; k < 15; ++k) bd[k] = k < nb ? bound[s][k] : INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int k = 0; k < 15; ++k) c += y[i] > bd[k] ? 1u : 0u;
+            idx[i] = c;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int s = segi[i];
+            const int nb = (1 << seg_bits[s]) - 1;
+            uint32_t c = 0;
+            for (int k = 0; k < nb; ++k) c += y[i] > bound[s][k] ? 1u : 0u;
+            idx[i] = c;
+        }
     }
 
     // pack and store
-    uint8_t* rec = a.codes[which] + ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * a.code_bytes[which];
+    uint8_t* rec = (which ? a.codes[1] : a.codes[0]) + ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (which ? a.code_bytes[1] : a.code_bytes[0]);
     const bool nib = mixed || seg_bits[0] == 4;
     if (nib) {
         const uint32_t v16 = idx[0] | (idx[1] << 4) | (idx[2] << 8) | (idx[3] << 12);
@@ -147,14 +174,133 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
         }
         if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = word;
     }
-    const int slots = a.norm_slots[which];
+    const int slots = (which ? a.norm_slots[1] : a.norm_slots[0]);
     if (lane < slots) {
         const size_t ni = ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * slots + lane;
         float n = nrm[0];
 #pragma unroll
         for (int k = 1; k < 4; ++k) n = lane == k ? nrm[k] : n;
-        if (a.norm_f16) static_cast<__half*>(a.norms[which])[ni] = __float2half_rn(n);
-        else static_cast<float*>(a.norms[which])[ni] = n;
+        if (a.norm_f16) static_cast<__half*>((which ? a.norms[1] : a.norms[0]))[ni] = __float2half_rn(n);
+        else static_cast<float*>((which ? a.norms[1] : a.norms[0]))[ni] = n;
+    }
+}
+
+// Encode one vector of a cache without mixed-rate keys: the rotation kind is a
+// template parameter, the boundaries of the lane's segment come in as float4s and
+// the count is unrolled.  Same steps and results as encode_vector.
+template <int BITS>
+__device__ __forceinline__ void search_pack(const QuantArgs& a, const float* bnd, const float y[4], uint8_t* rec) {
+    const int lane = threadIdx.x & 31;
+    constexpr int NB = (1 << BITS) - 1;
+    float bd[NB + 1];
+#pragma unroll
+    for (int k = 0; k < (NB + 1) / 4; ++k) {
+        const float4 f = reinterpret_cast<const float4*>(bnd)[k];
+        bd[4 * k] = f.x; bd[4 * k + 1] = f.y; bd[4 * k + 2] = f.z; bd[4 * k + 3] = f.w;
+    }
+    uint32_t idx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int k = 0; k < NB; ++k) c += y[i] > bd[k] ? 1u : 0u;
+        idx[i] = c;
+    }
+    if (BITS == 4) {
+        const uint32_t v16 = idx[0] | (idx[1] << 4) | (idx[2] << 8) | (idx[3] << 12);
+        const uint32_t lo = __shfl_sync(TQ_FULL_MASK, v16, (2 * lane) & 31);
+        const uint32_t hi = __shfl_sync(TQ_FULL_MASK, v16, (2 * lane + 1) & 31);
+        if (lane < 16) reinterpret_cast<uint32_t*>(rec)[lane] = lo | (hi << 16);
+    } else {
+        // lane l holds 12 bits at bit offset 12 l; word w takes lanes
+        // floor(32 w / 12) .. +3
+        const uint32_t v12 = idx[0] | (idx[1] << 3) | (idx[2] << 6) | (idx[3] << 9);
+        const int L0 = (32 * lane) / 12;
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int L = L0 + k;
+            const uint32_t val = __shfl_sync(TQ_FULL_MASK, v12, L < 32 ? L : 31);
+            const int off = 12 * L - 32 * lane;
+            if (L < 32 && off > -12 && off < 32) word |= off >= 0 ? (val << off) : (val >> (-off));
+        }
+        if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = word;
+    }
+}
+
+template <int ROT>
+__device__ __forceinline__ void encode_fast(const QuantArgs& a, const VecId& id, const float* xin) {
+    const int lane = threadIdx.x & 31;
+    const int which = id.which, h = id.h, t = id.t, b = id.b;
+    const int slot = a.start_pos[b] + t;
+    if (slot < 0 || slot >= a.Tcap) {
+        if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
+        return;
+    }
+    const tq_head_params& P = a.params[h];
+    float y[4] = {xin[0], xin[1], xin[2], xin[3]};
+    float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+    tq::rotate_forward(ROT, P, y);
+    float n;
+    if (ROT == TQ_ROT_WHT32) {   // one norm per 32-dim block = 8 lanes
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) ss += __shfl_xor_sync(TQ_FULL_MASK, ss, m);
+        n = sqrtf(ss);
+    } else {
+        n = sqrtf(tq::warp_sum(ss));
+    }
+    const float inv = n > 0.f ? 1.f / n : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] *= inv;
+    const int s = ROT == TQ_ROT_WHT32 ? lane >> 3 : 0;
+    const int bits = which == 0 ? P.k_seg_bits[s] : P.v_seg_bits[s];
+    const float* bnd = which == 0 ? P.k_bound[s] : P.v_bound[s];
+    uint8_t* rec = (which ? a.codes[1] : a.codes[0]) + ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (which ? a.code_bytes[1] : a.code_bytes[0]);
+    if (bits == 4) search_pack<4>(a, bnd, y, rec);
+    else search_pack<3>(a, bnd, y, rec);
+    // norms: one per vector, or one per 32-dim block (lanes 0, 8, 16, 24 hold them)
+    const int slots = (which ? a.norm_slots[1] : a.norm_slots[0]);
+    const float nv = ROT == TQ_ROT_WHT32 ? __shfl_sync(TQ_FULL_MASK, n, 8 * (lane & 3)) : n;
+    if (lane < slots) {
+        const size_t ni = ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * slots + lane;
+        if (a.norm_f16) static_cast<__half*>((which ? a.norms[1] : a.norms[0]))[ni] = __float2half_rn(nv);
+        else static_cast<float*>((which ? a.norms[1] : a.norms[0]))[ni] = nv;
+    }
+}
+
+// Each warp encodes vectors warp, warp + nwarps, ... (K and V alternate), the
+// next vector's input loaded while the current one is encoded.  Vector indices
+// fit in 32 bits (checked on the host).
+// ROT < 0: any rotation, mixed-rate keys allowed (encode_vector); else the
+// specialised path for that rotation kind.
+template <int ROT>
+__global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
+    __shared__ float xs_all[kWarps][128];
+    const int wib = threadIdx.x >> 5;
+    const uint32_t nwarps = gridDim.x * kWarps;
+    const uint32_t total = 2u * (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;
+    uint32_t v = blockIdx.x * kWarps + wib;
+    if (v >= total) return;
+    VecId id = vec_id(a, v);
+    float x[4];
+    tq::load4((id.which ? a.src[1] : a.src[0]), input_elem(a, id), a.in_dtype, x);
+    for (;;) {
+        const uint32_t vn = v + nwarps;
+        const bool more = vn < total && vn > v;
+        VecId idn = id;
+        float xn[4] = {0.f, 0.f, 0.f, 0.f};
+        if (more) {
+            idn = vec_id(a, vn);
+            tq::load4((idn.which ? a.src[1] : a.src[0]), input_elem(a, idn), a.in_dtype, xn);
+        }
+        if constexpr (ROT < 0) encode_vector(a, id, x, xs_all[wib]);
+        else encode_fast<ROT>(a, id, x);
+        if (!more) break;
+        __syncwarp();
+        v = vn;
+        id = idn;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = xn[i];
     }
 }
 
@@ -200,8 +346,15 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     a.norm_slots[0] = d->k_norm_slots;
     a.norm_slots[1] = d->v_norm_slots;
     const long long warps = 2LL * d->batch * n_new * d->n_kv_heads;
-    const long long blocks = (warps + kWarps - 1) / kWarps;
-    if (blocks > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
-    tq_quantize_kernel<<<(unsigned)blocks, kWarps * 32, 0, (cudaStream_t)stream>>>(a);
+    if (warps > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;   // vector indices are 32-bit in the kernel
+    long long blocks = (warps + kWarps - 1) / kWarps;
+    if (blocks > kMaxBlocks) blocks = kMaxBlocks;   // warps loop over the rest
+    const cudaStream_t st = (cudaStream_t)stream;
+    if (d->k_mixed) tq_quantize_kernel<-1><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    else if (d->rot == TQ_ROT_WHT128) tq_quantize_kernel<TQ_ROT_WHT128><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    else if (d->rot == TQ_ROT_WHT32) tq_quantize_kernel<TQ_ROT_WHT32><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    else if (d->rot == TQ_ROT_SO4_WHT128)
+        tq_quantize_kernel<TQ_ROT_SO4_WHT128><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    else tq_quantize_kernel<-1><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
     return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
