@@ -42,11 +42,12 @@ __device__ __forceinline__ void wht_warp(float v[4]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int m = 1; m < LANES; m <<= 1) {
-        const bool upper = lane & m;
+        // upper lane: o - v, lower lane: v + o; one fma with an exact +-1 factor
+        const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float o = __shfl_xor_sync(TQ_FULL_MASK, v[i], m);
-            v[i] = upper ? (o - v[i]) : (v[i] + o);
+            const float o = __shfl_xor_sync(TQ_FULL_MASK, v[i], m);
+            v[i] = fmaf(sgn, v[i], o);
         }
     }
 }

@@ -46,8 +46,9 @@ __device__ __forceinline__ VecId vec_id(const QuantArgs& a, uint32_t v_all) {
     return id;
 }
 
-__device__ __forceinline__ size_t input_elem(const QuantArgs& a, const VecId& id) {
-    return (((size_t)id.b * a.n_new + id.t) * a.Hkv + id.h) * 128 + 4 * (threadIdx.x & 31);
+// input [B][n_new][Hkv][128] in the vector order: element offset (v >> 1) * 128
+__device__ __forceinline__ size_t input_elem(uint32_t v_all) {
+    return (size_t)(v_all >> 1) * 128 + 4 * (threadIdx.x & 31);
 }
 
 // Encode one vector; xin holds this lane's 4 input values.
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
     if (v >= total) return;
     VecId id = vec_id(a, v);
     float x[4];
-    tq::load4((id.which ? a.src[1] : a.src[0]), input_elem(a, id), a.in_dtype, x);
+    tq::load4((id.which ? a.src[1] : a.src[0]), input_elem(v), a.in_dtype, x);
     for (;;) {
         const uint32_t vn = v + nwarps;
         const bool more = vn < total && vn > v;
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
         float xn[4] = {0.f, 0.f, 0.f, 0.f};
         if (more) {
             idn = vec_id(a, vn);
-            tq::load4((idn.which ? a.src[1] : a.src[0]), input_elem(a, idn), a.in_dtype, xn);
+            tq::load4((idn.which ? a.src[1] : a.src[0]), input_elem(vn), a.in_dtype, xn);
         }
         if constexpr (ROT < 0) encode_vector(a, id, x, xs_all[wib]);
         else encode_fast<ROT>(a, id, x);
