@@ -35,6 +35,10 @@
 
 namespace {
 
+// warps of a stream-K CTA (one CTA per SM) for up to four heads per KV head
+#ifndef TQ_TC_SK_WARPS
+#define TQ_TC_SK_WARPS 16
+#endif
 // section kernel: two tiles per softmax step (1) or one (0)
 #ifndef TQ_TC_TWO_TILES
 #define TQ_TC_TWO_TILES 0
@@ -831,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 3) dec
 // a warp that runs ahead takes more of them; at the end of a segment the CTA
 // merges its warps' states (the ring keeps streaming the next segment's tiles).
 template <int GPE>
-constexpr int sk_warps() { return GPE <= 4 ? 16 : 8; }
+constexpr int sk_warps() { return GPE <= 4 ? TQ_TC_SK_WARPS : 8; }
 
 template <int GPE>
 struct SkSmem {
