@@ -305,6 +305,167 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
     }
 }
 
+// ---- half-warp path: caches without mixed-rate keys, K and V of the same width.
+//
+// A warp takes one (batch, token, KV head): lanes 0-15 encode its K vector,
+// lanes 16-31 its V vector; lane j of a half holds coordinates 8j .. 8j+7.  The
+// three butterfly stages of strides 1, 2, 4 stay in the lane, the four of
+// strides 8 .. 64 cross lanes of the half; 3-bit codes of four lanes are the
+// three words of a 32-coordinate group.  Same steps and results as encode_vector.
+
+__device__ __forceinline__ void load8(const void* base, size_t elem, int dtype, float v[8]) {
+    if (dtype == TQ_F32) {
+        const float4 x = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+        const float4 y = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem + 4);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+    } else if (dtype == TQ_F16) {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __half*>(base) + elem);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+// Walsh-Hadamard butterflies over 8 * LANES coordinates held 8 per lane
+template <int LANES>
+__device__ __forceinline__ void wht8(float v[8]) {
+#pragma unroll
+    for (int st = 1; st < 8; st <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i & st) continue;
+            const float x = v[i], y = v[i + st];
+            v[i] = x + y;
+            v[i + st] = x - y;
+        }
+    }
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 1; m < LANES; m <<= 1) {
+        const float sgn = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o = __shfl_xor_sync(TQ_FULL_MASK, v[i], m);
+            v[i] = fmaf(sgn, v[i], o);
+        }
+    }
+}
+
+template <int ROT, int BITS>
+__global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
+    constexpr int NB = (1 << BITS) - 1;
+    const int lane = threadIdx.x & 31, hv = lane >> 4, j = lane & 15;
+    const uint32_t nwarps = gridDim.x * kWarps;
+    const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) pairs
+    uint32_t p = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (p >= total) return;
+    const void* src = hv ? a.src[1] : a.src[0];
+    float x[8];
+    load8(src, (size_t)p * 128 + 8 * j, a.in_dtype, x);
+    for (;;) {
+        const uint32_t pn = p + nwarps;
+        const bool more = pn < total && pn > p;
+        float xn[8];
+        if (more) load8(src, (size_t)pn * 128 + 8 * j, a.in_dtype, xn);
+
+        const uint32_t q = p / (uint32_t)a.Hkv;
+        const int h = (int)(p - q * (uint32_t)a.Hkv);
+        const uint32_t bb = q / (uint32_t)a.n_new;
+        const int t = (int)(q - bb * (uint32_t)a.n_new), b = (int)bb;
+        const int slot = a.start_pos[b] + t;
+        if (slot < 0 || slot >= a.Tcap) {
+            if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
+        } else {
+            const tq_head_params& P = a.params[h];
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = x[i];
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+            if (ROT != TQ_ROT_SO4_WHT128) {
+                const float4 s0 = reinterpret_cast<const float4*>(P.signs + 8 * j)[0];
+                const float4 s1 = reinterpret_cast<const float4*>(P.signs + 8 * j)[1];
+                y[0] *= s0.x; y[1] *= s0.y; y[2] *= s0.z; y[3] *= s0.w;
+                y[4] *= s1.x; y[5] *= s1.y; y[6] *= s1.z; y[7] *= s1.w;
+            }
+            float n;
+            if (ROT == TQ_ROT_WHT32) {   // four 32-dim blocks of 4 lanes, one norm each
+                wht8<4>(y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] *= 0.17677669529663687f;   // 1/sqrt(32)
+#pragma unroll
+                for (int m = 1; m < 4; m <<= 1) ss += __shfl_xor_sync(TQ_FULL_MASK, ss, m);
+            } else {
+                wht8<16>(y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] *= 0.08838834764831845f;   // 1/sqrt(128)
+                if (ROT == TQ_ROT_SO4_WHT128) {
+                    tq::so4_forward(P.quat[2 * j], y);
+                    tq::so4_forward(P.quat[2 * j + 1], y + 4);
+                }
+#pragma unroll
+                for (int m = 1; m < 16; m <<= 1) ss += __shfl_xor_sync(TQ_FULL_MASK, ss, m);
+            }
+            n = sqrtf(ss);
+            const float inv = n > 0.f ? 1.f / n : 0.f;
+            // codebook search: idx = #{k : y > boundary_k}
+            const int sgi = ROT == TQ_ROT_WHT32 ? j >> 2 : 0;
+            const float* bnd = hv ? P.v_bound[sgi] : P.k_bound[sgi];
+            float bd[NB + 1];
+#pragma unroll
+            for (int k = 0; k < (NB + 1) / 4; ++k) {
+                const float4 f = reinterpret_cast<const float4*>(bnd)[k];
+                bd[4 * k] = f.x; bd[4 * k + 1] = f.y; bd[4 * k + 2] = f.z; bd[4 * k + 3] = f.w;
+            }
+            uint32_t code = 0;   // 8 indices of BITS bits, coordinate 8j + i at bit BITS * i
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float yi = y[i] * inv;
+                uint32_t c = 0;
+#pragma unroll
+                for (int k = 0; k < NB; ++k) c += yi > bd[k] ? 1u : 0u;
+                code |= c << (BITS * i);
+            }
+            uint32_t* rec = reinterpret_cast<uint32_t*>(
+                (hv ? a.codes[1] : a.codes[0]) +
+                ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (hv ? a.code_bytes[1] : a.code_bytes[0]));
+            if (BITS == 4) {
+                rec[j] = code;
+            } else {
+                // lanes 4m .. 4m+3 hold 96 bits = words 3m .. 3m+2
+                const uint32_t nxt = __shfl_down_sync(TQ_FULL_MASK, code, 1);
+                const int r = j & 3, m4 = j >> 2;
+                if (r < 3) rec[3 * m4 + r] = (code >> (8 * r)) | (nxt << (24 - 8 * r));
+            }
+            const int slots = hv ? a.norm_slots[1] : a.norm_slots[0];
+            const float nv = ROT == TQ_ROT_WHT32 ? __shfl_sync(TQ_FULL_MASK, n, 16 * hv + 4 * (j & 3)) : n;
+            if (j < slots) {
+                const size_t ni = ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * slots + j;
+                void* nb = hv ? a.norms[1] : a.norms[0];
+                if (a.norm_f16) static_cast<__half*>(nb)[ni] = __float2half_rn(nv);
+                else static_cast<float*>(nb)[ni] = nv;
+            }
+        }
+        if (!more) break;
+        p = pn;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = xn[i];
+    }
+}
+
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 }  // namespace
@@ -351,6 +512,23 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     long long blocks = (warps + kWarps - 1) / kWarps;
     if (blocks > kMaxBlocks) blocks = kMaxBlocks;   // warps loop over the rest
     const cudaStream_t st = (cudaStream_t)stream;
+    if (!d->k_mixed && d->k_bits == d->v_bits && aligned(K, 16) && aligned(V, 16)) {
+        long long hb = (warps / 2 + kWarps - 1) / kWarps;   // one warp per (batch, token, KV head)
+        if (hb > kMaxBlocks) hb = kMaxBlocks;
+        const unsigned g = (unsigned)hb;
+        const bool b4 = d->k_bits == 4;
+        if (d->rot == TQ_ROT_WHT128) {
+            if (b4) tq_quantize_half<TQ_ROT_WHT128, 4><<<g, kWarps * 32, 0, st>>>(a);
+            else tq_quantize_half<TQ_ROT_WHT128, 3><<<g, kWarps * 32, 0, st>>>(a);
+        } else if (d->rot == TQ_ROT_WHT32) {
+            if (b4) tq_quantize_half<TQ_ROT_WHT32, 4><<<g, kWarps * 32, 0, st>>>(a);
+            else tq_quantize_half<TQ_ROT_WHT32, 3><<<g, kWarps * 32, 0, st>>>(a);
+        } else {
+            if (b4) tq_quantize_half<TQ_ROT_SO4_WHT128, 4><<<g, kWarps * 32, 0, st>>>(a);
+            else tq_quantize_half<TQ_ROT_SO4_WHT128, 3><<<g, kWarps * 32, 0, st>>>(a);
+        }
+        return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    }
     if (d->k_mixed) tq_quantize_kernel<-1><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
     else if (d->rot == TQ_ROT_WHT128) tq_quantize_kernel<TQ_ROT_WHT128><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
     else if (d->rot == TQ_ROT_WHT32) tq_quantize_kernel<TQ_ROT_WHT32><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
