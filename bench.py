@@ -322,22 +322,26 @@ def run_ours(args, wl, T, rank, world, local_rank):
 
     # end to end through the C ABI with host buffers: pinned H2D of the step's
     # inputs (q, new K/V token, positions, lengths) and D2H of the output
-    hq = q.cpu().pin_memory()
-    hk = k_new.cpu().pin_memory()
-    hv = v_new.cpu().pin_memory()
-    hs = start.cpu().pin_memory()
-    hl = seq.cpu().pin_memory()
+    # the step's host inputs live in one pinned buffer and go over in one copy
+    parts = [q, k_new, v_new, start, seq]
+    offs, off = [], 0
+    for x in parts:
+        offs.append(off)
+        off += (x.numel() * x.element_size() + 255) // 256 * 256
+    hbuf = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(off, dtype=torch.uint8, device=dev)
+    dviews = []
+    for x, o in zip(parts, offs):
+        nb = x.numel() * x.element_size()
+        hbuf[o:o + nb].copy_(x.reshape(-1).view(torch.uint8).cpu())
+        dviews.append(dbuf[o:o + nb].view(x.dtype).view(x.shape))
+    dq, dk, dv, ds, dl = dviews
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv, ds, dl = (torch.empty_like(x) for x in (q, k_new, v_new, start, seq))
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hs, hl))
+    h2d = off
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step(i):
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        ds.copy_(hs, non_blocking=True)
-        dl.copy_(hl, non_blocking=True)
+        dbuf.copy_(hbuf, non_blocking=True)
         step(i, None, dq, dk, dv, ds, dl, out)
         hout.copy_(out, non_blocking=True)
 
