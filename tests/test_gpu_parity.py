@@ -89,6 +89,58 @@ def test_quantize_append_matches_oracle(tq, name):
     assert bad / tot <= MAX_MISMATCH_FRAC, (bad, tot)
 
 
+def _check_codes_vs_oracle(st, cache, B, T):
+    kc = cache.codes_view("k").cpu().numpy()
+    vc = cache.codes_view("v").cpu().numpy()
+    kn = cache.norms_view("k").cpu().numpy()
+    vn = cache.norms_view("v").cpu().numpy()
+    tot = bad = 0
+    for b in range(B):
+        for h in range(st.wl.n_kv_heads):
+            for which, codes, norms in (("k", kc, kn), ("v", vc, vn)):
+                enc = oracle_encode(st, which, b, h)
+                spec = st.specs[h][0 if which == "k" else 1]
+                nbad, n, fw, fws, ok = compare_codes(codes[b, h, :T], enc, spec)
+                assert ok, f"{which} b={b} h={h}: a mismatch outside the near-boundary window"
+                bad += nbad
+                tot += n
+                assert compare_norms(norms[b, h, :T], enc), f"{which} norms b={b} h={h}"
+    assert bad / tot <= MAX_MISMATCH_FRAC, (bad, tot)
+    return kc, vc
+
+
+@pytest.mark.parametrize("name", ["llama8b", "so4", "block32_tq4"])
+def test_quantize_half_and_general_paths_agree(tq, name):
+    """16-byte aligned inputs take the half-warp path, 8-byte aligned ones the
+    one-warp-per-vector path; both match the oracle and each other."""
+    B, T = SMALL[name]
+    wl = _workload(name).with_(batch=B)
+    inp = W.make_inputs(wl, seq_len=T)
+    st = make_setup(tq, wl, inp, T + 5)
+    K = to_torch_input(torch, inp.K, wl.in_dtype)
+    V = to_torch_input(torch, inp.V, wl.in_dtype)
+    start = torch.zeros(B, dtype=torch.int32, device="cuda")
+    out = []
+    for shift in (0, 4):   # elements of offset: 0 -> 16-byte aligned, 4 -> 8-byte aligned (bf16)
+        c = tq.PackedKVCache(st.desc, st.blob)
+        if shift:
+            kb = torch.empty(K.numel() + shift, dtype=K.dtype, device="cuda")
+            vb = torch.empty(V.numel() + shift, dtype=V.dtype, device="cuda")
+            kb[shift:].copy_(K.reshape(-1))
+            vb[shift:].copy_(V.reshape(-1))
+            Kx, Vx = kb[shift:].view(K.shape), vb[shift:].view(V.shape)
+            assert Kx.data_ptr() % 16 == 8
+        else:
+            Kx, Vx = K, V
+            assert Kx.data_ptr() % 16 == 0
+        c.append(Kx, Vx, start)
+        torch.cuda.synchronize()
+        assert int(c.status.item()) == 0
+        out.append(_check_codes_vs_oracle(st, c, B, T))
+    for a, b in zip(out[0], out[1]):
+        assert np.mean(a != b) <= MAX_MISMATCH_FRAC
+
+
 def _upload_oracle_cache(tq, st, cache, B, T):
     """Write the oracle's records into the device cache; returns the encodings."""
     encs = {}
