@@ -223,6 +223,17 @@ def run_reference(args, wl, T, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def reduce_max_over_ranks(x, dist, device):
+    """Largest of x over the ranks of the default process group (x itself
+    without one); the job's time is the slowest rank's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------
 def run_ours(args, wl, T, rank, world, local_rank):
     import torch
@@ -298,11 +309,7 @@ def run_ours(args, wl, T, rank, world, local_rank):
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max_over_ranks(x, dist, dev)
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
