@@ -741,6 +741,60 @@ __device__ __forceinline__ void issue_tile(const DecodeArgs& a, uint32_t dst, in
     }
 }
 
+// The lane's part of the copies of one pair's tiles, set up once per segment.
+struct CopyPlan {
+    const uint8_t* gk;   // this lane's 16-byte chunk of tile 0 of the keys
+    const uint8_t* gv;
+    const uint8_t* gn;   // its 16-byte chunk of norm tile 0 (lanes 0..7)
+    uint32_t on;         // stage offset of that norm chunk
+    int nb;              // bytes per norm
+    bool has_n;
+};
+
+__device__ __forceinline__ CopyPlan copy_plan(const DecodeArgs& a, int b, int h) {
+    const int lane = threadIdx.x & 31;
+    CopyPlan cp;
+    cp.nb = a.norm_f16 ? 2 : 4;
+    const size_t head_tok = ((size_t)b * a.Hkv + h) * a.Tcap;
+    cp.gk = a.k_codes + head_tok * kRec + 16 * lane;
+    cp.gv = a.v_codes + head_tok * kRec + 16 * lane;
+    const int nch = lane & 3;
+    cp.has_n = lane < 8 && 16 * nch < kTile * cp.nb;
+    cp.gn = static_cast<const uint8_t*>(lane < 4 ? a.k_norms : a.v_norms) + head_tok * cp.nb + 16 * nch;
+    cp.on = (uint32_t)(lane < 4 ? offsetof(TcStage, kn) : offsetof(TcStage, vn)) + 16 * nch;
+    return cp;
+}
+
+// Tile t (of a sequence of L tokens) into the stage at dst; full tiles take no branch.
+__device__ __forceinline__ void issue_planned(const CopyPlan& cp, uint32_t dst, int L, int t) {
+    const int lane = threadIdx.x & 31;
+    const size_t co = (size_t)t * (kTile * kRec);
+    const int rem = L - t * kTile;
+    if (rem >= kTile) {
+        cp_async16s(dst + offsetof(TcStage, k) + 16 * lane, cp.gk + co, 16);
+        cp_async16s(dst + offsetof(TcStage, v) + 16 * lane, cp.gv + co, 16);
+        cp_async16p(dst + offsetof(TcStage, k) + 512 + 16 * lane, cp.gk + co + 512, lane < 16);
+        cp_async16p(dst + offsetof(TcStage, v) + 512 + 16 * lane, cp.gv + co + 512, lane < 16);
+        cp_async16p(dst + cp.on, cp.gn + (size_t)t * kTile * cp.nb, cp.has_n);
+    } else {   // ragged last tile of the sequence: zero-fill past its end
+        const int cb = rem * kRec;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int ch = lane + 32 * k;
+            if (ch < 48) {
+                const int n = min(16, max(0, cb - 16 * ch));
+                const size_t off = n ? co + 32 * 16 * k : 0;
+                cp_async16s(dst + offsetof(TcStage, k) + 16 * ch, cp.gk + off, n);
+                cp_async16s(dst + offsetof(TcStage, v) + 16 * ch, cp.gv + off, n);
+            }
+        }
+        if (cp.has_n) {
+            const int n = min(16, max(0, rem * cp.nb - 16 * (lane & 3)));
+            cp_async16s(dst + cp.on, cp.gn + (n ? (size_t)t * kTile * cp.nb : 0), n);
+        }
+    }
+}
+
 // ---- explicit splits: one CTA of 4 warps per (section, KV head, batch); its
 // warps take the section's tiles round-robin
 template <int GPE, int EP>
@@ -769,10 +823,11 @@ __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 3) dec
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(S.ring[warp]);
     constexpr uint32_t kStageBytes = (uint32_t)sizeof(TcStage);
     auto tile_of = [&](int i) { return sg.t_lo + warp + 4 * i; };
+    const CopyPlan cpl = copy_plan(a, b, h);
     constexpr int kAhead = TQ_TC_TWO_TILES ? 2 : 3;   // tiles in flight beyond those being processed
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {   // start the stream before the q rotation
-        if (k < nmine) issue_tile(a, ring_s + k * kStageBytes, b, h, L, tile_of(k));
+        if (k < nmine) issue_planned(cpl, ring_s + k * kStageBytes, L, tile_of(k));
         cp_async_commit();
     }
     for (int g = warp; g < GPE; g += 4) rotate_q(a, P, b, h, g, S.qts[g]);
@@ -787,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 3) dec
         for (int i = 0; i < nmine; i += 2) {
 #pragma unroll
             for (int k = 2; k < 4; ++k) {
-                if (i + k < nmine) issue_tile(a, ring_s + ((i + k) % 4) * kStageBytes, b, h, L, tile_of(i + k));
+                if (i + k < nmine) issue_planned(cpl, ring_s + ((i + k) % 4) * kStageBytes, L, tile_of(i + k));
                 cp_async_commit();
             }
             cp_async_wait<2>();
@@ -810,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 3) dec
         }
     } else {
         for (int i = 0; i < nmine; ++i) {
-            if (i + 3 < nmine) issue_tile(a, ring_s + ((i + 3) % 4) * kStageBytes, b, h, L, tile_of(i + 3));
+            if (i + 3 < nmine) issue_planned(cpl, ring_s + ((i + 3) % 4) * kStageBytes, L, tile_of(i + 3));
             cp_async_commit();
             cp_async_wait<3>();
             __syncwarp();
