@@ -363,6 +363,27 @@ __device__ __forceinline__ void wht8(float v[8]) {
     }
 }
 
+// #{k : y > bd[k]} over the 2^BITS - 1 ascending boundaries, as a binary search:
+// each comparison settles one bit of the index, the next threshold is selected by
+// the bits above it (same strict comparisons, same result as the count)  [TQ-MNN] §3.4
+template <int BITS>
+__device__ __forceinline__ uint32_t search_bits(float y, const float* bd) {
+    if constexpr (BITS == 3) {
+        const bool g2 = y > bd[3];
+        const bool g1 = y > (g2 ? bd[5] : bd[1]);
+        const bool g0 = y > (g2 ? (g1 ? bd[6] : bd[4]) : (g1 ? bd[2] : bd[0]));
+        return (g2 ? 4u : 0u) | (g1 ? 2u : 0u) | (g0 ? 1u : 0u);
+    } else {
+        const bool g3 = y > bd[7];
+        const bool g2 = y > (g3 ? bd[11] : bd[3]);
+        const bool g1 = y > (g3 ? (g2 ? bd[13] : bd[9]) : (g2 ? bd[5] : bd[1]));
+        const float t0 = g3 ? (g2 ? (g1 ? bd[14] : bd[12]) : (g1 ? bd[10] : bd[8]))
+                            : (g2 ? (g1 ? bd[6] : bd[4]) : (g1 ? bd[2] : bd[0]));
+        const bool g0 = y > t0;
+        return (g3 ? 8u : 0u) | (g2 ? 4u : 0u) | (g1 ? 2u : 0u) | (g0 ? 1u : 0u);
+    }
+}
+
 template <int ROT, int BITS>
 __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
     constexpr int NB = (1 << BITS) - 1;
@@ -374,16 +395,25 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
     const void* src = hv ? a.src[1] : a.src[0];
     float x[8];
     load8(src, (size_t)p * 128 + 8 * j, a.in_dtype, x);
+    // p = (b * n_new + t) * Hkv + h, carried forward by nwarps per pass without a division
+    const int Hkv = a.Hkv, n_new = a.n_new;
+    int h, t, b;
+    {
+        const uint32_t q = p / (uint32_t)Hkv;
+        h = (int)(p - q * (uint32_t)Hkv);
+        b = (int)(q / (uint32_t)n_new);
+        t = (int)(q - (uint32_t)b * (uint32_t)n_new);
+    }
+    const uint32_t sq = nwarps / (uint32_t)Hkv;
+    const int sh = (int)(nwarps - sq * (uint32_t)Hkv);
+    const int sb = (int)(sq / (uint32_t)n_new);
+    const int st = (int)(sq - (uint32_t)sb * (uint32_t)n_new);
     for (;;) {
         const uint32_t pn = p + nwarps;
         const bool more = pn < total && pn > p;
         float xn[8];
         if (more) load8(src, (size_t)pn * 128 + 8 * j, a.in_dtype, xn);
 
-        const uint32_t q = p / (uint32_t)a.Hkv;
-        const int h = (int)(p - q * (uint32_t)a.Hkv);
-        const uint32_t bb = q / (uint32_t)a.n_new;
-        const int t = (int)(q - bb * (uint32_t)a.n_new), b = (int)bb;
         const int slot = a.start_pos[b] + t;
         if (slot < 0 || slot >= a.Tcap) {
             if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
@@ -432,13 +462,7 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
             }
             uint32_t code = 0;   // 8 indices of BITS bits, coordinate 8j + i at bit BITS * i
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float yi = y[i] * inv;
-                uint32_t c = 0;
-#pragma unroll
-                for (int k = 0; k < NB; ++k) c += yi > bd[k] ? 1u : 0u;
-                code |= c << (BITS * i);
-            }
+            for (int i = 0; i < 8; ++i) code |= search_bits<BITS>(y[i] * inv, bd) << (BITS * i);
             uint32_t* rec = reinterpret_cast<uint32_t*>(
                 (hv ? a.codes[1] : a.codes[0]) +
                 ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (hv ? a.code_bytes[1] : a.code_bytes[0]));
@@ -461,6 +485,13 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
         }
         if (!more) break;
         p = pn;
+        h += sh;
+        const int cq = h >= Hkv ? 1 : 0;
+        h -= cq ? Hkv : 0;
+        t += st + cq;
+        const int cb = t >= n_new ? 1 : 0;
+        t -= cb ? n_new : 0;
+        b += sb + cb;
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = xn[i];
     }
