@@ -10,6 +10,8 @@
 // One warp encodes one vector (lane l owns coordinates 4l..4l+3): 16-byte or
 // 8-byte coalesced loads, warp-shuffle norm and butterflies, per-lane search,
 // shuffle assembly of the packed words, coalesced 4-byte stores.
+#include <numeric>
+
 #include "tq_device.cuh"
 
 namespace {
@@ -384,19 +386,79 @@ __device__ __forceinline__ uint32_t search_bits(float y, const float* bd) {
     }
 }
 
+// input element type fixed at compile time (DT: TQ_F32, TQ_F16 or TQ_BF16)
+template <int DT>
+__device__ __forceinline__ void load8t(const void* base, size_t elem, float v[8]) {
+    if constexpr (DT == TQ_F32) {
+        const float4 x = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+        const float4 y = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem + 4);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (DT == TQ_F16) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                v[2 * i] = f.x;
+                v[2 * i + 1] = f.y;
+            } else {
+                v[2 * i] = __uint_as_float(w[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+        }
+    }
+}
+
+// What one half-warp lane needs of its KV head's parameters: the signs (WHT
+// kinds) or the two quaternion pairs (SO(4)) of its 8 coordinates, and the
+// boundaries of its codebook.
 template <int ROT, int BITS>
+struct HalfParams {
+    float s[8];
+    float qa[8], qb[8];
+    float bd[1 << BITS];
+};
+
+template <int ROT, int BITS>
+__device__ __forceinline__ void load_half_params(const tq_head_params& P, int hv, int j, HalfParams<ROT, BITS>& hp) {
+    if constexpr (ROT == TQ_ROT_SO4_WHT128) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            hp.qa[i] = P.quat[2 * j][i];
+            hp.qb[i] = P.quat[2 * j + 1][i];
+        }
+    } else {
+        const float4 s0 = reinterpret_cast<const float4*>(P.signs + 8 * j)[0];
+        const float4 s1 = reinterpret_cast<const float4*>(P.signs + 8 * j)[1];
+        hp.s[0] = s0.x; hp.s[1] = s0.y; hp.s[2] = s0.z; hp.s[3] = s0.w;
+        hp.s[4] = s1.x; hp.s[5] = s1.y; hp.s[6] = s1.z; hp.s[7] = s1.w;
+    }
+    const int sgi = ROT == TQ_ROT_WHT32 ? j >> 2 : 0;
+    const float* bnd = hv ? P.v_bound[sgi] : P.k_bound[sgi];
+#pragma unroll
+    for (int k = 0; k < (1 << BITS) / 4; ++k) {
+        const float4 f = reinterpret_cast<const float4*>(bnd)[k];
+        hp.bd[4 * k] = f.x; hp.bd[4 * k + 1] = f.y; hp.bd[4 * k + 2] = f.z; hp.bd[4 * k + 3] = f.w;
+    }
+}
+
+template <int ROT, int BITS, int DT>
 __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
-    constexpr int NB = (1 << BITS) - 1;
     const int lane = threadIdx.x & 31, hv = lane >> 4, j = lane & 15;
     const uint32_t nwarps = gridDim.x * kWarps;
     const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) pairs
     uint32_t p = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (p >= total) return;
     const void* src = hv ? a.src[1] : a.src[0];
+    uint8_t* const cbase = hv ? a.codes[1] : a.codes[0];
+    const int cbytes = hv ? a.code_bytes[1] : a.code_bytes[0];
+    void* const nbase = hv ? a.norms[1] : a.norms[0];
+    const int slots = hv ? a.norm_slots[1] : a.norm_slots[0];
+    const int Hkv = a.Hkv, n_new = a.n_new, Tcap = a.Tcap;
     float x[8];
-    load8(src, (size_t)p * 128 + 8 * j, a.in_dtype, x);
+    load8t<DT>(src, (size_t)p * 128 + 8 * j, x);
     // p = (b * n_new + t) * Hkv + h, carried forward by nwarps per pass without a division
-    const int Hkv = a.Hkv, n_new = a.n_new;
     int h, t, b;
     {
         const uint32_t q = p / (uint32_t)Hkv;
@@ -408,29 +470,30 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
     const int sh = (int)(nwarps - sq * (uint32_t)Hkv);
     const int sb = (int)(sq / (uint32_t)n_new);
     const int st = (int)(sq - (uint32_t)sb * (uint32_t)n_new);
+    // the head's parameters, reloaded only when the head changes (never, when the
+    // launch makes the warp count a multiple of the head count)
+    HalfParams<ROT, BITS> hp;
+    int h_loaded = -1;
     for (;;) {
         const uint32_t pn = p + nwarps;
         const bool more = pn < total && pn > p;
         float xn[8];
-        if (more) load8(src, (size_t)pn * 128 + 8 * j, a.in_dtype, xn);
+        load8t<DT>(src, (size_t)(more ? pn : p) * 128 + 8 * j, xn);   // next pass (or this one again)
 
+        if (h != h_loaded) {
+            load_half_params<ROT, BITS>(a.params[h], hv, j, hp);
+            h_loaded = h;
+        }
         const int slot = a.start_pos[b] + t;
-        if (slot < 0 || slot >= a.Tcap) {
+        if (slot < 0 || slot >= Tcap) {
             if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
         } else {
-            const tq_head_params& P = a.params[h];
             float y[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) y[i] = x[i];
             float ss = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-            if (ROT != TQ_ROT_SO4_WHT128) {
-                const float4 s0 = reinterpret_cast<const float4*>(P.signs + 8 * j)[0];
-                const float4 s1 = reinterpret_cast<const float4*>(P.signs + 8 * j)[1];
-                y[0] *= s0.x; y[1] *= s0.y; y[2] *= s0.z; y[3] *= s0.w;
-                y[4] *= s1.x; y[5] *= s1.y; y[6] *= s1.z; y[7] *= s1.w;
-            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = ROT == TQ_ROT_SO4_WHT128 ? x[i] : x[i] * hp.s[i];
             float n;
             if (ROT == TQ_ROT_WHT32) {   // four 32-dim blocks of 4 lanes, one norm each
                 wht8<4>(y);
@@ -443,29 +506,19 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) y[i] *= 0.08838834764831845f;   // 1/sqrt(128)
                 if (ROT == TQ_ROT_SO4_WHT128) {
-                    tq::so4_forward(P.quat[2 * j], y);
-                    tq::so4_forward(P.quat[2 * j + 1], y + 4);
+                    tq::so4_forward(hp.qa, y);
+                    tq::so4_forward(hp.qb, y + 4);
                 }
 #pragma unroll
                 for (int m = 1; m < 16; m <<= 1) ss += __shfl_xor_sync(TQ_FULL_MASK, ss, m);
             }
             n = sqrtf(ss);
             const float inv = n > 0.f ? 1.f / n : 0.f;
-            // codebook search: idx = #{k : y > boundary_k}
-            const int sgi = ROT == TQ_ROT_WHT32 ? j >> 2 : 0;
-            const float* bnd = hv ? P.v_bound[sgi] : P.k_bound[sgi];
-            float bd[NB + 1];
-#pragma unroll
-            for (int k = 0; k < (NB + 1) / 4; ++k) {
-                const float4 f = reinterpret_cast<const float4*>(bnd)[k];
-                bd[4 * k] = f.x; bd[4 * k + 1] = f.y; bd[4 * k + 2] = f.z; bd[4 * k + 3] = f.w;
-            }
             uint32_t code = 0;   // 8 indices of BITS bits, coordinate 8j + i at bit BITS * i
 #pragma unroll
-            for (int i = 0; i < 8; ++i) code |= search_bits<BITS>(y[i] * inv, bd) << (BITS * i);
-            uint32_t* rec = reinterpret_cast<uint32_t*>(
-                (hv ? a.codes[1] : a.codes[0]) +
-                ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (hv ? a.code_bytes[1] : a.code_bytes[0]));
+            for (int i = 0; i < 8; ++i) code |= search_bits<BITS>(y[i] * inv, hp.bd) << (BITS * i);
+            const size_t rec_i = (((size_t)b * Hkv + h) * Tcap) + slot;
+            uint32_t* rec = reinterpret_cast<uint32_t*>(cbase + rec_i * cbytes);
             if (BITS == 4) {
                 rec[j] = code;
             } else {
@@ -474,13 +527,11 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
                 const int r = j & 3, m4 = j >> 2;
                 if (r < 3) rec[3 * m4 + r] = (code >> (8 * r)) | (nxt << (24 - 8 * r));
             }
-            const int slots = hv ? a.norm_slots[1] : a.norm_slots[0];
             const float nv = ROT == TQ_ROT_WHT32 ? __shfl_sync(TQ_FULL_MASK, n, 16 * hv + 4 * (j & 3)) : n;
             if (j < slots) {
-                const size_t ni = ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * slots + j;
-                void* nb = hv ? a.norms[1] : a.norms[0];
-                if (a.norm_f16) static_cast<__half*>(nb)[ni] = __float2half_rn(nv);
-                else static_cast<float*>(nb)[ni] = nv;
+                const size_t ni = rec_i * slots + j;
+                if (a.norm_f16) static_cast<__half*>(nbase)[ni] = __float2half_rn(nv);
+                else static_cast<float*>(nbase)[ni] = nv;
             }
         }
         if (!more) break;
@@ -495,6 +546,13 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = xn[i];
     }
+}
+
+template <int ROT, int BITS>
+void launch_half(unsigned g, cudaStream_t st, const QuantArgs& a) {
+    if (a.in_dtype == TQ_F32) tq_quantize_half<ROT, BITS, TQ_F32><<<g, kWarps * 32, 0, st>>>(a);
+    else if (a.in_dtype == TQ_F16) tq_quantize_half<ROT, BITS, TQ_F16><<<g, kWarps * 32, 0, st>>>(a);
+    else tq_quantize_half<ROT, BITS, TQ_BF16><<<g, kWarps * 32, 0, st>>>(a);
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -544,19 +602,26 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     if (blocks > kMaxBlocks) blocks = kMaxBlocks;   // warps loop over the rest
     const cudaStream_t st = (cudaStream_t)stream;
     if (!d->k_mixed && d->k_bits == d->v_bits && aligned(K, 16) && aligned(V, 16)) {
-        long long hb = (warps / 2 + kWarps - 1) / kWarps;   // one warp per (batch, token, KV head)
-        if (hb > kMaxBlocks) hb = kMaxBlocks;
+        const long long pairs = warps / 2;   // one warp per (batch, token, KV head)
+        long long hb = (pairs + kWarps - 1) / kWarps;
+        if (hb > kMaxBlocks) {
+            // warps loop over the rest; a warp count that is a multiple of the head
+            // count keeps each warp on one KV head (its parameters load once)
+            hb = kMaxBlocks;
+            const int m = d->n_kv_heads / std::gcd(d->n_kv_heads, kWarps);
+            if (hb >= m) hb -= hb % m;
+        }
         const unsigned g = (unsigned)hb;
         const bool b4 = d->k_bits == 4;
         if (d->rot == TQ_ROT_WHT128) {
-            if (b4) tq_quantize_half<TQ_ROT_WHT128, 4><<<g, kWarps * 32, 0, st>>>(a);
-            else tq_quantize_half<TQ_ROT_WHT128, 3><<<g, kWarps * 32, 0, st>>>(a);
+            if (b4) launch_half<TQ_ROT_WHT128, 4>(g, st, a);
+            else launch_half<TQ_ROT_WHT128, 3>(g, st, a);
         } else if (d->rot == TQ_ROT_WHT32) {
-            if (b4) tq_quantize_half<TQ_ROT_WHT32, 4><<<g, kWarps * 32, 0, st>>>(a);
-            else tq_quantize_half<TQ_ROT_WHT32, 3><<<g, kWarps * 32, 0, st>>>(a);
+            if (b4) launch_half<TQ_ROT_WHT32, 4>(g, st, a);
+            else launch_half<TQ_ROT_WHT32, 3>(g, st, a);
         } else {
-            if (b4) tq_quantize_half<TQ_ROT_SO4_WHT128, 4><<<g, kWarps * 32, 0, st>>>(a);
-            else tq_quantize_half<TQ_ROT_SO4_WHT128, 3><<<g, kWarps * 32, 0, st>>>(a);
+            if (b4) launch_half<TQ_ROT_SO4_WHT128, 4>(g, st, a);
+            else launch_half<TQ_ROT_SO4_WHT128, 3>(g, st, a);
         }
         return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
     }
