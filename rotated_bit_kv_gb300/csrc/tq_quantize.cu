@@ -548,6 +548,245 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
     }
 }
 
+// ---- tensor-core rotation (sign-flipped WHT128, 3-bit codes, fp16/bf16 input)
+//
+// A warp encodes 16 vectors at once: the K (rows 0-7) and V (rows 8-15) vectors of
+// 8 consecutive (batch, token, KV head) triples.  With i = 16 s + i' and
+// j = 16 u + j', the Sylvester matrix factors as H128[i][j] = H8[s][u] H16[i'][j'],
+// so for each half e of the 16-column block
+//   P_s = A_s . B_e        (A_s: columns 16s .. 16s+15 of the sign-flipped input,
+//                           B_e: 8 columns of H16; one mma m16n8k16 each)
+//   C_u = sum_s H8[s][u] P_s   (an 8-point butterfly on the fp32 accumulators).
+// Products of 16-bit inputs and +-1 are exact and accumulate in fp32, so the
+// result is the rotated vector times sqrt(128) up to fp32 rounding.  The squared
+// norms come from the same fragments: x_m . x_n is an mma of the tile with itself,
+// its diagonal the 16 norms.  [TQ-MNN] §3.1 (sign-flipped WHT), §3.4 (search).
+//
+// Column orders: A column k of step s is coordinate 16s + pi(k) with
+// pi(2c + b) = 4c + b, pi(2c + 8 + b) = 4c + 2 + b, so that lane c's operand is one
+// 8-byte load; output column n of half e is coordinate 16u + 4c + 2e + b for
+// n = 2c + b, so that lane c ends with coordinates 16u + 4c .. 16u + 4c + 3.
+
+template <int DT>
+__device__ __forceinline__ void mma_16816_x(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+    if constexpr (DT == TQ_BF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__host__ __device__ constexpr int popc4(int x) { return (x & 1) + ((x >> 1) & 1) + ((x >> 2) & 1) + ((x >> 3) & 1); }
+
+// +-1 in the 16-bit input format, packed for two k rows (lower k in the low half)
+template <int DT>
+__device__ __forceinline__ uint32_t pm1_pair(int neg_lo, int neg_hi) {
+    constexpr uint32_t one = DT == TQ_BF16 ? 0x3F80u : 0x3C00u;
+    return (one | (neg_lo ? 0x8000u : 0u)) | ((one | (neg_hi ? 0x8000u : 0u)) << 16);
+}
+
+constexpr int kTcWarps = 4;
+constexpr long long kTcMinTriples = 4096;   // smaller appends (decode steps) take the half-warp path
+constexpr long long kTcMaxBlocks = 152LL * 4 * 4;   // four waves of 4 resident CTAs per SM
+
+template <int DT>
+__global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) {
+    __shared__ __align__(16) uint8_t stage[kTcWarps][16][48];   // the tile's records: 2g K, 2g + 1 V
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3, warp = threadIdx.x >> 5;
+    const uint32_t nwarps = gridDim.x * kTcWarps;
+    const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) triples
+    const uint32_t tiles = (total + 7) / 8;
+    uint32_t tile = blockIdx.x * kTcWarps + (threadIdx.x >> 5);
+    if (tile >= tiles) return;
+    const int Hkv = a.Hkv, n_new = a.n_new, Tcap = a.Tcap;
+    const uint16_t* Ksrc = static_cast<const uint16_t*>(a.src[0]);
+    const uint16_t* Vsrc = static_cast<const uint16_t*>(a.src[1]);
+
+    // H16 columns of each half e as mma operand B (lane: rows 2c, 2c+1 / 2c+8, 2c+9, column g)
+    uint32_t hb[2][2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int j = 4 * (g >> 1) + 2 * e + (g & 1);
+        hb[e][0] = pm1_pair<DT>(popc4((4 * c) & j) & 1, popc4((4 * c + 1) & j) & 1);
+        hb[e][1] = pm1_pair<DT>(popc4((4 * c + 2) & j) & 1, popc4((4 * c + 3) & j) & 1);
+    }
+
+    // this lane's triple p = 8 tile + g, carried forward by 8 nwarps per pass
+    uint32_t p = tile * 8 + (uint32_t)g;
+    int h, t, b;
+    {
+        const uint32_t q = p / (uint32_t)Hkv;
+        h = (int)(p - q * (uint32_t)Hkv);
+        b = (int)(q / (uint32_t)n_new);
+        t = (int)(q - (uint32_t)b * (uint32_t)n_new);
+    }
+    const uint32_t step = 8u * nwarps;
+    const uint32_t sq = step / (uint32_t)Hkv;
+    const int sh = (int)(step - sq * (uint32_t)Hkv);
+    const int sb = (int)(sq / (uint32_t)n_new);
+    const int st = (int)(sq - (uint32_t)sb * (uint32_t)n_new);
+
+    // the head's sign masks (coordinates 16s + 4c .. +3) and K / V boundaries
+    uint32_t msk[8][2];
+    float kb[8], vb[8];
+    int h_loaded = -1;
+    auto load_head = [&](int hh) {   // hh is a valid head index for every lane
+        const tq_head_params& P = a.params[hh];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const float4 sg = *reinterpret_cast<const float4*>(P.signs + 16 * s + 4 * c);
+            msk[s][0] = (sg.x < 0.f ? 0x8000u : 0u) | (sg.y < 0.f ? 0x80000000u : 0u);
+            msk[s][1] = (sg.z < 0.f ? 0x8000u : 0u) | (sg.w < 0.f ? 0x80000000u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float4 f = reinterpret_cast<const float4*>(P.k_bound[0])[k];
+            const float4 v = reinterpret_cast<const float4*>(P.v_bound[0])[k];
+            kb[4 * k] = f.x; kb[4 * k + 1] = f.y; kb[4 * k + 2] = f.z; kb[4 * k + 3] = f.w;
+            vb[4 * k] = v.x; vb[4 * k + 1] = v.y; vb[4 * k + 2] = v.z; vb[4 * k + 3] = v.w;
+        }
+    };
+
+    // operand A of the tile: row g = K of triple p, row g + 8 = V of triple p
+    uint32_t ax[8][4];
+    auto load_tile = [&](uint32_t pp) {
+        const size_t base = (size_t)(pp < total ? pp : total - 1) * 128 + 4 * c;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 k2 = *reinterpret_cast<const uint2*>(Ksrc + base + 16 * s);
+            const uint2 v2 = *reinterpret_cast<const uint2*>(Vsrc + base + 16 * s);
+            ax[s][0] = k2.x; ax[s][2] = k2.y; ax[s][1] = v2.x; ax[s][3] = v2.y;
+        }
+    };
+    load_tile(p);
+
+    for (;;) {
+        const bool valid = p < total;
+        if (h != h_loaded) {
+            load_head(h);
+            h_loaded = h;
+        }
+        // squared norms: x_m . x_n over the tile; row g's K norm is entry (g, g), its V norm (g + 8, g)
+        float n1[4] = {0.f, 0.f, 0.f, 0.f}, n2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            mma_16816_x<DT>(n1, ax[s][0], ax[s][1], ax[s][2], ax[s][3], ax[s][0], ax[s][2]);
+            mma_16816_x<DT>(n2, ax[s][0], ax[s][1], ax[s][2], ax[s][3], ax[s][1], ax[s][3]);
+        }
+        // D x: flip the signs of the coordinates whose sign is -1
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            ax[s][0] ^= msk[s][0]; ax[s][1] ^= msk[s][0];
+            ax[s][2] ^= msk[s][1]; ax[s][3] ^= msk[s][1];
+        }
+        const int src_lane = 4 * g + (g >> 1);
+        float kss = (g & 1) ? n1[1] : n1[0], vss = (g & 1) ? n2[3] : n2[2];
+        kss = __shfl_sync(TQ_FULL_MASK, kss, src_lane);
+        vss = __shfl_sync(TQ_FULL_MASK, vss, src_lane);
+        const float kn = sqrtf(kss), vn = sqrtf(vss);
+        // y = H D x / (sqrt(128) |x|): one multiplier per vector
+        const float km = kn > 0.f ? 0.08838834764831845f * __frcp_rn(kn) : 0.f;
+        const float vm = vn > 0.f ? 0.08838834764831845f * __frcp_rn(vn) : 0.f;
+
+        uint32_t pc[8];   // codes of coordinates 16u + 4c .. +3: K at bits 0-11, V at 12-23
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pc[u] = 0;
+        uint32_t pn = p + step;
+        const bool more = pn < (tiles * 8u) && pn > p;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float acc[8][4];
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
+                mma_16816_x<DT>(acc[s], ax[s][0], ax[s][1], ax[s][2], ax[s][3], hb[e][0], hb[e][1]);
+            }
+            if (e == 1 && more) load_tile(pn);   // the operands are consumed: fetch the next tile
+#pragma unroll
+            for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    if (s & hs) continue;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float x = acc[s][i], y = acc[s + hs][i];
+                        acc[s][i] = x + y;
+                        acc[s + hs][i] = x - y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t k0 = search_bits<3>(acc[u][0] * km, kb), k1 = search_bits<3>(acc[u][1] * km, kb);
+                const uint32_t v0 = search_bits<3>(acc[u][2] * vm, vb), v1 = search_bits<3>(acc[u][3] * vm, vb);
+                pc[u] |= ((k0 | (k1 << 3)) | ((v0 | (v1 << 3)) << 12)) << (6 * e);
+            }
+        }
+
+        // records: lane pair (2m, 2m+1) holds 24 bits of K (the even lane writes
+        // them) and of V (the odd lane) at record bytes 6u + 3m .. +2; the 16 records
+        // of the tile are assembled in shared memory and leave as 16-byte stores
+        int slot = -1;
+        if (valid) {
+            slot = a.start_pos[b] + t;
+            if (slot < 0 || slot >= Tcap) {
+                if (c == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
+                slot = -1;
+            }
+        }
+        const bool odd = c & 1;
+        uint8_t* sr = &stage[warp][2 * g + (odd ? 1 : 0)][3 * (c >> 1)];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t o = __shfl_xor_sync(TQ_FULL_MASK, pc[u], 1);
+            const uint32_t w = odd ? ((o >> 12) & 0xFFFu) | (pc[u] & 0xFFF000u) : (pc[u] & 0xFFFu) | ((o & 0xFFFu) << 12);
+            uint8_t* r = sr + 6 * u;
+            if (c < 2) {
+                *reinterpret_cast<uint16_t*>(r) = (uint16_t)w;
+                r[2] = (uint8_t)(w >> 16);
+            } else {
+                r[0] = (uint8_t)w;
+                *reinterpret_cast<uint16_t*>(r + 1) = (uint16_t)(w >> 8);
+            }
+        }
+        const size_t rec_i = (((size_t)b * Hkv + h) * Tcap) + (slot < 0 ? 0 : slot);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {   // 48 chunks of 16 bytes: record q / 3, part q % 3
+            const int q = lane + 32 * k;
+            const int rr = (q < 48 ? q : 47) / 3, part = q - 3 * (q / 3);
+            const int src = 4 * (rr >> 1);
+            const int slot_r = __shfl_sync(TQ_FULL_MASK, slot, src);
+            const unsigned long long ri = __shfl_sync(TQ_FULL_MASK, (unsigned long long)rec_i, src);
+            if (q < 48 && slot_r >= 0) {
+                const uint4 v = *reinterpret_cast<const uint4*>(&stage[warp][rr][16 * part]);
+                *reinterpret_cast<uint4*>(((rr & 1) ? a.codes[1] : a.codes[0]) + ri * 48 + 16 * part) = v;
+            }
+        }
+        __syncwarp();
+        if (slot >= 0 && c < 2)
+            static_cast<__half*>(c ? a.norms[1] : a.norms[0])[rec_i] = __float2half_rn(c ? vn : kn);
+
+        if (!more) break;
+        p = pn;
+        h += sh;
+        const int cq = h >= Hkv ? 1 : 0;
+        h -= cq ? Hkv : 0;
+        t += st + cq;
+        const int cb = t >= n_new ? 1 : 0;
+        t -= cb ? n_new : 0;
+        b += sb + cb;
+    }
+}
+
 template <int ROT, int BITS>
 void launch_half(unsigned g, cudaStream_t st, const QuantArgs& a) {
     if (a.in_dtype == TQ_F32) tq_quantize_half<ROT, BITS, TQ_F32><<<g, kWarps * 32, 0, st>>>(a);
@@ -601,8 +840,26 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     long long blocks = (warps + kWarps - 1) / kWarps;
     if (blocks > kMaxBlocks) blocks = kMaxBlocks;   // warps loop over the rest
     const cudaStream_t st = (cudaStream_t)stream;
+    const long long triples = warps / 2;
+    if (!d->k_mixed && d->rot == TQ_ROT_WHT128 && d->k_bits == 3 && d->v_bits == 3 && d->norm_dtype == TQ_F16 &&
+        d->k_norm_slots == 1 && d->v_norm_slots == 1 && (in_dtype == TQ_BF16 || in_dtype == TQ_F16) &&
+        aligned(K, 8) && aligned(V, 8) && aligned(c->k_codes, 16) && aligned(c->v_codes, 16) &&
+        triples >= kTcMinTriples) {
+        // whole prompts: 16 vectors per warp through the tensor cores
+        long long tb = ((triples + 7) / 8 + kTcWarps - 1) / kTcWarps;
+        if (tb > kTcMaxBlocks) {
+            // warps loop over the rest; 8 x (warp count) a multiple of the head count
+            // keeps each lane on one KV head
+            tb = kTcMaxBlocks;
+            const int m = d->n_kv_heads / std::gcd(d->n_kv_heads, 8 * kTcWarps);
+            if (tb >= m) tb -= tb % m;
+        }
+        if (in_dtype == TQ_BF16) tq_quantize_tc<TQ_BF16><<<(unsigned)tb, kTcWarps * 32, 0, st>>>(a);
+        else tq_quantize_tc<TQ_F16><<<(unsigned)tb, kTcWarps * 32, 0, st>>>(a);
+        return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    }
     if (!d->k_mixed && d->k_bits == d->v_bits && aligned(K, 16) && aligned(V, 16)) {
-        const long long pairs = warps / 2;   // one warp per (batch, token, KV head)
+        const long long pairs = triples;   // one warp per (batch, token, KV head)
         long long hb = (pairs + kWarps - 1) / kWarps;
         if (hb > kMaxBlocks) {
             // warps loop over the rest; a warp count that is a multiple of the head

@@ -110,20 +110,21 @@ def _check_codes_vs_oracle(st, cache, B, T):
 
 
 @pytest.mark.parametrize("name", ["llama8b", "so4", "block32_tq4"])
-def test_quantize_half_and_general_paths_agree(tq, name):
-    """16-byte aligned inputs take the half-warp path, 8-byte aligned ones the
-    one-warp-per-vector path; both match the oracle and each other."""
+def test_quantize_paths_agree(tq, name):
+    """The write side has three kernels: whole prompts of 3-bit WHT128 caches with
+    16-bit inputs go through the tensor cores, other 16-byte aligned inputs (and
+    short appends) through the half-warp kernel, 8-byte aligned short appends
+    through the one-warp-per-vector kernel.  Each matches the oracle and the others."""
     B, T = SMALL[name]
     wl = _workload(name).with_(batch=B)
     inp = W.make_inputs(wl, seq_len=T)
     st = make_setup(tq, wl, inp, T + 5)
     K = to_torch_input(torch, inp.K, wl.in_dtype)
     V = to_torch_input(torch, inp.V, wl.in_dtype)
-    start = torch.zeros(B, dtype=torch.int32, device="cuda")
     out = []
-    for shift in (0, 4):   # elements of offset: 0 -> 16-byte aligned, 4 -> 8-byte aligned (bf16)
+    for mode, shift in (("whole", 0), ("chunks", 0), ("chunks", 4)):
         c = tq.PackedKVCache(st.desc, st.blob)
-        if shift:
+        if shift:   # an offset of 4 elements: 8-byte (bf16) aligned only
             kb = torch.empty(K.numel() + shift, dtype=K.dtype, device="cuda")
             vb = torch.empty(V.numel() + shift, dtype=V.dtype, device="cuda")
             kb[shift:].copy_(K.reshape(-1))
@@ -133,12 +134,58 @@ def test_quantize_half_and_general_paths_agree(tq, name):
         else:
             Kx, Vx = K, V
             assert Kx.data_ptr() % 16 == 0
-        c.append(Kx, Vx, start)
+        if mode == "chunks":   # appends of 40 tokens (short appends never take the tensor-core kernel)
+            for t0 in range(0, T, 40):
+                t1 = min(T, t0 + 40)
+                kc, vc = Kx[:, t0:t1], Vx[:, t0:t1]
+                if shift:   # keep the 8-byte alignment of the chunk copies
+                    kc = torch.empty(kc.numel() + shift, dtype=K.dtype, device="cuda")[shift:].view(kc.shape)
+                    vc = torch.empty(vc.numel() + shift, dtype=V.dtype, device="cuda")[shift:].view(vc.shape)
+                    kc.copy_(Kx[:, t0:t1])
+                    vc.copy_(Vx[:, t0:t1])
+                else:
+                    kc, vc = kc.contiguous(), vc.contiguous()
+                c.append(kc, vc, torch.full((B,), t0, dtype=torch.int32, device="cuda"))
+        else:
+            c.append(Kx, Vx, torch.zeros(B, dtype=torch.int32, device="cuda"))
         torch.cuda.synchronize()
         assert int(c.status.item()) == 0
         out.append(_check_codes_vs_oracle(st, c, B, T))
-    for a, b in zip(out[0], out[1]):
-        assert np.mean(a != b) <= MAX_MISMATCH_FRAC
+    for x in out[1:]:
+        for a, b in zip(out[0], x):
+            assert np.mean(a != b) <= MAX_MISMATCH_FRAC
+
+
+@pytest.mark.parametrize("in_dtype,B,T,pairs", [
+    (W.BF16, 2, 701, None),              # 4206 triples: a ragged last tile of 6
+    (W.F16, 2, 701, None),               # fp16 operands
+    (W.BF16, 2, 14001, [(0, 0), (1, 2)]),   # more tiles than warps: the grid-stride loop
+])
+def test_quantize_tc_heads_and_tails(tq, in_dtype, B, T, pairs):
+    """Tensor-core write path with 3 KV heads (lanes of a warp on different heads;
+    the warp count rounded to keep each lane on one head) against the oracle."""
+    wl = W.llama8b_decode().with_(n_q_heads=12, n_kv_heads=3, batch=B, in_dtype=in_dtype)
+    inp = W.make_inputs(wl, seq_len=T)
+    st = make_setup(tq, wl, inp, T + 3)
+    c = tq.PackedKVCache(st.desc, st.blob)
+    K = to_torch_input(torch, inp.K, wl.in_dtype)
+    V = to_torch_input(torch, inp.V, wl.in_dtype)
+    c.append(K, V, torch.full((B,), 2, dtype=torch.int32, device="cuda"))   # slots 2 .. T+1
+    torch.cuda.synchronize()
+    assert int(c.status.item()) == 0
+    kc, vc = c.codes_view("k").cpu().numpy(), c.codes_view("v").cpu().numpy()
+    kn, vn = c.norms_view("k").cpu().numpy(), c.norms_view("v").cpu().numpy()
+    bad = tot = 0
+    for (b, h) in pairs or [(b, h) for b in range(B) for h in range(3)]:
+        for which, codes, norms in (("k", kc, kn), ("v", vc, vn)):
+            enc = oracle_encode(st, which, b, h)
+            nb, n, _, _, ok = compare_codes(codes[b, h, 2:T + 2], enc, st.specs[h][0 if which == "k" else 1])
+            assert ok, f"{which} b={b} h={h}"
+            bad += nb
+            tot += n
+            assert compare_norms(norms[b, h, 2:T + 2], enc)
+            assert not codes[b, h, :2].any() and not codes[b, h, T + 2:].any()
+    assert bad / tot <= MAX_MISMATCH_FRAC
 
 
 def _upload_oracle_cache(tq, st, cache, B, T):
