@@ -594,13 +594,17 @@ __device__ __forceinline__ uint32_t pm1_pair(int neg_lo, int neg_hi) {
 }
 
 constexpr int kTcWarps = 4;
+constexpr int kTcRow = 288;   // bytes per staged row: 256 + 32, so that the 8-byte operand reads share no bank
+constexpr float kCellMagic = 1573120.f;   // 256 + 1.5 * 2^20: the sum's unit in the last place is 1/8
 constexpr long long kTcMinTriples = 4096;   // smaller appends (decode steps) take the half-warp path
 constexpr long long kTcMaxBlocks = 152LL * 4 * 4;   // four waves of 4 resident CTAs per SM
 
-template <int DT>
-__global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) {
-    __shared__ __align__(16) uint8_t stage[kTcWarps][16][48];   // the tile's records: 2g K, 2g + 1 V
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3, warp = threadIdx.x >> 5;
+// The tile loop of one warp; TAB: codebook search through the cell table `tab`
+// (one table for every head, K and V), else a binary search on the head's boundaries.
+template <int DT, bool TAB>
+__device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, uint8_t (*stage)[48],
+                                         uint8_t (*ring)[16][kTcRow]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const uint32_t nwarps = gridDim.x * kTcWarps;
     const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) triples
     const uint32_t tiles = (total + 7) / 8;
@@ -647,7 +651,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
             msk[s][1] = (sg.z < 0.f ? 0x8000u : 0u) | (sg.w < 0.f ? 0x80000000u : 0u);
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < 2 && !TAB; ++k) {
             const float4 f = reinterpret_cast<const float4*>(P.k_bound[0])[k];
             const float4 v = reinterpret_cast<const float4*>(P.v_bound[0])[k];
             kb[4 * k] = f.x; kb[4 * k + 1] = f.y; kb[4 * k + 2] = f.z; kb[4 * k + 3] = f.w;
@@ -655,24 +659,48 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
         }
     };
 
-    // operand A of the tile: row g = K of triple p, row g + 8 = V of triple p
-    uint32_t ax[8][4];
-    auto load_tile = [&](uint32_t pp) {
-        const size_t base = (size_t)(pp < total ? pp : total - 1) * 128 + 4 * c;
+    // The warp's tiles stream through a two-stage ring in shared memory (cp.async,
+    // 16 bytes a lane): rows 0-7 = K, 8-15 = V of triples 8 tl .. 8 tl + 7 (rows past
+    // the last triple repeat it)
+    auto issue = [&](uint32_t tl, int stg) {
+        const uint32_t p0 = tl * 8;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint2 k2 = *reinterpret_cast<const uint2*>(Ksrc + base + 16 * s);
-            const uint2 v2 = *reinterpret_cast<const uint2*>(Vsrc + base + 16 * s);
-            ax[s][0] = k2.x; ax[s][2] = k2.y; ax[s][1] = v2.x; ax[s][3] = v2.y;
+        for (int k = 0; k < 8; ++k) {
+            const int i = lane + 32 * k, row = i >> 4, col = i & 15;
+            uint32_t pp = p0 + (uint32_t)(row & 7);
+            pp = pp < total ? pp : total - 1;
+            const uint16_t* src = (k < 4 ? Ksrc : Vsrc) + (size_t)pp * 128 + col * 8;
+            const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&ring[stg][row][col * 16]);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
         }
     };
-    load_tile(p);
+    uint32_t ax[8][4];   // operand A of the tile: row g = K of triple p, row g + 8 = V of triple p
+    uint32_t tl = tile;
+    int stg = 0;
+    issue(tl, 0);
+    asm volatile("cp.async.commit_group;");
+    if (tl + nwarps < tiles && tl + nwarps > tl) issue(tl + nwarps, 1);
+    asm volatile("cp.async.commit_group;");
 
     for (;;) {
         const bool valid = p < total;
         if (h != h_loaded) {
             load_head(h);
             h_loaded = h;
+        }
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 k2 = *reinterpret_cast<const uint2*>(&ring[stg][g][32 * s + 8 * c]);
+            const uint2 v2 = *reinterpret_cast<const uint2*>(&ring[stg][g + 8][32 * s + 8 * c]);
+            ax[s][0] = k2.x; ax[s][2] = k2.y; ax[s][1] = v2.x; ax[s][3] = v2.y;
+        }
+        __syncwarp();
+        {   // refill the stage with the tile after next
+            const uint32_t t2 = tl + 2 * nwarps;
+            if (t2 < tiles && t2 > tl) issue(t2, stg);
+            asm volatile("cp.async.commit_group;");
         }
         // squared norms: x_m . x_n over the tile; row g's K norm is entry (g, g), its V norm (g + 8, g)
         float n1[4] = {0.f, 0.f, 0.f, 0.f}, n2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -709,7 +737,6 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
                 acc[s][0] = acc[s][1] = acc[s][2] = acc[s][3] = 0.f;
                 mma_16816_x<DT>(acc[s], ax[s][0], ax[s][1], ax[s][2], ax[s][3], hb[e][0], hb[e][1]);
             }
-            if (e == 1 && more) load_tile(pn);   // the operands are consumed: fetch the next tile
 #pragma unroll
             for (int hs = 1; hs < 8; hs <<= 1) {
 #pragma unroll
@@ -723,11 +750,21 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
                     }
                 }
             }
+            auto code_of = [&](float yn, const float* bd) -> uint32_t {
+                if constexpr (TAB) {
+                    // cell of yn: bits 3..11 of yn * 128 + 256 + 1.5 * 2^20 (steps of 1/8)
+                    const float f = fmaf(yn, 128.f, kCellMagic);
+                    const float2 en = tab[(__float_as_uint(f) & 0xFF8u) >> 3];
+                    return __float_as_uint(en.y) + (yn > en.x ? 1u : 0u);
+                } else {
+                    return search_bits<3>(yn, bd);
+                }
+            };
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const uint32_t k0 = search_bits<3>(acc[u][0] * km, kb), k1 = search_bits<3>(acc[u][1] * km, kb);
-                const uint32_t v0 = search_bits<3>(acc[u][2] * vm, vb), v1 = search_bits<3>(acc[u][3] * vm, vb);
-                pc[u] |= ((k0 | (k1 << 3)) | ((v0 | (v1 << 3)) << 12)) << (6 * e);
+                const uint32_t k0 = code_of(acc[u][0] * km, kb), k1 = code_of(acc[u][1] * km, kb);
+                const uint32_t v0 = code_of(acc[u][2] * vm, vb), v1 = code_of(acc[u][3] * vm, vb);
+                pc[u] += ((k0 + (k1 << 3)) + ((v0 + (v1 << 3)) << 12)) << (6 * e);
             }
         }
 
@@ -743,7 +780,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
             }
         }
         const bool odd = c & 1;
-        uint8_t* sr = &stage[warp][2 * g + (odd ? 1 : 0)][3 * (c >> 1)];
+        uint8_t* sr = &stage[2 * g + (odd ? 1 : 0)][3 * (c >> 1)];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const uint32_t o = __shfl_xor_sync(TQ_FULL_MASK, pc[u], 1);
@@ -767,7 +804,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
             const int slot_r = __shfl_sync(TQ_FULL_MASK, slot, src);
             const unsigned long long ri = __shfl_sync(TQ_FULL_MASK, (unsigned long long)rec_i, src);
             if (q < 48 && slot_r >= 0) {
-                const uint4 v = *reinterpret_cast<const uint4*>(&stage[warp][rr][16 * part]);
+                const uint4 v = *reinterpret_cast<const uint4*>(&stage[rr][16 * part]);
                 *reinterpret_cast<uint4*>(((rr & 1) ? a.codes[1] : a.codes[0]) + ri * 48 + 16 * part) = v;
             }
         }
@@ -777,6 +814,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
 
         if (!more) break;
         p = pn;
+        tl += nwarps;
+        stg ^= 1;
         h += sh;
         const int cq = h >= Hkv ? 1 : 0;
         h -= cq ? Hkv : 0;
@@ -785,6 +824,48 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
         t -= cb ? n_new : 0;
         b += sb + cb;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Cell table of the codebook search: cell c holds yn with yn * 128 + 256 in
+// [c - 1/8, c + 1] (the cell of the rounded value, widened by the rounding);
+// entry c = (the boundary inside that interval or +inf, the number of boundaries
+// below it).  Exact when no interval holds two boundaries: then
+// #{k : yn > b_k} = idx0 + (yn > inner boundary).
+
+template <int DT>
+__global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) {
+    __shared__ __align__(16) uint8_t stage[kTcWarps][16][48];   // the tile's records: 2g K, 2g + 1 V
+    __shared__ __align__(16) uint8_t ring[kTcWarps][2][16][kTcRow];
+    __shared__ __align__(16) float2 tab[512];
+    __shared__ int use_tab;
+    const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;
+    if ((uint32_t)blockIdx.x * kTcWarps * 8 >= total) return;   // no tile for this CTA (uniform)
+    if (threadIdx.x == 0) use_tab = 1;
+    __syncthreads();
+    // one table serves all heads when every head's K and V boundaries equal head 0's K boundaries
+    const float* b0 = a.params[0].k_bound[0];
+    for (int i = threadIdx.x; i < a.Hkv * 14; i += blockDim.x) {
+        const tq_head_params& P = a.params[i / 14];
+        const int k = i % 14;
+        if ((k < 7 ? P.k_bound[0][k] : P.v_bound[0][k - 7]) != b0[k % 7]) use_tab = 0;
+    }
+    for (int cc = threadIdx.x; cc < 512; cc += blockDim.x) {
+        const float lo = ((float)cc - 256.125f) * 0.0078125f, hi = ((float)cc - 255.f) * 0.0078125f;
+        int below = 0, inside = 0;
+        float bnd = INFINITY;
+        for (int k = 0; k < 7; ++k) {
+            const float bk = b0[k];
+            if (bk < lo) ++below;
+            else if (bk <= hi) { ++inside; bnd = bk; }
+        }
+        if (inside > 1) use_tab = 0;
+        tab[cc] = make_float2(bnd, __uint_as_float((uint32_t)below));
+    }
+    __syncthreads();
+    const int w = threadIdx.x >> 5;
+    if (use_tab) qtc_loop<DT, true>(a, tab, stage[w], ring[w]);
+    else qtc_loop<DT, false>(a, tab, stage[w], ring[w]);
 }
 
 template <int ROT, int BITS>

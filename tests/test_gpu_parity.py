@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import workloads as W
+from oracle import tq_oracle as O
 from gpu_harness import (ATT_TOL, MAX_MISMATCH_FRAC, att_error, compare_codes, compare_norms, make_setup,
                          oracle_attention, oracle_encode, to_torch_input)
 
@@ -186,6 +187,38 @@ def test_quantize_tc_heads_and_tails(tq, in_dtype, B, T, pairs):
             assert compare_norms(norms[b, h, 2:T + 2], enc)
             assert not codes[b, h, :2].any() and not codes[b, h, T + 2:].any()
     assert bad / tot <= MAX_MISMATCH_FRAC
+
+
+def test_quantize_tc_search_without_shared_table(tq):
+    """The tensor-core write kernel searches through one cell table when every
+    head's K and V boundaries are the same (they are whenever the library built
+    the parameters); otherwise it falls back to a binary search per head.  Head 1's
+    V boundaries moved up by one ulp force the fallback: every head still matches
+    the oracle, and every other vector's codes equal those of the table search."""
+    B, T = SMALL["llama8b"]
+    wl = _workload("llama8b").with_(batch=B)
+    inp = W.make_inputs(wl, seq_len=T)
+    st = make_setup(tq, wl, inp, T + 5)
+    bd = O.codebook(128, 3).boundaries.astype(np.float32)   # the library's fp32 boundaries
+    raw = np.frombuffer(bytes(st.blob), dtype=np.uint8).copy()
+    pat = bd.tobytes()
+    hits = [i for i in range(0, raw.size - len(pat) + 1, 4) if raw[i:i + len(pat)].tobytes() == pat]
+    assert len(hits) == 2 * wl.n_kv_heads, len(hits)   # K then V boundaries of each head, in head order
+    moved = raw.copy()
+    moved[hits[3]:hits[3] + len(pat)] = np.frombuffer(np.nextafter(bd, np.float32(np.inf)).tobytes(), np.uint8)
+    K = to_torch_input(torch, inp.K, wl.in_dtype)
+    V = to_torch_input(torch, inp.V, wl.in_dtype)
+    res = []
+    for blob in (raw, moved):
+        c = tq.PackedKVCache(st.desc, blob)
+        c.append(K, V, torch.zeros(B, dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        assert int(c.status.item()) == 0
+        res.append(_check_codes_vs_oracle(st, c, B, T))
+    (k0, v0), (k1, v1) = res
+    assert np.array_equal(k0, k1)
+    keep = [h for h in range(wl.n_kv_heads) if h != 1]
+    assert np.array_equal(v0[:, keep], v1[:, keep])
 
 
 def _upload_oracle_cache(tq, st, cache, B, T):
