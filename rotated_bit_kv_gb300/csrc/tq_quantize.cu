@@ -595,7 +595,8 @@ __device__ __forceinline__ uint32_t pm1_pair(int neg_lo, int neg_hi) {
 
 constexpr int kTcWarps = 4;
 constexpr int kTcRow = 288;   // bytes per staged row: 256 + 32, so that the 8-byte operand reads share no bank
-constexpr float kCellMagic = 1573120.f;   // 256 + 1.5 * 2^20: the sum's unit in the last place is 1/8
+constexpr int kCells = 128;                // cells of 1/32 over [-2, 2)
+constexpr float kCellMagic = 1572928.f;   // 64 + 1.5 * 2^20: the sum's unit in the last place is 1/8
 constexpr long long kTcMinTriples = 4096;   // smaller appends (decode steps) take the half-warp path
 constexpr long long kTcMaxBlocks = 152LL * 4 * 4;   // four waves of 4 resident CTAs per SM
 
@@ -752,9 +753,9 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
             }
             auto code_of = [&](float yn, const float* bd) -> uint32_t {
                 if constexpr (TAB) {
-                    // cell of yn: bits 3..11 of yn * 128 + 256 + 1.5 * 2^20 (steps of 1/8)
-                    const float f = fmaf(yn, 128.f, kCellMagic);
-                    const float2 en = tab[(__float_as_uint(f) & 0xFF8u) >> 3];
+                    // cell of yn: bits 3..9 of yn * 32 + 64 + 1.5 * 2^20 (steps of 1/8)
+                    const float f = fmaf(yn, 32.f, kCellMagic);
+                    const float2 en = tab[(__float_as_uint(f) & 0x3F8u) >> 3];
                     return __float_as_uint(en.y) + (yn > en.x ? 1u : 0u);
                 } else {
                     return search_bits<3>(yn, bd);
@@ -827,7 +828,7 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Cell table of the codebook search: cell c holds yn with yn * 128 + 256 in
+// Cell table of the codebook search: cell c holds yn with yn * 32 + 64 in
 // [c - 1/8, c + 1] (the cell of the rounded value, widened by the rounding);
 // entry c = (the boundary inside that interval or +inf, the number of boundaries
 // below it).  Exact when no interval holds two boundaries: then
@@ -837,7 +838,7 @@ template <int DT>
 __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) {
     __shared__ __align__(16) uint8_t stage[kTcWarps][16][48];   // the tile's records: 2g K, 2g + 1 V
     __shared__ __align__(16) uint8_t ring[kTcWarps][2][16][kTcRow];
-    __shared__ __align__(16) float2 tab[512];
+    __shared__ __align__(16) float2 tab[kCells];
     __shared__ int use_tab;
     const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;
     if ((uint32_t)blockIdx.x * kTcWarps * 8 >= total) return;   // no tile for this CTA (uniform)
@@ -850,8 +851,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
         const int k = i % 14;
         if ((k < 7 ? P.k_bound[0][k] : P.v_bound[0][k - 7]) != b0[k % 7]) use_tab = 0;
     }
-    for (int cc = threadIdx.x; cc < 512; cc += blockDim.x) {
-        const float lo = ((float)cc - 256.125f) * 0.0078125f, hi = ((float)cc - 255.f) * 0.0078125f;
+    for (int cc = threadIdx.x; cc < kCells; cc += blockDim.x) {
+        const float lo = ((float)cc - 64.125f) * 0.03125f, hi = ((float)cc - 63.f) * 0.03125f;
         int below = 0, inside = 0;
         float bnd = INFINITY;
         for (int k = 0; k < 7; ++k) {
