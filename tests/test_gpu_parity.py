@@ -416,6 +416,35 @@ def test_append_positions_and_incremental(tq):
                           torch.zeros(B, dtype=torch.int32, device="cuda"), 0)
 
 
+def test_quantize_tc_positions_outside_capacity(tq):
+    """Whole-prompt (tensor-core) append whose positions leave [0, capacity) at
+    either end: each token outside is skipped and flagged, the others encoded."""
+    B, T = 2, 300                       # 4800 triples: the tensor-core kernel
+    wl = _workload("llama8b").with_(batch=B)
+    inp = W.make_inputs(wl, seq_len=T)
+    cap = T + 5
+    st = make_setup(tq, wl, inp, cap)
+    c = tq.PackedKVCache(st.desc, st.blob)
+    K = to_torch_input(torch, inp.K, wl.in_dtype)
+    V = to_torch_input(torch, inp.V, wl.in_dtype)
+    start = cap - 100   # batch 0: tokens 0..99 fit, 100.. run past the end
+    c.append(K, V, torch.tensor([start, -5], dtype=torch.int32, device="cuda"))   # batch 1: tokens 0..4 before slot 0
+    torch.cuda.synchronize()
+    assert int(c.status.item()) & tq.TQ_DEV_BAD_POSITION
+    for which in ("k", "v"):
+        codes = c.codes_view(which).cpu().numpy()
+        norms = c.norms_view(which).cpu().numpy()
+        assert not codes[0, :, :start].any() and not norms[0, :, :start].any()
+        assert not codes[1, :, T - 5:].any() and not norms[1, :, T - 5:].any()
+        for h in range(wl.n_kv_heads):
+            spec = st.specs[h][0 if which == "k" else 1]
+            for b, t0, t1, s0 in ((0, 0, 100, start), (1, 5, T, 0)):
+                enc = oracle_encode(st, which, b, h, t0, t1)
+                _, _, _, _, ok = compare_codes(codes[b, h, s0:s0 + t1 - t0], enc, spec)
+                assert ok
+                assert compare_norms(norms[b, h, s0:s0 + t1 - t0], enc)
+
+
 def test_argument_errors(tq):
     st, cache = _encode_on_gpu(tq, "tiny", 1, 8)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
