@@ -32,6 +32,10 @@
  *     TQ_DEV_* bit into *d_status when d_status is not NULL.
  *   - The library keeps no global mutable state; calls on different streams
  *     with disjoint buffers are independent.
+ *   - The tensor-core decode kernel is launched as a programmatic dependent of
+ *     the kernel before it on the stream: its blocks may be placed while that
+ *     kernel finishes, and wait on the device for its completion before they
+ *     read anything.  The order the caller sees is the plain stream order.
  */
 #ifndef TQ_H_
 #define TQ_H_

@@ -801,6 +801,9 @@ template <int GPE, int EP>
 __global__ void __launch_bounds__(kThreads, GPE <= 4 ? TQ_TC_MIN_BLOCKS : 3) decode_tc(DecodeArgs a) {
     constexpr int NT = GPE / 4;
     __shared__ TcSmem S;
+    // launched as a programmatic dependent of the previous kernel in the stream:
+    // nothing is read before that kernel has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     build_table<kThreads>(a, S.tab);
@@ -1143,9 +1146,19 @@ cudaError_t tq_decode_tc_launch(const tq_cache_desc* d, const tq::DecodeArgs& a,
         else decode_sk<8, 8><<<sk_grid, sk_warps<8>() * 32, sk_smem_bytes<8>(), stream>>>(a);
         return cudaPeekAtLastError();
     }
-    dim3 grid(splits, d->n_kv_heads, d->batch);
-    if (d->group <= 1) decode_tc<4, 1><<<grid, kThreads, 0, stream>>>(a);
-    else if (d->group <= 4) decode_tc<4, 4><<<grid, kThreads, 0, stream>>>(a);
-    else decode_tc<8, 8><<<grid, kThreads, 0, stream>>>(a);
-    return cudaPeekAtLastError();
+    // programmatic dependent launch: the CTAs are placed while the previous kernel
+    // (typically the token append) finishes, and wait for it on the device
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, d->n_kv_heads, d->batch);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (d->group <= 1) return cudaLaunchKernelEx(&cfg, decode_tc<4, 1>, a);
+    if (d->group <= 4) return cudaLaunchKernelEx(&cfg, decode_tc<4, 4>, a);
+    return cudaLaunchKernelEx(&cfg, decode_tc<8, 8>, a);
 }

@@ -445,6 +445,9 @@ __device__ __forceinline__ void load_half_params(const tq_head_params& P, int hv
 
 template <int ROT, int BITS, int DT>
 __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
+    // a programmatic dependent launched after this kernel (decode) may be placed now;
+    // it still waits for this grid's completion before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, hv = lane >> 4, j = lane & 15;
     const uint32_t nwarps = gridDim.x * kWarps;
     const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) pairs
