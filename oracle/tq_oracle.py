@@ -28,7 +28,7 @@ the method, in the order the pages give them.  Sources, by page title:
   Delta_i = (3/4) s_i 4^(-b_i), same-width grouping, key-axis split with
   log-sum-exp merge.
 
-Readings where the pages are silent or ambiguous (each also listed in the design doc):
+Readings where the pages are silent or ambiguous:
 * density exponent (d-3)/2 (the §2.2 formula; the intuition paragraph's
   (d-2)/2 omits the Jacobian of the slice);
 * the codebook dimension d is the width of the normalised block (128, 32, or a
