@@ -411,6 +411,86 @@ def run_ours(args, wl, T, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def library_setup(tq, wl, inp, t_capacity):
+    """Descriptor and parameter blob through the library alone.  Mixed-rate keys:
+    block energies and the greedy allocation from the library's own entry
+    points, one seeded Haar matrix per non-empty same-width group (ascending
+    width) of each KV head."""
+    block_bits = mats = None
+    if wl.mixed_k:
+        G = wl.group
+        kc = W.as_float64(inp.K[0, :wl.calib_tokens], wl.in_dtype).astype(np.float32)
+        qc = W.as_float64(inp.q_calib, wl.in_dtype).astype(np.float32)
+        bbs, flat = [], []
+        for h in range(wl.n_kv_heads):
+            s_h = tq.tq_block_energy(qc[:, h * G:(h + 1) * G], kc[:, h])
+            bb = tq.tq_block_bit_alloc(s_h, wl.b_min, wl.b_max, wl.avg_bits * (wl.head_dim // 2))
+            bbs.append(bb)
+            for b in range(wl.b_min, wl.b_max + 1):
+                n = 2 * int(np.count_nonzero(np.asarray(bb) == b))
+                if n:
+                    flat.append(W.haar_orthogonal(n, wl.seed, h, b).ravel())
+        block_bits = np.stack(bbs).astype(np.int32)
+        mats = np.concatenate(flat)
+    desc = tq.tq_cache_desc_init(wl.head_dim, wl.n_q_heads, wl.n_kv_heads, wl.batch, t_capacity, wl.rot,
+                                 0 if wl.mixed_k else wl.k_bits, wl.v_bits, wl.norm_dtype, int(wl.mixed_k))
+    blob = tq.tq_params_build(desc, signs=inp.signs, quats=inp.quats, k_block_bits=block_bits, k_group_mats=mats)
+    return desc, blob
+
+
+def run_sweep(args):
+    """Decode time on every synthetic workload (not the bench line): one cache
+    filled by a whole-prompt append, the library's plan, L2 flushed before each
+    timed launch, CUDA events around the decode alone."""
+    import torch
+
+    import rotated_bit_kv_gb300 as tq
+
+    tq.build()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cases = [(W.llama8b_decode(seq_len=t), t) for t in (512, 2048, 8192)]
+    cases += [(W.block32(3), 8192), (W.block32(4), 8192)]
+    cases += [(W.so4_wht(seq_len=t), t) for t in (128, 512, 2048, 8192, 32768)]
+    cases += [(W.mixed_rate_long(seq_len=t), t) for t in (131072, 524288)]
+    print("| workload | B | T | plan (splits, V mode) | decode us | GB/s | of measured peak |")
+    print("|---|---|---|---|---|---|---|")
+    for wl, T in cases:
+        wl = wl.with_(batch=wl.batch, seq_len=T)
+        inp = W.make_inputs(wl, seq_len=T)
+        desc, blob = library_setup(tq, wl, inp, T)
+        cache = tq.PackedKVCache(desc, blob, device=dev)
+        K = _to_torch(torch, inp.K, wl.in_dtype, dev)
+        V = _to_torch(torch, inp.V, wl.in_dtype, dev)
+        cache.append(K, V, torch.zeros(wl.batch, dtype=torch.int32, device=dev))
+        del K, V
+        q = _to_torch(torch, inp.q, wl.in_dtype, dev)
+        seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
+        out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+        splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_AUTO, 0)
+        for _ in range(3):
+            cache.decode(q, seq, T, out=out)
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            cache.decode(q, seq, T, out=out)
+            b.record()
+            times.append((a, b))
+        torch.cuda.synchronize()
+        if int(cache.status.item()) != 0:
+            raise RuntimeError(f"device status {int(cache.status.item())}")
+        us = statistics.median(x.elapsed_time(y) for x, y in times) * 1e3
+        nbytes = step_bytes(wl, T, desc)["decode"]
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(f"| {wl.name} | {wl.batch} | {T} | {splits}, {vmode} | {us:.1f} | {gbs:.0f} | {100 * gbs / peak:.1f} % |",
+              flush=True)
+        del cache, q, out
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,7 +502,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=0, help="key-axis splits (0: the library's plan)")
     ap.add_argument("--streamk", action="store_true", help="tensor-core kernel with the stream-K partition")
+    ap.add_argument("--sweep", action="store_true",
+                    help="decode time on every synthetic workload (a table, not the bench line)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

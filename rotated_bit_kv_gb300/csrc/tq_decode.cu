@@ -324,7 +324,7 @@ constexpr int kSMs = 152;
 // stream-K grid is unavailable: an SM with at least four CTAs works through
 // them at a fixed rate, so a step takes about max(4, ceil(CTAs / SMs)) x (tiles
 // per warp + about two tiles of start-up); sections of at least 64 tokens.
-int tc_uniform_splits(long long pairs, int max_seq_len) {
+int tc_uniform_splits(long long pairs, int max_seq_len, int gp) {
     long long cap = (max_seq_len + 63) / 64;
     if (cap > TQ_MAX_SPLITS) cap = TQ_MAX_SPLITS;
     long long best = 1;
@@ -334,7 +334,8 @@ int tc_uniform_splits(long long pairs, int max_seq_len) {
         const long long per_warp = (sec + 63) / 64;
         long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
         if (per_sm < 4) per_sm = 4;
-        const double cost = (double)per_sm * ((double)per_warp + 2.0);
+        // + the last CTA's merge of the pair's sp partials (gp heads), after the rest
+        const double cost = (double)per_sm * ((double)per_warp + 2.0) + (sp > 1 ? (double)sp * gp / 24.0 : 0.0);
         if (sp == 1 || cost < best_cost - 1e-9) { best_cost = cost; best = sp; }
     }
     return (int)best;
@@ -378,7 +379,7 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     int splits = n_splits;
     const long long pairs = (long long)d->batch * d->n_kv_heads;
     if (splits == 0 && mode == TQ_VMODE_TENSOR) {
-        splits = tc_uniform_splits(pairs, max_seq_len);
+        splits = tc_uniform_splits(pairs, max_seq_len, padded_group(d->group));
     } else if (splits == 0) {
         // fill the GPU: about four resident 128-thread CTAs per SM, sections of
         // at least 64 tokens
@@ -421,7 +422,8 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     if (mode == TQ_VMODE_TENSOR_STREAMK) {
         mode = TQ_VMODE_TENSOR;
         sk_grid = tq_decode_tc_sk_grid(d, max_seq_len);
-        if (sk_grid == 0) splits = tc_uniform_splits((long long)d->batch * d->n_kv_heads, max_seq_len);
+        if (sk_grid == 0)
+            splits = tc_uniform_splits((long long)d->batch * d->n_kv_heads, max_seq_len, padded_group(d->group));
     }
     DecodeArgs a;
     a.k_codes = static_cast<const uint8_t*>(c->k_codes);

@@ -197,6 +197,59 @@ __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
     return L;
 }
 
+// Log-sum-exp merge of `parts` published partials (rows [part t][head g] of
+// kPartStride floats: o~[128], m, l) into ot[g][0..127], normalised  [Block-GTQ].
+// A warp per head finds M_g = max_t m_t and L_g = sum_t 2^(m_t - M_g) l_t; then each
+// thread accumulates four coordinates of one head over the parts, its loads
+// independent of each other so that their latencies overlap.  Empty parts
+// (m = -inf) weigh 0; a pair with no tokens gives 0.  NTHR threads.
+template <int GP, int NTHR>
+__device__ __forceinline__ void merge_parts(const float* base, int parts, float (*ot)[128]) {
+    __shared__ float sM[GP], sL[GP];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int g = warp; g < GP; g += NTHR / 32) {
+        float M = -INFINITY;
+        for (int t = lane; t < parts; t += 32) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(TQ_FULL_MASK, M, o));
+        float L = 0.f;
+        for (int t = lane; t < parts; t += 32) {
+            const float* pr = base + ((size_t)t * GP + g) * kPartStride;
+            const float mt = __ldcg(pr + 128);
+            L = fmaf(mt == -INFINITY ? 0.f : exp2f(mt - M), __ldcg(pr + 129), L);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(TQ_FULL_MASK, L, o);
+        if (lane == 0) {
+            sM[g] = M;
+            sL[g] = L;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < GP * 32; i += NTHR) {
+        const int g = i >> 5, d4 = i & 31;
+        const float M = sM[g];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int t = 0; t < parts; ++t) {
+            const float* pr = base + ((size_t)t * GP + g) * kPartStride;
+            const float mt = __ldcg(pr + 128);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(pr) + d4);
+            const float w = mt == -INFINITY ? 0.f : exp2f(mt - M);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        const float L = sL[g];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        ot[g][4 * d4] = acc.x * inv;
+        ot[g][4 * d4 + 1] = acc.y * inv;
+        ot[g][4 * d4 + 2] = acc.z * inv;
+        ot[g][4 * d4 + 3] = acc.w * inv;
+    }
+}
+
 // Epilogue: `ot[g][c]` holds this CTA's unnormalised o~, (m[g], l[g]) its
 // softmax state (identical in every thread).  Either finalise directly (one
 // split) or publish the partial and let the last CTA merge.
@@ -220,35 +273,9 @@ __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*o
         __syncthreads();
         if (!*is_last) return;
         __threadfence();
-        // log-sum-exp merge over the splits  [Block-GTQ]; the loads of a pass
-        // are independent of each other so that their latencies overlap
-        const float* base = a.ws_part + (((size_t)b * a.Hkv + h) * a.n_splits * GP) * kPartStride;
-        float M[GP], lsum[GP], acc[GP];
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            M[g] = -INFINITY;
-            lsum[g] = 0.f;
-            acc[g] = 0.f;
-        }
-#pragma unroll 4
-        for (int t = 0; t < a.n_splits; ++t) {
-#pragma unroll
-            for (int g = 0; g < GP; ++g) M[g] = fmaxf(M[g], __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
-        }
-#pragma unroll 4
-        for (int t = 0; t < a.n_splits; ++t) {
-#pragma unroll
-            for (int g = 0; g < GP; ++g) {
-                const float* pr = base + ((size_t)t * GP + g) * kPartStride;
-                const float mt = __ldcg(pr + 128), lt = __ldcg(pr + 129), ov = __ldcg(pr + tid);
-                const float w = mt == -INFINITY ? 0.f : exp2f(mt - M[g]);
-                lsum[g] = fmaf(w, lt, lsum[g]);
-                acc[g] = fmaf(w, ov, acc[g]);
-            }
-        }
-        // each thread rewrites only its own coordinate of ot
-#pragma unroll
-        for (int g = 0; g < GP; ++g) ot[g][tid] = lsum[g] > 0.f ? acc[g] / lsum[g] : 0.f;
+        // log-sum-exp merge over the splits  [Block-GTQ]
+        merge_parts<GP, kThreads>(a.ws_part + (((size_t)b * a.Hkv + h) * a.n_splits * GP) * kPartStride,
+                                  a.n_splits, ot);
         if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
         __syncthreads();
     } else {

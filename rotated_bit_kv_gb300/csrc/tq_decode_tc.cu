@@ -637,25 +637,8 @@ __device__ void finish_segment(const DecodeArgs& a, const tq_head_params& P, flo
         __syncthreads();
         if (!*is_last) return;
         __threadfence();
-        // log-sum-exp merge over the pair's parts  [Block-GTQ]; the loads of a
-        // pass are independent of each other so that their latencies overlap
-        const float* base = a.ws_part + (size_t)sg.first * GP * kPartStride;
-        for (int i = tid; i < GP * 128; i += NTHR) {
-            const int g = i >> 7, d = i & 127;
-            float M = -INFINITY;
-#pragma unroll 4
-            for (int t = 0; t < sg.parts; ++t) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
-            float lsum = 0.f, acc = 0.f;
-#pragma unroll 4
-            for (int t = 0; t < sg.parts; ++t) {
-                const float* pr = base + ((size_t)t * GP + g) * kPartStride;
-                const float mt = __ldcg(pr + 128), lt = __ldcg(pr + 129), ov = __ldcg(pr + d);
-                const float w = mt == -INFINITY ? 0.f : exp2f(mt - M);
-                lsum = fmaf(w, lt, lsum);
-                acc = fmaf(w, ov, acc);
-            }
-            ot[g][d] = lsum > 0.f ? acc / lsum : 0.f;   // each thread rewrites only its own entries
-        }
+        // log-sum-exp merge over the pair's parts  [Block-GTQ]
+        merge_parts<GP, NTHR>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot);
         if (tid == 0) a.tickets[pair] = 0;   // ready for the next call
         __syncthreads();
     } else {
