@@ -457,6 +457,8 @@ def run_sweep(args):
     print("| workload | B | T | plan (splits, V mode) | decode us | GB/s | of measured peak |")
     print("|---|---|---|---|---|---|---|")
     for wl, T in cases:
+        if args.only and args.only not in wl.name:
+            continue
         wl = wl.with_(batch=wl.batch, seq_len=T)
         inp = W.make_inputs(wl, seq_len=T)
         desc, blob = library_setup(tq, wl, inp, T)
@@ -468,15 +470,15 @@ def run_sweep(args):
         q = _to_torch(torch, inp.q, wl.in_dtype, dev)
         seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
         out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
-        splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_AUTO, 0)
+        splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_AUTO, args.splits)
         for _ in range(3):
-            cache.decode(q, seq, T, out=out)
+            cache.decode(q, seq, T, out=out, n_splits=args.splits)
         times = []
         for _ in range(args.steps):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            cache.decode(q, seq, T, out=out)
+            cache.decode(q, seq, T, out=out, n_splits=args.splits)
             b.record()
             times.append((a, b))
         torch.cuda.synchronize()
@@ -504,6 +506,7 @@ def main():
     ap.add_argument("--streamk", action="store_true", help="tensor-core kernel with the stream-K partition")
     ap.add_argument("--sweep", action="store_true",
                     help="decode time on every synthetic workload (a table, not the bench line)")
+    ap.add_argument("--only", default="", help="sweep: workloads whose name contains this")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

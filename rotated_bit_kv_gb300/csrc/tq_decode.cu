@@ -381,10 +381,14 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     if (splits == 0 && mode == TQ_VMODE_TENSOR) {
         splits = tc_uniform_splits(pairs, max_seq_len, padded_group(d->group));
     } else if (splits == 0) {
-        // fill the GPU: about four resident 128-thread CTAs per SM, sections of
-        // at least 64 tokens
-        const long long target = 4LL * kSMs;
-        long long sp = (target + pairs - 1) / pairs;
+        // about 1.6 times the sections that fill the GPU once (four resident
+        // 128-thread CTAs per SM), at most 128 partials per pair (the last CTA
+        // merges them after the rest: past ~128 the merge costs more than the
+        // shorter sections save, as measured on the dimension-parallel kernel),
+        // sections of at least 64 tokens
+        const long long fill = (4LL * kSMs + pairs - 1) / pairs;
+        long long sp = (fill * 8 + 4) / 5;
+        if (sp > 128) sp = 128;
         const long long cap = (max_seq_len + 63) / 64;
         if (sp > cap) sp = cap;
         if (sp < 1) sp = 1;
