@@ -326,6 +326,22 @@ def test_decode_tensor_tile_edges(tq, name, T):
         _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, n_splits)
 
 
+@pytest.mark.parametrize("n_splits", [77, 300])
+@pytest.mark.parametrize("name,v_mode", [("so4", 2), ("block32_tq4", 1), ("llama8b", 0)])
+def test_decode_many_splits(tq, name, v_mode, n_splits):
+    """Key-axis splits well beyond a warp's width (the merge walks the partials
+    32 at a time for the weights, 8 at a time for the outputs), many of them
+    empty (sections of a few tokens, rounded to whole tiles), ragged lengths."""
+    B, T = 2, 1000
+    seq_lens = W.ragged_lengths(B, T, 7)
+    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=_aligned_cap(T), seq_lens=seq_lens)
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.from_numpy(st.inp.seq_lens).cuda()
+    _check_decode(tq, st, cache, encs, q, sl, T, v_mode, n_splits)
+    assert int(cache.status.item()) == 0
+
+
 @pytest.mark.parametrize("name", TC_NAMES)
 def test_decode_streamk_matches_oracle(tq, name):
     """Stream-K partition: every tile of every pair spread over one wave of
