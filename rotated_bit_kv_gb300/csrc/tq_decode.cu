@@ -332,8 +332,9 @@ int tc_uniform_splits(long long pairs, int max_seq_len, int gp) {
     for (long long sp = 1; sp <= cap; ++sp) {
         const long long sec = (max_seq_len + sp - 1) / sp;
         const long long per_warp = (sec + 63) / 64;
-        long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
-        if (per_sm < 4) per_sm = 4;
+        // CTAs an SM works through one after another (measured: fewer, longer
+        // sections win while the grid is under a wave or two)
+        const long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
         // + the last CTA's merge of the pair's sp partials (gp heads), after the rest
         const double cost = (double)per_sm * ((double)per_warp + 2.0) + (sp > 1 ? (double)sp * gp / 24.0 : 0.0);
         if (sp == 1 || cost < best_cost - 1e-9) { best_cost = cost; best = sp; }

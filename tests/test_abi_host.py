@@ -145,7 +145,7 @@ def test_decode_plan_host_only(tqlib):
     d = tq.tq_cache_desc_init(128, 32, 8, 32, 8192, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
     sp, vm = tq.tq_decode_plan(d, 8192)
     # tensor-core path; 4 splits x 256 (batch, KV head) pairs = 1024 CTAs, 6.7 per SM,
-    # 32 tiles per warp: the cheapest max(4, ceil(CTAs / 152)) x (tiles per warp + 2)
+    # 32 tiles per warp: the cheapest ceil(CTAs / 152) x (tiles per warp + 2) + merge
     assert (sp, vm) == (4, tq.TQ_VMODE_TENSOR)
     sp, vm = tq.tq_decode_plan(d, 8192, tq.TQ_VMODE_DIM_PARALLEL)
     assert 1 <= sp <= tq.TQ_MAX_SPLITS and vm == tq.TQ_VMODE_DIM_PARALLEL
