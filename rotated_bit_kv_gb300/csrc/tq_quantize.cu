@@ -928,7 +928,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     const long long triples = warps / 2;
     if (!d->k_mixed && d->rot == TQ_ROT_WHT128 && d->k_bits == 3 && d->v_bits == 3 && d->norm_dtype == TQ_F16 &&
         d->k_norm_slots == 1 && d->v_norm_slots == 1 && (in_dtype == TQ_BF16 || in_dtype == TQ_F16) &&
-        aligned(K, 8) && aligned(V, 8) && aligned(c->k_codes, 16) && aligned(c->v_codes, 16) &&
+        aligned(K, 16) && aligned(V, 16) && aligned(c->k_codes, 16) && aligned(c->v_codes, 16) &&
         triples >= kTcMinTriples) {
         // whole prompts: 16 vectors per warp through the tensor cores
         long long tb = ((triples + 7) / 8 + kTcWarps - 1) / kTcWarps;

@@ -113,9 +113,10 @@ def _check_codes_vs_oracle(st, cache, B, T):
 @pytest.mark.parametrize("name", ["llama8b", "so4", "block32_tq4"])
 def test_quantize_paths_agree(tq, name):
     """The write side has three kernels: whole prompts of 3-bit WHT128 caches with
-    16-bit inputs go through the tensor cores, other 16-byte aligned inputs (and
-    short appends) through the half-warp kernel, 8-byte aligned short appends
-    through the one-warp-per-vector kernel.  Each matches the oracle and the others."""
+    16-bit, 16-byte aligned inputs go through the tensor cores, other 16-byte
+    aligned inputs (and short appends) through the half-warp kernel, inputs aligned
+    to 8 bytes only (whole prompts or chunks) through the one-warp-per-vector
+    kernel.  Each matches the oracle and the others."""
     B, T = SMALL[name]
     wl = _workload(name).with_(batch=B)
     inp = W.make_inputs(wl, seq_len=T)
@@ -123,7 +124,7 @@ def test_quantize_paths_agree(tq, name):
     K = to_torch_input(torch, inp.K, wl.in_dtype)
     V = to_torch_input(torch, inp.V, wl.in_dtype)
     out = []
-    for mode, shift in (("whole", 0), ("chunks", 0), ("chunks", 4)):
+    for mode, shift in (("whole", 0), ("chunks", 0), ("chunks", 4), ("whole", 4)):
         c = tq.PackedKVCache(st.desc, st.blob)
         if shift:   # an offset of 4 elements: 8-byte (bf16) aligned only
             kb = torch.empty(K.numel() + shift, dtype=K.dtype, device="cuda")
