@@ -450,9 +450,9 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peak, _ = measured_peak()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    cases = [(W.llama8b_decode(seq_len=t), t) for t in (512, 2048, 8192)]
+    cases = [(W.llama8b_decode(seq_len=t), t) for t in (128, 256, 512, 2048, 8192)]
     cases += [(W.block32(3), 8192), (W.block32(4), 8192)]
-    cases += [(W.so4_wht(seq_len=t), t) for t in (128, 512, 2048, 8192, 32768)]
+    cases += [(W.so4_wht(seq_len=t), t) for t in (128, 256, 512, 2048, 8192, 32768)]
     cases += [(W.mixed_rate_long(seq_len=t), t) for t in (131072, 524288)]
     print("| workload | B | T | plan (splits, V mode) | decode us | GB/s | of measured peak |")
     print("|---|---|---|---|---|---|---|")

@@ -266,9 +266,9 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const tq_cache_ptrs* ca
                               size_t workspace_bytes, int32_t* d_status, void* stream);
 
 /* tq_decode_attention with explicit choices, for tests and tuning:
- *   v_mode    TQ_VMODE_* (AUTO picks token parallel below the crossover length,
- *             the tensor-core path where the format supports it, otherwise
- *             dimension parallel)
+ *   v_mode    TQ_VMODE_* (AUTO picks the tensor-core path where the format
+ *             supports it, at every length; otherwise token parallel below the
+ *             crossover length and dimension parallel above)
  *   n_splits  key-axis splits per (batch, KV head), 1..TQ_MAX_SPLITS, or 0 for
  *             the automatic choice
  * Errors: as tq_decode_attention; TQ_ERR_UNSUPPORTED if v_mode is TENSOR and

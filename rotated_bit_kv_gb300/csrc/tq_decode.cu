@@ -368,8 +368,10 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     const bool tc = tq_decode_tc_supported(d);
     int mode = v_mode;
     if (mode == TQ_VMODE_AUTO) {
-        if (max_seq_len < tq_v_crossover()) mode = TQ_VMODE_TOKEN_PARALLEL;
-        else mode = tc ? TQ_VMODE_TENSOR : TQ_VMODE_DIM_PARALLEL;
+        // the tensor-core kernel wins at every length measured (T = 128 .. 32768);
+        // without it, token-parallel below the crossover, dimension-parallel above
+        if (tc) mode = TQ_VMODE_TENSOR;
+        else mode = max_seq_len < tq_v_crossover() ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
     }
     if ((mode == TQ_VMODE_TENSOR || mode == TQ_VMODE_TENSOR_STREAMK) && !tc) return TQ_ERR_UNSUPPORTED;
     if (mode == TQ_VMODE_TENSOR_STREAMK) {   // no per-pair sections

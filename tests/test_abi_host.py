@@ -155,7 +155,9 @@ def test_decode_plan_host_only(tqlib):
         tq.tq_decode_plan(d2, 8190, tq.TQ_VMODE_TENSOR)
     assert e.value.status == tq.TQ_ERR_UNSUPPORTED
     sp, vm = tq.tq_decode_plan(d, 100)
-    assert vm == tq.TQ_VMODE_TOKEN_PARALLEL and sp <= 2
+    assert vm == tq.TQ_VMODE_TENSOR and sp <= 2                         # the tensor path at every length
+    sp, vm = tq.tq_decode_plan(d2, 100)
+    assert vm == tq.TQ_VMODE_TOKEN_PARALLEL and sp <= 2                 # without it, token-parallel when short
     with pytest.raises(tq.TQError):
         tq.tq_decode_plan(d, 0)
     with pytest.raises(tq.TQError):

@@ -285,7 +285,8 @@ def test_decode_short_and_tile_edges(tq, T):
 
 def test_v_mode_switch_at_crossover(tq):
     st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=600)          # capacity 608: tensor path available
-    assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
+    assert tq.tq_decode_plan(st.desc, 8)[1] == tq.TQ_VMODE_TENSOR     # at every length
+    assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TENSOR
     assert tq.tq_decode_plan(st.desc, 512)[1] == tq.TQ_VMODE_TENSOR
     st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=601)          # unaligned capacity: CUDA-core path
     assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
