@@ -30,8 +30,10 @@
  *     can see (a sequence length above the cache capacity, a write position
  *     outside the cache) are clamped or skipped, never trapped, and OR a
  *     TQ_DEV_* bit into *d_status when d_status is not NULL.
- *   - The library keeps no global mutable state; calls on different streams
- *     with disjoint buffers are independent.
+ *   - Apart from tq_decode_attention_noalloc (a fixed scratch array shared by
+ *     all its calls, which must therefore be ordered on one stream) the library
+ *     keeps no global mutable state: calls on different streams with disjoint
+ *     buffers are independent.
  *   - The tensor-core decode kernel is launched as a programmatic dependent of
  *     the kernel before it on the stream: its blocks may be placed while that
  *     kernel finishes, and wait on the device for its completion before they
@@ -91,8 +93,12 @@ typedef int32_t tq_status;
 #define TQ_VMODE_AUTO            -1
 #define TQ_VMODE_TOKEN_PARALLEL   0
 #define TQ_VMODE_DIM_PARALLEL     1
-#define TQ_VMODE_TENSOR           2  /* dimension parallel on tensor cores */
-#define TQ_VMODE_TENSOR_STREAMK   3  /* tensor cores, stream-K partition (explicit only) */
+#define TQ_VMODE_TENSOR           2  /* dimension parallel on tensor cores (tile layout) */
+#define TQ_VMODE_TENSOR_STREAMK   3  /* same kernel as TQ_VMODE_TENSOR (kept as an alias) */
+
+/* Cache layouts (tq_cache_desc.layout, chosen by tq_cache_desc_init) */
+#define TQ_LAYOUT_NATURAL  0  /* one packed record per token, token-major             */
+#define TQ_LAYOUT_TILE16   1  /* 16-token tiles in the order the decode kernel reads */
 
 #define TQ_HEAD_DIM     128
 #define TQ_MAX_GROUP     16   /* maximum n_q_heads / n_kv_heads */
@@ -101,19 +107,54 @@ typedef int32_t tq_status;
 /* ---------------------------------------------------------------- layout */
 /* Cache descriptor.  Filled by tq_cache_desc_init; treat as read-only.
  *
- * Device layout of the cache (all token-major per (batch, KV head)):
- *   k_codes [batch][n_kv_heads][t_capacity][k_code_bytes]   uint8
- *   k_norms [batch][n_kv_heads][t_capacity][k_norms]        norm_dtype
- *   v_codes [batch][n_kv_heads][t_capacity][v_code_bytes]   uint8
- *   v_norms [batch][n_kv_heads][t_capacity][v_norms]        norm_dtype
- * A code record holds the 128 indices of one vector in rotated-coordinate
- * order: 3-bit indices LSB first (index i at bits [3i, 3i+3) of the
- * little-endian byte stream: 8 indices per 3 bytes, 48 B) or 4-bit indices
- * two per byte (index 2j in the low nibble of byte j, 64 B) [TQ-MNN §3.3].
- * Mixed-rate keys use the 4-bit container for every width (one index per
- * nibble) with the groups in ascending bit width [Block-GTQ, packed cache].
- * Norm slots: 1 (WHT128, SO4_WHT128), 4 (WHT32: one per 32-dim block) or 4
- * (mixed-rate keys: slot b-1 holds the norm of the b-bit group, 0 if empty). */
+ * Code records.  The record of one vector holds its 128 indices in rotated-
+ * coordinate order: 3-bit indices LSB first (index i at bits [3i, 3i+3) of the
+ * little-endian byte stream: 8 indices per 3 bytes, 48 B) or 4-bit indices two
+ * per byte (index 2j in the low nibble of byte j, 64 B) [TQ-MNN §3.3].  Mixed-
+ * rate keys use the 4-bit container for every width (one index per nibble) with
+ * the groups in ascending bit width [Block-GTQ, packed cache].  A "field" is the
+ * pair of indices of coordinates (2i, 2i+1): bits [6i, 6i+6) (3-bit) or byte i
+ * (4-bit) of the record.  Norm slots: 1 (WHT128, SO4_WHT128), 4 (WHT32: one per
+ * 32-dim block) or 4 (mixed-rate keys: slot b-1 holds the norm of the b-bit
+ * group, 0 if empty).
+ *
+ * Positions per (batch, KV head): t_alloc = t_capacity rounded up to a multiple
+ * of 16 (TQ_LAYOUT_TILE16) or t_capacity (TQ_LAYOUT_NATURAL).  Every array is
+ * [batch][n_kv_heads][t_alloc positions] of per-position data:
+ *   k_codes, v_codes  k_code_bytes / v_code_bytes per position, uint8
+ *   k_norms, v_norms  k_norm_slots / v_norm_slots per position, norm_dtype
+ *
+ * TQ_LAYOUT_NATURAL (mixed-rate keys, or more than 8 query heads per KV head,
+ * or fp32 norms with WHT32): position t holds the record and norms of token t.
+ *
+ * TQ_LAYOUT_TILE16 (every other cache): positions come in tiles of 16; tile j of
+ * a (batch, KV head) holds tokens 16j .. 16j+15 in 16 * code_bytes bytes of codes
+ * and 16 * slots norms, arranged as the decode kernel's 32 lanes read them.
+ * Lane L = 4r + c (r = 0..7, c = 0..3) owns 2W words of a code tile (W = 3 for
+ * 3-bit, 4 for 4-bit): words 0..3 at byte 16L, words 4..2W-1 at byte
+ * 512 + 8(W-2)L.
+ *   keys:   words 0..W-1 hold token r, words W..2W-1 token r+8; a token's W
+ *           words in lane L hold its fields s = 0..15 of pairs
+ *           i = 8(s>>1) + c + 4(s&1).
+ *   values: words 0..W-1 hold token 2c in their low 16-bit halves and token
+ *           2c+1 in their high halves, words W..2W-1 tokens 2c+8 and 2c+9; a
+ *           token's W halves in lane L hold its fields q = 0..7 of pairs
+ *           16(q>>1) + r + 8(q&1).
+ *   4-bit: key field s is byte s&3 of word s>>2; value field q is byte q&1 of
+ *           half q>>1.
+ *   3-bit: key fields 0..11 and value fields 0..5 have a byte each (key: byte
+ *           s&3 of word s>>2; value: byte q&1 of half q>>1); in the bytes of the
+ *           token's first and third word the field is bits 0-5, in those of its
+ *           second word field bits 0-1 are byte bits 0-1 and field bits 2-5 byte
+ *           bits 4-7.  Key fields 12..15 (value fields 6, 7) are spread over byte
+ *           lane g = s-12 (q-6) of the token's three words: field bits 0-1 in
+ *           bits 6-7 of the first word's byte, bits 2-3 in bits 2-3 of the
+ *           second's, bits 4-5 in bits 6-7 of the third's.
+ *   norms:  one slot: token t at element 2(t&7) + (t>>3) of the tile; four
+ *           slots: keys (2(t&7) + (t>>3))*4 + b, values
+ *           ((((t&7)>>1)*2 + (t>>3))*4 + b)*2 + (t&1).
+ * Each key word and each value half belongs to one token, so appends of single
+ * tokens never rewrite another token's bytes. */
 typedef struct tq_cache_desc {
     int32_t head_dim;
     int32_t n_q_heads;
@@ -132,6 +173,8 @@ typedef struct tq_cache_desc {
     int32_t k_norm_slots;
     int32_t v_norm_slots;
     int32_t norm_bytes;     /* 2 or 4 */
+    int32_t layout;         /* TQ_LAYOUT_* */
+    int32_t t_alloc;        /* positions per (batch, KV head) (see above) */
     int64_t params_bytes;   /* size of the parameter blob (tq_params_build) */
 } tq_cache_desc;
 
@@ -237,11 +280,11 @@ tq_status tq_quantize_append(const tq_cache_desc* desc, const tq_cache_ptrs* cac
 
 /* Workspace bytes tq_decode_attention needs for at most max_splits key-axis
  * splits: partial (m, l, o~) per (batch, q head, split) plus one ticket per
- * (batch, KV head).  For caches the tensor-core kernel supports it also covers
- * the stream-K partials (at least 1216 + batch * n_kv_heads partial slots), so
- * max_splits = 1 is enough for the automatic plan.  The ticket words must be zero before the first call on a
- * workspace (e.g. a cudaMemset of the whole buffer); every call leaves them
- * zero again. */
+ * (batch, KV head).  For TQ_LAYOUT_TILE16 caches it also covers the tensor-core
+ * kernel's partials (one per CTA and piece of a pair: at most 1216 + batch *
+ * n_kv_heads slots), so max_splits = 1 is enough for the automatic plan.  The
+ * ticket words must be zero before the first call on a workspace (e.g. a
+ * cudaMemset of the whole buffer); every call leaves them zero again. */
 size_t tq_decode_workspace_bytes(const tq_cache_desc* desc, int32_t max_splits);
 
 /* One decode step of attention on the packed cache [RotaryQuant, Key design 3;
@@ -257,7 +300,7 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc* desc, int32_t max_splits);
  *   out          device fp32 [batch][n_q_heads][128]
  *   workspace    device, >= tq_decode_workspace_bytes(desc, splits used); the
  *                splits used are at most TQ_MAX_SPLITS and at most
- *                ceil(max_seq_len / 64)
+ *                ceil(max_seq_len / 64) (1 for TQ_LAYOUT_TILE16 caches)
  *   d_status     device int32 or NULL
  * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
 tq_status tq_decode_attention(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
@@ -266,13 +309,16 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const tq_cache_ptrs* ca
                               size_t workspace_bytes, int32_t* d_status, void* stream);
 
 /* tq_decode_attention with explicit choices, for tests and tuning:
- *   v_mode    TQ_VMODE_* (AUTO picks the tensor-core path where the format
- *             supports it, at every length; otherwise token parallel below the
- *             crossover length and dimension parallel above)
- *   n_splits  key-axis splits per (batch, KV head), 1..TQ_MAX_SPLITS, or 0 for
- *             the automatic choice
- * Errors: as tq_decode_attention; TQ_ERR_UNSUPPORTED if v_mode is TENSOR and
- * the cache format has no tensor-core kernel. */
+ *   v_mode    TQ_VMODE_*.  TQ_LAYOUT_TILE16 caches run the tensor-core kernel
+ *             (AUTO, TENSOR or TENSOR_STREAMK); TQ_LAYOUT_NATURAL caches run
+ *             the CUDA-core kernels (AUTO: token parallel below the crossover
+ *             length, dimension parallel above; or either one explicitly).
+ *   n_splits  0 for the automatic choice; else, CUDA-core kernels: key-axis
+ *             splits per (batch, KV head), 1..TQ_MAX_SPLITS; tensor-core
+ *             kernel: the number of CTAs the tiles of all pairs are divided
+ *             over, 1..1216
+ * Errors: as tq_decode_attention; TQ_ERR_UNSUPPORTED if v_mode asks for a
+ * kernel that does not read the cache's layout. */
 tq_status tq_decode_attention_ex(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
                                  const void* q, int32_t q_dtype, const int32_t* d_seq_lens,
                                  int32_t max_seq_len, float* out, void* workspace,
@@ -307,12 +353,11 @@ tq_status tq_decode_attention_noalloc(const tq_cache_desc* desc, const tq_cache_
 /* Size in bytes of the fixed scratch array behind tq_decode_attention_noalloc. */
 size_t tq_decode_noalloc_max_scratch_bytes(void);
 
-/* The splits and V mode tq_decode_attention would use (host only).
- * tq_decode_attention_ex with v_mode TQ_VMODE_TENSOR and n_splits == 0 plans
- * the same splits; the tensor-core kernel also has a "stream-K" partition
- * (all 16-token tiles of all (batch, KV head) pairs spread evenly over one wave
- * of persistent CTAs, a pair's pieces merged by the last of them), selected by
- * v_mode TQ_VMODE_TENSOR_STREAMK; it needs tq_decode_workspace_bytes(desc, 1). */
+/* The splits and V mode tq_decode_attention would use (host only).  For the
+ * tensor-core kernel *splits_out is the number of CTAs (the 16-token tiles of
+ * all (batch, KV head) pairs, in pair order, are divided evenly over them; the
+ * pieces of a pair are merged by the last CTA to finish it), 0 when the
+ * device's occupancy is not known yet (no call has run on it). */
 tq_status tq_decode_plan(const tq_cache_desc* desc, int32_t max_seq_len, int32_t v_mode,
                          int32_t n_splits, int32_t* splits_out, int32_t* v_mode_out);
 

@@ -23,6 +23,7 @@ TQ_F32, TQ_F16, TQ_BF16 = 0, 1, 2
 TQ_ROT_WHT128, TQ_ROT_WHT32, TQ_ROT_SO4_WHT128 = 0, 1, 2
 TQ_PART_K_CODES, TQ_PART_K_NORMS, TQ_PART_V_CODES, TQ_PART_V_NORMS, TQ_PART_PARAMS = range(5)
 TQ_VMODE_AUTO, TQ_VMODE_TOKEN_PARALLEL, TQ_VMODE_DIM_PARALLEL, TQ_VMODE_TENSOR, TQ_VMODE_TENSOR_STREAMK = -1, 0, 1, 2, 3
+TQ_LAYOUT_NATURAL, TQ_LAYOUT_TILE16 = 0, 1
 TQ_HEAD_DIM, TQ_MAX_GROUP, TQ_MAX_SPLITS = 128, 16, 1024
 
 
@@ -36,7 +37,7 @@ class tq_cache_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "head_dim", "n_q_heads", "n_kv_heads", "batch", "t_capacity", "rot", "k_bits", "v_bits",
         "norm_dtype", "k_mixed", "group", "k_code_bytes", "v_code_bytes", "k_norm_slots",
-        "v_norm_slots", "norm_bytes")] + [("params_bytes", ctypes.c_int64)]
+        "v_norm_slots", "norm_bytes", "layout", "t_alloc")] + [("params_bytes", ctypes.c_int64)]
 
 
 class tq_cache_ptrs(ctypes.Structure):
@@ -277,16 +278,20 @@ class PackedKVCache:
         return out
 
     def norms_view(self, which: str):
+        """The norms array as stored: [batch][n_kv][t_alloc * slots] (norm dtype);
+        in the tile layout the positions within each 16-token tile are permuted
+        as include/tq.h documents."""
         torch = _torch()
         d = self.desc
         slots = d.k_norm_slots if which == "k" else d.v_norm_slots
         raw = self.k_norms if which == "k" else self.v_norms
         dt = torch.float16 if d.norm_dtype == TQ_F16 else torch.float32
-        n = d.batch * d.n_kv_heads * d.t_capacity * slots
-        return raw[: n * d.norm_bytes].view(dt).view(d.batch, d.n_kv_heads, d.t_capacity, slots)
+        n = d.batch * d.n_kv_heads * d.t_alloc * slots
+        return raw[: n * d.norm_bytes].view(dt).view(d.batch, d.n_kv_heads, d.t_alloc * slots)
 
     def codes_view(self, which: str):
+        """The code array as stored: [batch][n_kv][t_alloc * code_bytes] uint8."""
         d = self.desc
         nb = d.k_code_bytes if which == "k" else d.v_code_bytes
         raw = self.k_codes if which == "k" else self.v_codes
-        return raw[: d.batch * d.n_kv_heads * d.t_capacity * nb].view(d.batch, d.n_kv_heads, d.t_capacity, nb)
+        return raw[: d.batch * d.n_kv_heads * d.t_alloc * nb].view(d.batch, d.n_kv_heads, d.t_alloc * nb)

@@ -320,28 +320,6 @@ bool aligned(const void* p, size_t n) { return ((uintptr_t)p % n) == 0; }
 
 constexpr int kSMs = 152;
 
-// Sections per (batch, KV head) pair for the tensor-core kernel when the
-// stream-K grid is unavailable: an SM with at least four CTAs works through
-// them at a fixed rate, so a step takes about max(4, ceil(CTAs / SMs)) x (tiles
-// per warp + about two tiles of start-up); sections of at least 64 tokens.
-int tc_uniform_splits(long long pairs, int max_seq_len, int gp) {
-    long long cap = (max_seq_len + 63) / 64;
-    if (cap > TQ_MAX_SPLITS) cap = TQ_MAX_SPLITS;
-    long long best = 1;
-    double best_cost = 0.0;
-    for (long long sp = 1; sp <= cap; ++sp) {
-        const long long sec = (max_seq_len + sp - 1) / sp;
-        const long long per_warp = (sec + 63) / 64;
-        // CTAs an SM works through one after another (measured: fewer, longer
-        // sections win while the grid is under a wave or two)
-        const long long per_sm = (pairs * sp + kSMs - 1) / kSMs;
-        // + the last CTA's merge of the pair's sp partials (gp heads), after the rest
-        const double cost = (double)per_sm * ((double)per_warp + 2.0) + (sp > 1 ? (double)sp * gp / 24.0 : 0.0);
-        if (sp == 1 || cost < best_cost - 1e-9) { best_cost = cost; best = sp; }
-    }
-    return (int)best;
-}
-
 }  // namespace
 
 extern "C" {
@@ -355,7 +333,9 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc* d, int32_t max_splits) {
         const size_t sk = (size_t)tq_decode_tc_sk_slots(d);
         if (sk > slots) slots = sk;
     }
-    const size_t part = slots * padded_group(d->group) * kPartStride * sizeof(float);
+    // the tensor-core kernel's partials hold 4 or 8 heads (its head groups)
+    const int gp = tq_decode_tc_supported(d) ? (d->group <= 4 ? 4 : 8) : padded_group(d->group);
+    const size_t part = slots * (size_t)gp * kPartStride * sizeof(float);
     const size_t tick = ((pairs * sizeof(int32_t)) + 255) & ~(size_t)255;
     return tick + part;
 }
@@ -365,25 +345,23 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     if (!d || d->head_dim != TQ_HEAD_DIM || max_seq_len < 1 || max_seq_len > d->t_capacity) return TQ_ERR_INVALID_ARG;
     if (v_mode < TQ_VMODE_AUTO || v_mode > TQ_VMODE_TENSOR_STREAMK) return TQ_ERR_INVALID_ARG;
     if (n_splits < 0 || n_splits > TQ_MAX_SPLITS) return TQ_ERR_INVALID_ARG;
-    const bool tc = tq_decode_tc_supported(d);
-    int mode = v_mode;
-    if (mode == TQ_VMODE_AUTO) {
-        // the tensor-core kernel wins at every length measured (T = 128 .. 32768);
-        // without it, token-parallel below the crossover, dimension-parallel above
-        if (tc) mode = TQ_VMODE_TENSOR;
-        else mode = max_seq_len < tq_v_crossover() ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
-    }
-    if ((mode == TQ_VMODE_TENSOR || mode == TQ_VMODE_TENSOR_STREAMK) && !tc) return TQ_ERR_UNSUPPORTED;
-    if (mode == TQ_VMODE_TENSOR_STREAMK) {   // no per-pair sections
-        if (splits_out) *splits_out = 0;
+    int mode = v_mode == TQ_VMODE_TENSOR_STREAMK ? TQ_VMODE_TENSOR : v_mode;
+    if (tq_decode_tc_supported(d)) {
+        // tile layout: the tensor-core kernel, at every length (measured faster than
+        // the token-parallel kernel down to T = 128)
+        if (mode == TQ_VMODE_AUTO) mode = TQ_VMODE_TENSOR;
+        if (mode != TQ_VMODE_TENSOR) return TQ_ERR_UNSUPPORTED;
+        if (n_splits > tq_decode_tc_max_grid()) return TQ_ERR_INVALID_ARG;
+        if (splits_out) *splits_out = n_splits > 0 ? n_splits : tq_decode_tc_sk_grid(d, max_seq_len);
         if (v_mode_out) *v_mode_out = mode;
         return TQ_OK;
     }
+    // natural layout: token-parallel below the crossover, dimension-parallel above
+    if (mode == TQ_VMODE_TENSOR) return TQ_ERR_UNSUPPORTED;
+    if (mode == TQ_VMODE_AUTO) mode = max_seq_len < tq_v_crossover() ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
     int splits = n_splits;
     const long long pairs = (long long)d->batch * d->n_kv_heads;
-    if (splits == 0 && mode == TQ_VMODE_TENSOR) {
-        splits = tc_uniform_splits(pairs, max_seq_len, padded_group(d->group));
-    } else if (splits == 0) {
+    if (splits == 0) {
         // about 1.6 times the sections that fill the GPU once (four resident
         // 128-thread CTAs per SM), at most 128 partials per pair (the last CTA
         // merges them after the rest: past ~128 the merge costs more than the
@@ -418,19 +396,14 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     int splits = 0, mode = 0;
     tq_status st = tq_decode_plan(d, max_seq_len, v_mode, n_splits, &splits, &mode);
     if (st != TQ_OK) return st;
+    const bool tc = mode == TQ_VMODE_TENSOR;
+    if (tc && splits < 1) return TQ_ERR_CUDA;   // the device's occupancy could not be read
     const int kf = tq_k_fmt(d), vf = tq_v_fmt(d);
     int GP = 1;
     KernelFn fn = nullptr;
-    if (mode != TQ_VMODE_TENSOR && mode != TQ_VMODE_TENSOR_STREAMK) {
+    if (!tc) {
         fn = pick_kernel(d->group, kf, vf, mode, &GP);
         if (!fn) return TQ_ERR_UNSUPPORTED;
-    }
-    int sk_grid = 0;
-    if (mode == TQ_VMODE_TENSOR_STREAMK) {
-        mode = TQ_VMODE_TENSOR;
-        sk_grid = tq_decode_tc_sk_grid(d, max_seq_len);
-        if (sk_grid == 0)
-            splits = tc_uniform_splits((long long)d->batch * d->n_kv_heads, max_seq_len, padded_group(d->group));
     }
     DecodeArgs a;
     a.k_codes = static_cast<const uint8_t*>(c->k_codes);
@@ -446,8 +419,8 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.status = d_status;
     a.tickets = nullptr;
     a.ws_part = nullptr;
-    if (splits > 1 || sk_grid > 0) {
-        const size_t need = sk_grid > 0 ? tq_decode_workspace_bytes(d, 1) : tq_decode_workspace_bytes(d, splits);
+    if (splits > 1) {   // tensor core: several CTAs may share a pair
+        const size_t need = tq_decode_workspace_bytes(d, tc ? 1 : splits);
         if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return TQ_ERR_WORKSPACE;
         const size_t pairs = (size_t)d->batch * d->n_kv_heads;
         const size_t tick = ((pairs * sizeof(int32_t)) + 255) & ~(size_t)255;
@@ -458,23 +431,18 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.Hq = d->n_q_heads;
     a.Hkv = d->n_kv_heads;
     a.G = d->group;
-    a.Tcap = d->t_capacity;
+    a.Tcap = d->t_alloc;
+    a.t_cap = d->t_capacity;
     a.max_seq = max_seq_len;
-    a.n_splits = splits;
-    a.split_len = splits > 0 ? (max_seq_len + splits - 1) / splits : 0;
-    if (mode == TQ_VMODE_TENSOR) {
-        // sections start on 16-token tiles (16-byte aligned copies of codes and norms)
-        const int al = tq_decode_tc_split_align();
-        a.split_len = (a.split_len + al - 1) / al * al;
-    }
+    a.n_splits = tc ? 0 : splits;
+    a.split_len = tc ? 0 : (max_seq_len + splits - 1) / splits;
     a.q_dtype = q_dtype;
     a.norm_f16 = d->norm_dtype == TQ_F16;
     a.rot = d->rot;
     a.k_mixed = d->k_mixed;
     a.fold_mul = 1u << 20;
     if (d->batch > 65535 || d->n_kv_heads > 65535) return TQ_ERR_INVALID_ARG;
-    if (mode == TQ_VMODE_TENSOR)
-        return tq_decode_tc_launch(d, a, splits, sk_grid, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    if (tc) return tq_decode_tc_launch(d, a, splits, (cudaStream_t)stream) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
     dim3 grid(splits, d->n_kv_heads, d->batch);
     fn<<<grid, kThreads, 0, (cudaStream_t)stream>>>(a);
     return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
@@ -536,9 +504,10 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_cache_desc* d, const t
     int32_t splits = 0, mode = 0;
     tq_status st = tq_decode_plan(d, max_seq_len, TQ_VMODE_AUTO, 0, &splits, &mode);
     if (st != TQ_OK) return st;
+    if (splits < 1) return TQ_ERR_CUDA;
     if (splits == 1) return tq_decode_attention_ex(d, c, q, q_dtype, d_seq_lens, max_seq_len, out, nullptr, 0,
                                                    d_status, stream, TQ_VMODE_AUTO, 1);
-    const size_t need = tq_decode_workspace_bytes(d, splits > 0 ? splits : 1);
+    const size_t need = tq_decode_workspace_bytes(d, mode == TQ_VMODE_TENSOR ? 1 : splits);
     if (need == 0 || need > kNoAllocScratchBytes) return TQ_ERR_WORKSPACE;
     void* scratch = nullptr;
     st = scratch_address(&scratch);

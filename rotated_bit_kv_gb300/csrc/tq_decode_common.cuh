@@ -21,7 +21,9 @@ struct DecodeArgs {
     float* ws_part;
     int32_t* tickets;
     int32_t* status;
-    int B, Hq, Hkv, G, Tcap, max_seq, n_splits, split_len, q_dtype, norm_f16, rot, k_mixed;
+    // Tcap: positions per (batch, KV head) in the arrays (t_alloc); t_cap: the
+    // logical capacity (t_capacity)
+    int B, Hq, Hkv, G, Tcap, t_cap, max_seq, n_splits, split_len, q_dtype, norm_f16, rot, k_mixed;
     uint32_t fold_mul;   // 1 << 20 (a runtime operand keeps the selector fold on the FMA pipe)
 };
 }  // namespace tq
@@ -190,7 +192,7 @@ __device__ __forceinline__ void prologue(const DecodeArgs& a, const tq_head_para
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
     int L = a.seq_lens[b];
     int flags = 0;
-    if (L > a.Tcap) { flags |= TQ_DEV_SEQ_OVER_CAPACITY; L = a.Tcap; }
+    if (L > a.t_cap) { flags |= TQ_DEV_SEQ_OVER_CAPACITY; L = a.t_cap; }
     if (L > a.max_seq) { flags |= TQ_DEV_SEQ_OVER_MAX; L = a.max_seq; }
     if (L < 0) L = 0;
     if (flags && a.status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.status, flags);  // once per batch
@@ -298,14 +300,12 @@ __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*o
 
 }  // namespace
 
-// Tensor-core decode (tq_decode_tc.cu).  Returns false when the cache format
-// or group size has no tensor-core kernel.
+// Tensor-core decode on the tile layout (tq_decode_tile.cu).  Supported: every
+// TQ_LAYOUT_TILE16 cache.
 bool tq_decode_tc_supported(const tq_cache_desc* d);
-int tq_decode_tc_split_align();
-// Stream-K partition: partial slots the workspace must hold, and the grid (one
-// wave of resident CTAs; 0 when the occupancy cannot be read).
+// partial slots the workspace must hold, and the automatic grid (CTAs; 0 when the
+// occupancy cannot be read)
 int tq_decode_tc_sk_slots(const tq_cache_desc* d);
 int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len);
-// sk_grid > 0: stream-K over that many CTAs; else `splits` sections per pair.
-cudaError_t tq_decode_tc_launch(const tq_cache_desc* d, const tq::DecodeArgs& a, int splits, int sk_grid,
-                                cudaStream_t stream);
+int tq_decode_tc_max_grid();
+cudaError_t tq_decode_tc_launch(const tq_cache_desc* d, const tq::DecodeArgs& a, int grid, cudaStream_t stream);

@@ -1,0 +1,884 @@
+// Tensor-core decode attention on the 16-token tile layout (tq_tile.cuh): 3- or
+// 4-bit codes, one 128-wide rotation segment (WHT128, SO(4) o WHT128) or four
+// 32-wide blocks with a norm each (WHT32), up to 8 query heads per KV head.
+//
+// [RotaryQuant] Key design 3 and [TQ-MNN] §3.3: the QK dot products and the V
+// accumulation run in the rotated domain directly on the packed codes; q is
+// rotated once, the output once.  [Block-GTQ]: dequantised fp16 operands with
+// fp32 accumulation on tensor cores; key-axis split with log-sum-exp merge.
+//
+// Each warp takes whole tiles.  A lane loads its 48 (3-bit) or 64 (4-bit) bytes
+// of a tile's keys and values with two coalesced global loads each, straight into
+// registers, and turns every byte of them into an mma operand register with one
+// byte permute (the byte, placed above the lane's column, is the address) and one
+// shared-memory load from a table of code pairs: row e of the table holds, in
+// every lane's column, the fp16 pair (s c[lo(e)], s c[hi(e)]) of the field in
+// byte e, so the 32 lanes of a warp never share a bank.  Per group of four query
+// heads and per tile:
+//   QK:  S[16 tok x 8] = K~[16 x 128] . B_q[128 x 8]          (8 mma m16n8k16)
+//   PV:  O[64 pairs x 8] += V~[64 pairs x 32] . B_p[32 x 8]    (8 mma m16n8k16)
+// In QK column 2g of B_q holds head g's rotated query rounded to fp16 and column
+// 2g + 1 its rounding error, so that their sum carries the query to about 2^-22;
+// for the WHT32 format each 32-wide block accumulates in its own chain, which the
+// block's norm weighs.
+// In PV a row is a coordinate pair, a k index a (token, parity) pair and
+// B_p[(t, j)][(g, j')] = p_g(t) n_V(t) [j == j'], so that every operand register is
+// one field of one token for keys and values alike.
+//
+// Work split (stream-K): all tiles of all (batch, KV head) pairs, in pair order,
+// are divided evenly over a grid of persistent CTAs; a CTA's range is a sequence
+// of pieces of pairs.  The CTA's warps take a piece's tiles round-robin, merge
+// their softmax states in shared memory, and publish the piece's (m, l, o~); the
+// last CTA to finish a pair merges its pieces by log-sum-exp and applies R_V^T.
+#include <stddef.h>
+
+#include <mutex>
+#include <utility>
+
+#include "tq_decode_common.cuh"
+#include "tq_tile.cuh"
+
+namespace {
+
+using tqtile::kTok;
+
+#ifndef TQ_TILE_WARPS
+#define TQ_TILE_WARPS 8
+#endif
+constexpr int kNW = TQ_TILE_WARPS;       // warps per CTA
+constexpr int kNThr = kNW * 32;
+constexpr int kMaxGrid = 152 * 8;        // bound on CTAs (sizes the partial slots)
+
+template <int GPE>
+constexpr int pieces_per_round() { return GPE <= 4 ? 8 : 2; }
+
+// A piece: tiles [t_lo, t_hi) of pair (b, h) whose sequence has L tokens.  Its
+// partial goes to slot `slot`; the pair's partials are slots [first, first + parts).
+struct Seg {
+    int b, h, L, t_lo, t_hi, slot, first, parts;
+};
+
+template <int GPE>
+struct TileSmem {
+    static constexpr int NP = pieces_per_round<GPE>();
+    uint32_t tab[256 * 64];      // row e: 32 lane columns of table X, then 32 of table Y
+    float qts[NP][GPE][128];     // rotated queries of the round's pieces (log2 units)
+    float wo[kNW][GPE][128];     // warp states
+    float wm[kNW][8], wl[kNW][8];
+    float ot[8][128];
+    float mm[8], ll[8];
+    Seg seg[NP + 1];
+    long long scan[kNW];
+    long long b_base, next_pos, cur_base;
+    int b_first, cur_b, nseg, is_last;
+};
+
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float ex2(float x) {   // hardware 2^x (ftz); 2^-inf = 0
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ldg_stream4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_stream2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg_u64(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_u128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+template <class Fn, int... I>
+__device__ __forceinline__ void unroll_seq(Fn&& f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, class Fn>
+__device__ __forceinline__ void unroll(Fn&& f) {
+    unroll_seq(f, std::make_integer_sequence<int, N>{});
+}
+
+// ---- code-pair table and lookups
+
+// Table row e: columns 0..31 = X(e), 32..63 = Y(e), each value in all 32 columns.
+// 3-bit: X(e) = (s c[e & 7], s c[(e >> 3) & 7]) (field in byte bits 0-5);
+// Y(e) reads the field from byte bits 0-1 and 4-7 (the middle word of a group).
+// 4-bit: X(e) = (s c[e & 15], s c[e >> 4]).  s: the codebook's fp16 scale.
+template <int BITS>
+__device__ __forceinline__ void build_table(const tq_head_params& P0, uint32_t* tab) {
+    const float sc = P0.v_h_scale[0];
+    const float* cb = P0.v_cent[0];
+    for (int i = threadIdx.x; i < 256 * 16; i += kNThr) {
+        const int e = i >> 4, part = i & 15;
+        int lo, hi;
+        if (BITS == 4) {
+            lo = e & 15;
+            hi = e >> 4;
+        } else if (part < 8) {
+            lo = e & 7;
+            hi = (e >> 3) & 7;
+        } else {
+            const int f = (e & 3) | ((e >> 4) << 2);
+            lo = f & 7;
+            hi = f >> 3;
+        }
+        const uint32_t v = pack_h2(sc * cb[lo], sc * cb[hi]);
+        reinterpret_cast<uint4*>(tab)[i] = make_uint4(v, v, v, v);
+    }
+}
+
+__device__ __forceinline__ uint32_t lk(const uint32_t* tab, uint32_t addr) {
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(tab) + addr);
+}
+
+// table word of byte K of w: the byte goes to bits 8-15, the lane's column
+// offset (4 lane, + 128 for table Y) comes from byte 0 of `col`
+template <int K>
+__device__ __forceinline__ uint32_t lkb(const uint32_t* tab, uint32_t w, uint32_t col) {
+    return lk(tab, prmt(w, col, 0x5504u | (K << 4)));
+}
+
+// Table words of a three-word group of 3-bit codes: o[4 w + k] for byte k of word
+// w, o[12 + g] for the field spread over byte lane g of the three words.
+__device__ __forceinline__ void group3(const uint32_t* tab, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cx,
+                                       uint32_t cy, uint32_t (&o)[16]) {
+    unroll<4>([&](auto k_c) {
+        constexpr int k = decltype(k_c)::value;
+        o[k] = lkb<k>(tab, w0, cx);
+        o[4 + k] = lkb<k>(tab, w1, cy);
+        o[8 + k] = lkb<k>(tab, w2, cx);
+    });
+    const uint32_t m1 = 0x03030303u, m2 = 0x0F0F0F0Fu;
+    const uint32_t s1 = ((w0 >> 6) & m1) | (w1 & ~m1);
+    const uint32_t s2 = (s1 & m2) | ((w2 >> 2) & ~m2);
+    unroll<4>([&](auto g_c) {
+        constexpr int g = decltype(g_c)::value;
+        o[12 + g] = lkb<g>(tab, s2, cx);
+    });
+}
+
+// ... of a four-word group of 4-bit codes: o[4 w + k] for byte k of word w.
+__device__ __forceinline__ void group4(const uint32_t* tab, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                       uint32_t cx, uint32_t (&o)[16]) {
+    unroll<4>([&](auto k_c) {
+        constexpr int k = decltype(k_c)::value;
+        o[k] = lkb<k>(tab, w0, cx);
+        o[4 + k] = lkb<k>(tab, w1, cx);
+        o[8 + k] = lkb<k>(tab, w2, cx);
+        o[12 + k] = lkb<k>(tab, w3, cx);
+    });
+}
+
+// index into a value group's table words of field q of the low-half token (A) and
+// of the high-half token (B)
+template <int BITS>
+__host__ __device__ constexpr int vA(int q) {
+    return (BITS == 4 || q < 6) ? 4 * (q >> 1) + (q & 1) : 12 + (q - 6);
+}
+template <int BITS>
+__host__ __device__ constexpr int vB(int q) {
+    return (BITS == 4 || q < 6) ? 4 * (q >> 1) + 2 + (q & 1) : 14 + (q - 6);
+}
+
+// ---- per-lane context and tile registers
+
+struct Lane {
+    int r, c;
+    uint32_t cx, cy;           // table column offsets (X, Y) in byte 0
+    uint32_t sel_lo, sel_hi;   // P operand selectors (parity e = r & 1)
+    uint32_t sw_a, sw_b;       // value-norm pair selectors for the A and B token of a pair
+};
+
+__device__ __forceinline__ Lane lane_ctx() {
+    Lane l;
+    const int lane = threadIdx.x & 31;
+    l.r = lane >> 2;
+    l.c = lane & 3;
+    l.cx = 4u * lane;
+    l.cy = 4u * lane + 128u;
+    const bool e = l.r & 1;
+    // (x, 0) for parity 0, (0, x) for parity 1, x = low / high half of the source
+    l.sel_lo = e ? 0x1044u : 0x4410u;
+    l.sel_hi = e ? 0x3244u : 0x4432u;
+    l.sw_a = e ? 0x1032u : 0x3210u;
+    l.sw_b = e ? 0x3210u : 0x1032u;
+    return l;
+}
+
+template <int BITS, int NSEG>
+struct TileRegs {
+    static constexpr int W = tqtile::group_words(BITS);
+    uint32_t k[2 * W], v[2 * W];
+    uint32_t kn[NSEG == 1 ? 2 : 4];   // one slot: (n_r, n_r+8) as fp16 pair or two fp32
+    uint32_t vn[NSEG == 1 ? 2 : 8];
+};
+
+// Base pointers of one (batch, KV head) pair.
+struct PairPtr {
+    const uint8_t* k;
+    const uint8_t* v;
+    const uint8_t* kn;
+    const uint8_t* vn;
+};
+
+template <int BITS, int NSEG>
+__device__ __forceinline__ PairPtr pair_ptr(const DecodeArgs& a, int b, int h) {
+    const size_t pair = (size_t)b * a.Hkv + h;
+    const size_t tiles = (size_t)(a.Tcap / kTok);   // Tcap here is the allocated (tile-rounded) length
+    const int nb = a.norm_f16 ? 2 : 4;
+    PairPtr p;
+    p.k = a.k_codes + pair * tiles * tqtile::tile_bytes(BITS);
+    p.v = a.v_codes + pair * tiles * tqtile::tile_bytes(BITS);
+    p.kn = static_cast<const uint8_t*>(a.k_norms) + pair * tiles * kTok * NSEG * nb;
+    p.vn = static_cast<const uint8_t*>(a.v_norms) + pair * tiles * kTok * NSEG * nb;
+    return p;
+}
+
+template <int BITS, int NSEG>
+__device__ __forceinline__ void load_tile(TileRegs<BITS, NSEG>& td, const PairPtr& pp, int t, const Lane& ln,
+                                          bool f16n) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t* kt = pp.k + (size_t)t * tqtile::tile_bytes(BITS);
+    const uint8_t* vt = pp.v + (size_t)t * tqtile::tile_bytes(BITS);
+    const uint4 k0 = ldg_stream4(kt + 16 * lane), v0 = ldg_stream4(vt + 16 * lane);
+    td.k[0] = k0.x; td.k[1] = k0.y; td.k[2] = k0.z; td.k[3] = k0.w;
+    td.v[0] = v0.x; td.v[1] = v0.y; td.v[2] = v0.z; td.v[3] = v0.w;
+    if constexpr (BITS == 3) {
+        const uint2 k1 = ldg_stream2(kt + 512 + 8 * lane), v1 = ldg_stream2(vt + 512 + 8 * lane);
+        td.k[4] = k1.x; td.k[5] = k1.y;
+        td.v[4] = v1.x; td.v[5] = v1.y;
+    } else {
+        const uint4 k1 = ldg_stream4(kt + 512 + 16 * lane), v1 = ldg_stream4(vt + 512 + 16 * lane);
+        td.k[4] = k1.x; td.k[5] = k1.y; td.k[6] = k1.z; td.k[7] = k1.w;
+        td.v[4] = v1.x; td.v[5] = v1.y; td.v[6] = v1.z; td.v[7] = v1.w;
+    }
+    if constexpr (NSEG == 1) {
+        if (f16n) {
+            td.kn[0] = ldg_u32(pp.kn + ((size_t)t * kTok + 2 * ln.r) * 2);
+            td.vn[0] = ldg_u32(pp.vn + ((size_t)t * kTok + 2 * ln.r) * 2);
+            td.kn[1] = td.vn[1] = 0;
+        } else {
+            const uint2 kk = ldg_u64(pp.kn + ((size_t)t * kTok + 2 * ln.r) * 4);
+            const uint2 vv = ldg_u64(pp.vn + ((size_t)t * kTok + 2 * ln.r) * 4);
+            td.kn[0] = kk.x; td.kn[1] = kk.y;
+            td.vn[0] = vv.x; td.vn[1] = vv.y;
+        }
+    } else {   // fp16 block norms: keys of tokens r, r + 8; values of tokens 2c, 2c+1, 2c+8, 2c+9
+        const uint4 kk = ldg_u128(pp.kn + ((size_t)t * kTok * 4 + 8 * ln.r) * 2);
+        td.kn[0] = kk.x; td.kn[1] = kk.y; td.kn[2] = kk.z; td.kn[3] = kk.w;
+        const uint4 v0n = ldg_u128(pp.vn + ((size_t)t * kTok * 4 + 16 * ln.c) * 2);
+        const uint4 v1n = ldg_u128(pp.vn + ((size_t)t * kTok * 4 + 16 * ln.c + 8) * 2);
+        td.vn[0] = v0n.x; td.vn[1] = v0n.y; td.vn[2] = v0n.z; td.vn[3] = v0n.w;
+        td.vn[4] = v1n.x; td.vn[5] = v1n.y; td.vn[6] = v1n.z; td.vn[7] = v1n.w;
+    }
+}
+
+// Online-softmax state of one warp for NT groups of four heads; lane (r, c) holds
+// head 4j + c: o~ at coordinates 32 mt + 2r + {0, 1, 16, 17} (unnormalised), the
+// running base m (log2 units) and its part of the running sum l.
+template <int NT>
+struct WState {
+    float o[NT][4][4];
+    float m[NT], l[NT];
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            m[j] = -INFINITY;
+            l[j] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) o[j][mt][0] = o[j][mt][1] = o[j][mt][2] = o[j][mt][3] = 0.f;
+        }
+    }
+};
+
+__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+
+// fp16 pair of (x, y) (hi = false) or of what the fp16 rounding of (x, y) leaves
+// (hi = true gives the rounded pair itself)
+__device__ __forceinline__ uint32_t pack_part(float x, float y, bool lo) {
+    const uint32_t h = pack_h2(x, y);
+    if (!lo) return h;
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    return pack_h2(x - f.x, y - f.y);
+}
+
+// QK operand B from q~ ([GPE][128] floats, log2 units) times kinv: lane (r, c), head
+// 4j + r/2; k step st holds coordinates 16 st + 2c, +1 (b0) and 16 st + 2c + 8, +9
+// (b1).  Column parity r & 1 carries the fp16 rounding of q~ (0) or its rounding
+// error (1), so that the two columns add up to q~ to about 2^-22.
+template <int NT>
+__device__ __forceinline__ void load_bq(const float (*qts)[128], const Lane& ln, float kinv,
+                                        uint32_t (&bq)[NT][8][2]) {
+    const bool odd = ln.r & 1;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const float* qh = qts[4 * j + (ln.r >> 1)];
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            const int d0 = 16 * st + 2 * ln.c, d1 = d0 + 8;
+            bq[j][st][0] = pack_part(qh[d0] * kinv, qh[d0 + 1] * kinv, odd);
+            bq[j][st][1] = pack_part(qh[d1] * kinv, qh[d1 + 1] * kinv, odd);
+        }
+    }
+}
+
+// QK, online softmax and PV for one tile of `nval` valid tokens.
+template <int NT, int BITS, int NSEG>
+__device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nval, const uint32_t* tab,
+                                          const Lane& ln, const uint32_t (&bq)[NT][8][2], bool f16n,
+                                          WState<NT>& ws) {
+    const int r = ln.r;
+    // ---- QK: rows = tokens r (kr) and r + 8 (k8); accumulator chains: k steps of
+    // even / odd index (one norm) or one chain per 32-wide block (k steps 2b, 2b+1)
+    constexpr int CH = NSEG == 1 ? 2 : 4;
+    float acc[NT][CH][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < CH; ++q) acc[j][q][0] = acc[j][q][1] = acc[j][q][2] = acc[j][q][3] = 0.f;
+    {
+        uint32_t kr[16], k8[16];
+        if constexpr (BITS == 3) {
+            group3(tab, td.k[0], td.k[1], td.k[2], ln.cx, ln.cy, kr);
+            group3(tab, td.k[3], td.k[4], td.k[5], ln.cx, ln.cy, k8);
+        } else {
+            group4(tab, td.k[0], td.k[1], td.k[2], td.k[3], ln.cx, kr);
+            group4(tab, td.k[4], td.k[5], td.k[6], td.k[7], ln.cx, k8);
+        }
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            const int ch = NSEG == 1 ? (st & 1) : (st >> 1);
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+                mma16816(acc[j][ch], kr[2 * st], k8[2 * st], kr[2 * st + 1], k8[2 * st + 1], bq[j][st][0],
+                         bq[j][st][1]);
+        }
+    }
+
+    // ---- scores (log2 units) of tokens r and r + 8 for head 4j + c
+    float s0[NT], s8[NT];
+    if constexpr (NSEG == 1) {
+        const float kn0 = f16n ? h_lo(td.kn[0]) : __uint_as_float(td.kn[0]);
+        const float kn8 = f16n ? h_hi(td.kn[0]) : __uint_as_float(td.kn[1]);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {   // both columns: rounded q~ and its remainder
+            s0[j] = ((acc[j][0][0] + acc[j][1][0]) + (acc[j][0][1] + acc[j][1][1])) * kn0;
+            s8[j] = ((acc[j][0][2] + acc[j][1][2]) + (acc[j][0][3] + acc[j][1][3])) * kn8;
+        }
+    } else {
+        float n0[4], n8[4];
+        n0[0] = h_lo(td.kn[0]); n0[1] = h_hi(td.kn[0]); n0[2] = h_lo(td.kn[1]); n0[3] = h_hi(td.kn[1]);
+        n8[0] = h_lo(td.kn[2]); n8[1] = h_hi(td.kn[2]); n8[2] = h_lo(td.kn[3]); n8[3] = h_hi(td.kn[3]);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {   // per block: rounded q~ and its remainder, then the block's norm
+            float a0 = n0[0] * (acc[j][0][0] + acc[j][0][1]), a8 = n8[0] * (acc[j][0][2] + acc[j][0][3]);
+#pragma unroll
+            for (int b = 1; b < 4; ++b) {
+                a0 = fmaf(n0[b], acc[j][b][0] + acc[j][b][1], a0);
+                a8 = fmaf(n8[b], acc[j][b][2] + acc[j][b][3], a8);
+            }
+            s0[j] = a0;
+            s8[j] = a8;
+        }
+    }
+    const bool ragged = nval < kTok;
+    if (ragged) {   // tokens past the end take no weight
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            if (r >= nval) s0[j] = -INFINITY;
+            if (r + 8 >= nval) s8[j] = -INFINITY;
+        }
+    }
+
+    // ---- online softmax: the base moves only when the tile maximum exceeds it by
+    // more than 4 (log2 units), so p <= 16 and rescales are rare
+    float mn[NT];
+    bool move = false;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        float mt = fmaxf(s0[j], s8[j]);
+        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 16));
+        mn[j] = mt > ws.m[j] + 4.f ? mt : ws.m[j];
+        move = move || mn[j] != ws.m[j];
+    }
+    if (__any_sync(TQ_FULL_MASK, move)) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const float cf = ex2(ws.m[j] - mn[j]);   // 0 on the first tile (m = -inf)
+            ws.l[j] *= cf;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                ws.o[j][mt][0] *= cf; ws.o[j][mt][1] *= cf; ws.o[j][mt][2] *= cf; ws.o[j][mt][3] *= cf;
+            }
+            ws.m[j] = mn[j];
+        }
+    }
+
+    // ---- P operand (k = token-parity pairs, columns = head-parity pairs)
+    // After the transposes lane (r, c) holds, for head r/2 (+4j), tokens 2c, 2c+1
+    // (T0) and 2c+8, 2c+9 (T1); k step u = 0 takes tokens 2c (b0) and 2c+1 (b1),
+    // u = 1 tokens 2c+8 and 2c+9.
+    uint32_t bp[NT][2][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        float p0 = ex2(s0[j] - ws.m[j]), p8 = ex2(s8[j] - ws.m[j]);
+        ws.l[j] += p0 + p8;
+        if constexpr (NSEG == 1) {
+            float vn0 = f16n ? h_lo(td.vn[0]) : __uint_as_float(td.vn[0]);
+            float vn8 = f16n ? h_hi(td.vn[0]) : __uint_as_float(td.vn[1]);
+            if (ragged) {   // past the end: zero weight even if the stored norm is not finite
+                vn0 = r < nval ? vn0 : 0.f;
+                vn8 = r + 8 < nval ? vn8 : 0.f;
+            }
+            p0 *= vn0;
+            p8 *= vn8;
+        }
+        const uint32_t t0 = movtrans(pack_h2(p0, p0)), t1 = movtrans(pack_h2(p8, p8));
+        bp[j][0][0] = prmt(t0, 0u, ln.sel_lo);
+        bp[j][0][1] = prmt(t0, 0u, ln.sel_hi);
+        bp[j][1][0] = prmt(t1, 0u, ln.sel_lo);
+        bp[j][1][1] = prmt(t1, 0u, ln.sel_hi);
+    }
+
+    // ---- PV: group u of the values holds tokens 2c + 8u (A) and 2c + 1 + 8u (B)
+    unroll<2>([&](auto u_c) {
+        constexpr int u = decltype(u_c)::value;
+        constexpr int W = tqtile::group_words(BITS);
+        uint32_t vg[16];
+        if constexpr (BITS == 3) group3(tab, td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], ln.cx, ln.cy, vg);
+        else group4(tab, td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], td.v[W * u + 3], ln.cx, vg);
+        // four blocks: each m tile is one block; its value norms scale the P operand
+        uint32_t wa[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};
+        if constexpr (NSEG == 4) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                uint32_t w = td.vn[4 * u + b];   // (n_b(2c + 8u), n_b(2c + 1 + 8u))
+                if (ragged) {
+                    const int ta = 2 * ln.c + 8 * u;
+                    w = (ta < nval ? (w & 0xFFFFu) : 0u) | (ta + 1 < nval ? (w & 0xFFFF0000u) : 0u);
+                }
+                wa[b] = prmt(w, w, ln.sw_a);
+                wb[b] = prmt(w, w, ln.sw_b);
+            }
+        }
+        unroll<4>([&](auto mt_c) {
+            constexpr int mt = decltype(mt_c)::value;
+            const uint32_t a0 = vg[vA<BITS>(2 * mt)], a1 = vg[vA<BITS>(2 * mt + 1)];
+            const uint32_t a2 = vg[vB<BITS>(2 * mt)], a3 = vg[vB<BITS>(2 * mt + 1)];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                if constexpr (NSEG == 1) {
+                    mma16816(ws.o[j][mt], a0, a1, a2, a3, bp[j][u][0], bp[j][u][1]);
+                } else {
+                    mma16816(ws.o[j][mt], a0, a1, a2, a3, hmul2(bp[j][u][0], wa[mt]), hmul2(bp[j][u][1], wb[mt]));
+                }
+            }
+        });
+    });
+}
+
+// A warp's state into its merge slot: wo[g][128], wm[g], wl[g] for its heads.
+template <int NT>
+__device__ __forceinline__ void warp_state_out(WState<NT>& ws, const Lane& ln, float (*wo)[128], float* wm,
+                                               float* wl) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) ws.l[j] += __shfl_xor_sync(TQ_FULL_MASK, ws.l[j], msk);
+        if (ln.r == 0) {
+            wm[4 * j + ln.c] = ws.m[j];
+            wl[4 * j + ln.c] = ws.l[j];
+        }
+        float* dst = wo[4 * j + ln.c];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            const int d = 32 * mt + 2 * ln.r;
+            *reinterpret_cast<float2*>(dst + d) = make_float2(ws.o[j][mt][0], ws.o[j][mt][1]);
+            *reinterpret_cast<float2*>(dst + d + 16) = make_float2(ws.o[j][mt][2], ws.o[j][mt][3]);
+        }
+    }
+}
+
+// Merge the kNW warp states into ot[g][128] (scaled by vinv) and mm/ll[g].
+template <int EP, int GPE>
+__device__ __forceinline__ void merge_warps(const float (*wo)[GPE][128], const float (*wm)[8], const float (*wl)[8],
+                                            float vinv, float (*ot)[128], float* mm, float* ll) {
+    for (int i = threadIdx.x; i < EP * 128; i += kNThr) {
+        const int g = i >> 7, d = i & 127;
+        float M = -INFINITY;
+        for (int w = 0; w < kNW; ++w) M = fmaxf(M, wm[w][g]);
+        float Lt = 0.f, ov = 0.f;
+        for (int w = 0; w < kNW; ++w) {
+            const float wt = (M == -INFINITY || wm[w][g] == -INFINITY) ? 0.f : exp2f(wm[w][g] - M);
+            Lt = fmaf(wt, wl[w][g], Lt);
+            ov = fmaf(wt, wo[w][g][d], ov);
+        }
+        ot[g][d] = ov * vinv;   // the table carried the scale s
+        if (d == 0) {
+            mm[g] = M;
+            ll[g] = Lt;
+        }
+    }
+}
+
+// Finish a piece: ot[g][c] holds its unnormalised o~, (mm[g], ll[g]) its softmax
+// state (shared memory).  One part: normalise and write; else publish the partial
+// and let the last CTA of the pair merge all of them.
+template <int GP>
+__device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const float* mm,
+                             const float* ll, int* is_last, const Seg& sg) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int pair = sg.b * a.Hkv + sg.h;
+    if (sg.parts > 1) {
+        float* part = a.ws_part + (size_t)sg.slot * GP * kPartStride;
+        for (int i = tid; i < GP * 128; i += kNThr) part[(i >> 7) * kPartStride + (i & 127)] = ot[i >> 7][i & 127];
+        if (tid < GP) {
+            part[tid * kPartStride + 128] = mm[tid];
+            part[tid * kPartStride + 129] = ll[tid];
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const int ticket = atomicAdd(a.tickets + pair, 1);
+            *is_last = ticket == sg.parts - 1;
+        }
+        __syncthreads();
+        if (!*is_last) return;
+        __threadfence();
+        // log-sum-exp merge over the pair's parts  [Block-GTQ]
+        merge_parts<GP, kNThr>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot);
+        if (tid == 0) a.tickets[pair] = 0;   // ready for the next call
+        __syncthreads();
+    } else {
+        for (int i = tid; i < GP * 128; i += kNThr) {
+            const int g = i >> 7;
+            ot[g][i & 127] = ll[g] > 0.f ? ot[g][i & 127] / ll[g] : 0.f;
+        }
+        __syncthreads();
+    }
+    // o = R_V^T o~, once per query head  [RotaryQuant Key design 3, Kernel D]
+    for (int g = warp; g < a.G; g += kNW) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ot[g][4 * lane + i];
+        tq::rotate_inverse(a.rot, P, v);
+        float4* o4 = reinterpret_cast<float4*>(a.out + ((size_t)sg.b * a.Hq + (size_t)sg.h * a.G + g) * 128) + lane;
+        *o4 = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// q~ = R_K q of head g of pair (b, h) into dst[128] (log2 units); one warp
+__device__ __forceinline__ void rotate_q(const DecodeArgs& a, const tq_head_params& P, int b, int h, int g,
+                                         float* dst) {
+    const int lane = threadIdx.x & 31;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (g < a.G) {
+        const size_t elem = ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128 + 4 * lane;
+        tq::load4(a.q, elem, a.q_dtype, v);
+        tq::rotate_forward(a.rot, P, v);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[4 * lane + i] = v[i] * (kLog2e * kInvSqrtD);
+}
+
+// clamped length of batch b's sequences (flags raised when asked)
+__device__ __forceinline__ int seq_len_of(const DecodeArgs& a, int b, bool report) {
+    int L = a.seq_lens[b];
+    int flags = 0;
+    if (L > a.t_cap) { flags |= TQ_DEV_SEQ_OVER_CAPACITY; L = a.t_cap; }
+    if (L > a.max_seq) { flags |= TQ_DEV_SEQ_OVER_MAX; L = a.max_seq; }
+    if (L < 0) L = 0;
+    if (report && flags && a.status) atomicOr(a.status, flags);
+    return L;
+}
+
+template <int NT, int BITS, int NSEG>
+__global__ void __launch_bounds__(kNThr, NT == 1 ? 2 : 1) decode_tile(DecodeArgs a) {
+    constexpr int GPE = 4 * NT;
+    constexpr int NP = pieces_per_round<GPE>();
+    extern __shared__ __align__(128) unsigned char tile_smem_raw[];
+    TileSmem<GPE>& S = *reinterpret_cast<TileSmem<GPE>*>(tile_smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // launched as a programmatic dependent of the previous kernel in the stream:
+    // nothing is read before that kernel has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    build_table<BITS>(a.params[0], S.tab);
+    const bool f16n = a.norm_f16 != 0;
+
+    // ---- the CTA's range of tile positions: all tiles of all pairs in pair order
+    const int per = (a.B + kNThr - 1) / kNThr;   // batches summed by each thread, in order
+    const int bt0 = min(a.B, tid * per), bt1 = min(a.B, bt0 + per);
+    long long loc = 0;
+    for (int bb = bt0; bb < bt1; ++bb) loc += (seq_len_of(a, bb, blockIdx.x == 0) + kTok - 1) / kTok;
+    long long inc = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const long long y = __shfl_up_sync(TQ_FULL_MASK, inc, d);
+        if (lane >= d) inc += y;
+    }
+    if (lane == 31) S.scan[warp] = inc;
+    if (tid == 0) S.b_first = -1;
+    __syncthreads();
+    long long before = 0, total = 0;
+    for (int w = 0; w < kNW; ++w) {
+        before += w < warp ? S.scan[w] : 0;
+        total += S.scan[w];
+    }
+    const long long pre = before + inc - loc;   // tiles per head of batches < bt0
+    const long long tiles_all = total * a.Hkv;
+    const long long Wd = (tiles_all + gridDim.x - 1) / gridDim.x;
+    const long long lo = (long long)blockIdx.x * Wd, hi = min(lo + Wd, tiles_all);
+    if (lo < hi && (long long)a.Hkv * pre <= lo && lo < (long long)a.Hkv * (pre + loc)) {
+        long long p = (long long)a.Hkv * pre;
+        for (int bb = bt0; bb < bt1; ++bb) {
+            const long long n = (long long)a.Hkv * ((seq_len_of(a, bb, false) + kTok - 1) / kTok);
+            if (lo < p + n) { S.b_first = bb; S.b_base = p; break; }
+            p += n;
+        }
+    }
+    // batches with no tokens get zero output (no tile of theirs exists)
+    for (int bb = blockIdx.x; bb < a.B; bb += gridDim.x) {
+        if (seq_len_of(a, bb, false) == 0) {
+            float* ob = a.out + (size_t)bb * a.Hq * 128;
+            for (int i = tid; i < a.Hq * 128; i += kNThr) ob[i] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (lo >= hi || S.b_first < 0) return;
+    if (tid == 0) {
+        S.next_pos = lo;
+        S.cur_b = S.b_first;
+        S.cur_base = S.b_base;
+    }
+    const Lane ln = lane_ctx();
+    const float kinv = 1.0f / a.params[0].k_h_scale[0], vinv = 1.0f / a.params[0].v_h_scale[0];
+
+    for (;;) {
+        // ---- next round: up to NP pieces from next_pos (thread 0)
+        __syncthreads();
+        if (tid == 0) {
+            long long p = S.next_pos, base = S.cur_base;
+            int b = S.cur_b, n = 0;
+            while (p < hi && n < NP && b < a.B) {
+                const int L = seq_len_of(a, b, false);
+                const int nt = (L + kTok - 1) / kTok;
+                if (nt == 0 || p >= base + (long long)a.Hkv * nt) {
+                    base += (long long)a.Hkv * nt;
+                    ++b;
+                    continue;
+                }
+                const long long rel = p - base;
+                const int h = (int)(rel / nt);
+                const int t = (int)(rel - (long long)h * nt);
+                const long long pstart = base + (long long)h * nt;
+                const int take = (int)min((long long)(nt - t), hi - p);
+                const long long fc = pstart / Wd, lc = (pstart + nt - 1) / Wd;
+                const int pair = b * a.Hkv + h;
+                Seg& sg = S.seg[n];
+                sg.b = b;
+                sg.h = h;
+                sg.L = L;
+                sg.t_lo = t;
+                sg.t_hi = t + take;
+                sg.first = (int)fc + pair;   // slot of CTA c for pair p: c + p (unique along the tile order)
+                sg.slot = (int)blockIdx.x + pair;
+                sg.parts = (int)(lc - fc + 1);
+                p += take;
+                ++n;
+            }
+            S.nseg = n;
+            S.next_pos = p;
+            S.cur_b = b;
+            S.cur_base = base;
+        }
+        __syncthreads();
+        const int nseg = S.nseg;
+        if (nseg == 0) break;
+
+        // first tile of the round, in flight while the queries are rotated
+        TileRegs<BITS, NSEG> ta, tb;
+        PairPtr pp = pair_ptr<BITS, NSEG>(a, S.seg[0].b, S.seg[0].h);
+        bool a_loaded = false;
+        if (S.seg[0].t_lo + warp < S.seg[0].t_hi) {
+            load_tile(ta, pp, S.seg[0].t_lo + warp, ln, f16n);
+            a_loaded = true;
+        }
+        for (int i = warp; i < nseg * GPE; i += kNW) {
+            const Seg& sg = S.seg[i / GPE];
+            rotate_q(a, a.params[sg.h], sg.b, sg.h, i % GPE, S.qts[i / GPE][i % GPE]);
+        }
+        __syncthreads();
+
+        for (int k = 0; k < nseg; ++k) {
+            const Seg sg = S.seg[k];
+            const tq_head_params& P = a.params[sg.h];
+            uint32_t bq[NT][8][2];
+            load_bq<NT>(S.qts[k], ln, kinv, bq);
+            WState<NT> ws;
+            ws.reset();
+            // this warp's tiles of the piece: t_lo + warp + kNW i; tile 0 is in ta
+            const int n = sg.t_hi - sg.t_lo > warp ? (sg.t_hi - sg.t_lo - warp + kNW - 1) / kNW : 0;
+            auto tile_at = [&](int i) { return sg.t_lo + warp + kNW * i; };
+            auto nval_at = [&](int i) { return min(kTok, sg.L - tile_at(i) * kTok); };
+            if (n > 0 && !a_loaded) load_tile(ta, pp, tile_at(0), ln, f16n);
+            for (int i = 0; i < n; i += 2) {
+                if (i + 1 < n) load_tile(tb, pp, tile_at(i + 1), ln, f16n);
+                tile_step<NT, BITS, NSEG>(ta, nval_at(i), S.tab, ln, bq, f16n, ws);
+                if (i + 1 >= n) break;
+                if (i + 2 < n) load_tile(ta, pp, tile_at(i + 2), ln, f16n);
+                tile_step<NT, BITS, NSEG>(tb, nval_at(i + 1), S.tab, ln, bq, f16n, ws);
+            }
+            // the next piece's first tile, in flight during the merge
+            a_loaded = false;
+            if (k + 1 < nseg) {
+                const Seg& sn = S.seg[k + 1];
+                pp = pair_ptr<BITS, NSEG>(a, sn.b, sn.h);
+                if (sn.t_lo + warp < sn.t_hi) {
+                    load_tile(ta, pp, sn.t_lo + warp, ln, f16n);
+                    a_loaded = true;
+                }
+            }
+            warp_state_out<NT>(ws, ln, S.wo[warp], S.wm[warp], S.wl[warp]);
+            __syncthreads();
+            merge_warps<GPE, GPE>(S.wo, S.wm, S.wl, vinv, S.ot, S.mm, S.ll);
+            __syncthreads();
+            finish_piece<GPE>(a, P, S.ot, S.mm, S.ll, &S.is_last, sg);
+            __syncthreads();
+        }
+    }
+}
+
+template <int NT, int BITS, int NSEG>
+constexpr size_t smem_bytes() { return sizeof(TileSmem<4 * NT>); }
+
+using KernelPtr = void (*)(DecodeArgs);
+
+template <int NT, int BITS, int NSEG>
+KernelPtr kernel_of() { return decode_tile<NT, BITS, NSEG>; }
+
+KernelPtr pick(const tq_cache_desc* d, size_t* smem) {
+    const bool b4 = d->k_bits == 4;
+    const bool blk = d->rot == TQ_ROT_WHT32;
+    if (d->group <= 4) {
+        *smem = sizeof(TileSmem<4>);
+        if (blk) return b4 ? kernel_of<1, 4, 4>() : kernel_of<1, 3, 4>();
+        return b4 ? kernel_of<1, 4, 1>() : kernel_of<1, 3, 1>();
+    }
+    *smem = sizeof(TileSmem<8>);
+    if (blk) return b4 ? kernel_of<2, 4, 4>() : kernel_of<2, 3, 4>();
+    return b4 ? kernel_of<2, 4, 1>() : kernel_of<2, 3, 1>();
+}
+
+// resident CTAs of the kernel for this format (CTAs per SM x SMs), looked up once
+// per device and kernel
+int grid_cap(const tq_cache_desc* d) {
+    static std::mutex mu;
+    static int cache[64][8];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int which = (d->group <= 4 ? 0 : 4) + (d->k_bits == 4 ? 2 : 0) + (d->rot == TQ_ROT_WHT32 ? 1 : 0);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev][which]) {
+        size_t smem = 0;
+        KernelPtr fn = pick(d, &smem);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kNThr, smem) != cudaSuccess || n < 1) return 0;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 0;
+        cache[dev][which] = n * sms;
+    }
+    return cache[dev][which];
+}
+
+}  // namespace
+
+bool tq_decode_tc_supported(const tq_cache_desc* d) { return d->layout == TQ_LAYOUT_TILE16; }
+
+int tq_decode_tc_sk_slots(const tq_cache_desc* d) { return kMaxGrid + d->batch * d->n_kv_heads; }
+
+int tq_decode_tc_max_grid() { return kMaxGrid; }
+
+int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len) {
+    // resident CTAs on this device; without one, the design's: 2 (4 query heads
+    // per KV head) or 1 (8) CTAs per SM on 152 SMs
+    int cap = grid_cap(d);
+    if (cap <= 0) cap = (d->group <= 4 ? 2 : 1) * 152;
+    // at least 4 tiles per warp of a CTA on average
+    const long long tiles = (long long)d->batch * d->n_kv_heads * ((max_seq_len + kTok - 1) / kTok);
+    long long g = (tiles + 4 * kNW - 1) / (4 * kNW);
+    if (g > cap) g = cap;
+    if (g > kMaxGrid) g = kMaxGrid;
+    return g < 1 ? 1 : (int)g;
+}
+
+cudaError_t tq_decode_tc_launch(const tq_cache_desc* d, const tq::DecodeArgs& a, int grid, cudaStream_t stream) {
+    // sets the kernel's dynamic shared-memory limit on this device (once)
+    if (grid_cap(d) <= 0) return cudaErrorInvalidConfiguration;
+    size_t smem = 0;
+    KernelPtr fn = pick(d, &smem);
+    // programmatic dependent launch: the CTAs are placed while the previous kernel
+    // (typically the token append) finishes, and wait for it on the device
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kNThr);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, a);
+}

@@ -292,13 +292,21 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     d->k_norm_slots = (k_mixed || rot == TQ_ROT_WHT32) ? 4 : 1;
     d->v_norm_slots = rot == TQ_ROT_WHT32 ? 4 : 1;
     d->norm_bytes = norm_dtype == TQ_F16 ? 2 : 4;
+    // the tile layout (read by the tensor-core decode kernel) for every format it
+    // covers: no mixed-rate keys, at most 8 query heads per KV head, fp16 norms
+    // for the four-block format
+    const bool tile = !k_mixed && d->group <= 8 && !(rot == TQ_ROT_WHT32 && norm_dtype != TQ_F16);
+    d->layout = tile ? TQ_LAYOUT_TILE16 : TQ_LAYOUT_NATURAL;
+    const int64_t alloc = tile ? ((int64_t)t_capacity + 15) / 16 * 16 : t_capacity;
+    if (alloc > 0x7fffffff) return TQ_ERR_INVALID_ARG;
+    d->t_alloc = (int32_t)alloc;
     d->params_bytes = tq_params_blob_bytes(n_kv_heads, k_mixed);
     return TQ_OK;
 }
 
 size_t tq_cache_bytes(const tq_cache_desc* d, int32_t part) {
     if (!d || d->head_dim != TQ_HEAD_DIM) return 0;
-    size_t vecs = (size_t)d->batch * d->n_kv_heads * d->t_capacity;
+    size_t vecs = (size_t)d->batch * d->n_kv_heads * d->t_alloc;
     switch (part) {
         case TQ_PART_K_CODES: return vecs * d->k_code_bytes;
         case TQ_PART_K_NORMS: return vecs * d->k_norm_slots * d->norm_bytes;

@@ -13,6 +13,7 @@
 #include <numeric>
 
 #include "tq_device.cuh"
+#include "tq_tile.cuh"
 
 namespace {
 
@@ -24,9 +25,39 @@ struct QuantArgs {
     const float* kmat;           // mixed-rate keys only
     const int32_t* start_pos;
     int32_t* status;
-    int B, n_new, Hkv, Tcap, in_dtype, norm_f16, rot, k_mixed;
+    // Tcap: the capacity (valid positions); t_alloc: positions per (batch, KV
+    // head) in the arrays; tiled: TQ_LAYOUT_TILE16 (tq_tile.cuh) else one record
+    // per position
+    int B, n_new, Hkv, Tcap, t_alloc, tiled, in_dtype, norm_f16, rot, k_mixed;
     int code_bytes[2], norm_slots[2];
 };
+
+// Element index of norm slot k of the vector at position `pos` = pair * t_alloc +
+// slot (which: 0 keys, 1 values).
+__device__ __forceinline__ size_t norm_index(const QuantArgs& a, int which, size_t pos, int slots, int k) {
+    if (!a.tiled) return pos * slots + k;
+    const size_t base = (pos & ~(size_t)15) * slots;
+    const int t = (int)(pos & 15);
+    if (slots == 1) return base + tqtile::norm_pos1(t);
+    return base + (which == 0 ? tqtile::norm_pos4_k(t, k) : tqtile::norm_pos4_v(t, k));
+}
+
+// Scatter the packed record `rec` (shared memory, visible to the whole warp) of
+// the vector at position `pos` into its tile; every lane of the warp calls this.
+__device__ __forceinline__ void store_tiled(const QuantArgs& a, int which, size_t pos, const uint32_t* rec,
+                                            int bits, int lane) {
+    uint8_t* codes = which ? a.codes[1] : a.codes[0];
+    const int t = (int)(pos & 15);
+    if (bits == 3) {
+        uint8_t* tile = codes + (pos >> 4) * tqtile::tile_bytes(3);
+        if (which == 0) tqtile::store_key<3>(tile, rec, t, lane);
+        else tqtile::store_value<3>(tile, rec, t, lane);
+    } else {
+        uint8_t* tile = codes + (pos >> 4) * tqtile::tile_bytes(4);
+        if (which == 0) tqtile::store_key<4>(tile, rec, t, lane);
+        else tqtile::store_value<4>(tile, rec, t, lane);
+    }
+}
 
 constexpr int kWarps = 8;
 constexpr long long kMaxBlocks = 152LL * 8 * 4;   // four waves of 8 resident CTAs per SM
@@ -153,8 +184,11 @@ __device__ __forceinline__ void encode_vector(const QuantArgs& a, const VecId& i
         }
     }
 
-    // pack and store
-    uint8_t* rec = (which ? a.codes[1] : a.codes[0]) + ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (which ? a.code_bytes[1] : a.code_bytes[0]);
+    // pack and store (tile layout: the record goes through the warp's staging
+    // buffer, free here since mixed-rate keys never use that layout)
+    const size_t pos = (((size_t)b * a.Hkv + h) * a.t_alloc) + slot;
+    uint8_t* rec = a.tiled ? reinterpret_cast<uint8_t*>(xs)
+                           : (which ? a.codes[1] : a.codes[0]) + pos * (which ? a.code_bytes[1] : a.code_bytes[0]);
     const bool nib = mixed || seg_bits[0] == 4;
     if (nib) {
         const uint32_t v16 = idx[0] | (idx[1] << 4) | (idx[2] << 8) | (idx[3] << 12);
@@ -177,9 +211,13 @@ __device__ __forceinline__ void encode_vector(const QuantArgs& a, const VecId& i
         }
         if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = word;
     }
+    if (a.tiled) {
+        __syncwarp();
+        store_tiled(a, which, pos, reinterpret_cast<const uint32_t*>(rec), nib ? 4 : 3, lane);
+    }
     const int slots = (which ? a.norm_slots[1] : a.norm_slots[0]);
     if (lane < slots) {
-        const size_t ni = ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * slots + lane;
+        const size_t ni = norm_index(a, which, pos, slots, lane);
         float n = nrm[0];
 #pragma unroll
         for (int k = 1; k < 4; ++k) n = lane == k ? nrm[k] : n;
@@ -232,7 +270,7 @@ __device__ __forceinline__ void search_pack(const QuantArgs& a, const float* bnd
 }
 
 template <int ROT>
-__device__ __forceinline__ void encode_fast(const QuantArgs& a, const VecId& id, const float* xin) {
+__device__ __forceinline__ void encode_fast(const QuantArgs& a, const VecId& id, const float* xin, float* xs) {
     const int lane = threadIdx.x & 31;
     const int which = id.which, h = id.h, t = id.t, b = id.b;
     const int slot = a.start_pos[b] + t;
@@ -258,14 +296,20 @@ __device__ __forceinline__ void encode_fast(const QuantArgs& a, const VecId& id,
     const int s = ROT == TQ_ROT_WHT32 ? lane >> 3 : 0;
     const int bits = which == 0 ? P.k_seg_bits[s] : P.v_seg_bits[s];
     const float* bnd = which == 0 ? P.k_bound[s] : P.v_bound[s];
-    uint8_t* rec = (which ? a.codes[1] : a.codes[0]) + ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * (which ? a.code_bytes[1] : a.code_bytes[0]);
+    const size_t pos = (((size_t)b * a.Hkv + h) * a.t_alloc) + slot;
+    uint8_t* rec = a.tiled ? reinterpret_cast<uint8_t*>(xs)
+                           : (which ? a.codes[1] : a.codes[0]) + pos * (which ? a.code_bytes[1] : a.code_bytes[0]);
     if (bits == 4) search_pack<4>(a, bnd, y, rec);
     else search_pack<3>(a, bnd, y, rec);
+    if (a.tiled) {
+        __syncwarp();
+        store_tiled(a, which, pos, reinterpret_cast<const uint32_t*>(rec), bits, lane);
+    }
     // norms: one per vector, or one per 32-dim block (lanes 0, 8, 16, 24 hold them)
     const int slots = (which ? a.norm_slots[1] : a.norm_slots[0]);
     const float nv = ROT == TQ_ROT_WHT32 ? __shfl_sync(TQ_FULL_MASK, n, 8 * (lane & 3)) : n;
     if (lane < slots) {
-        const size_t ni = ((((size_t)b * a.Hkv + h) * a.Tcap) + slot) * slots + lane;
+        const size_t ni = norm_index(a, which, pos, slots, lane);
         if (a.norm_f16) static_cast<__half*>((which ? a.norms[1] : a.norms[0]))[ni] = __float2half_rn(nv);
         else static_cast<float*>((which ? a.norms[1] : a.norms[0]))[ni] = nv;
     }
@@ -297,7 +341,7 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
             tq::load4((idn.which ? a.src[1] : a.src[0]), input_elem(vn), a.in_dtype, xn);
         }
         if constexpr (ROT < 0) encode_vector(a, id, x, xs_all[wib]);
-        else encode_fast<ROT>(a, id, x);
+        else encode_fast<ROT>(a, id, x, xs_all[wib]);
         if (!more) break;
         __syncwarp();
         v = vn;
@@ -448,6 +492,7 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
     // a programmatic dependent launched after this kernel (decode) may be placed now;
     // it still waits for this grid's completion before it reads anything
     asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ __align__(16) uint32_t recbuf[kWarps][2][16];   // tile layout: the K and V records
     const int lane = threadIdx.x & 31, hv = lane >> 4, j = lane & 15;
     const uint32_t nwarps = gridDim.x * kWarps;
     const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) pairs
@@ -520,8 +565,9 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
             uint32_t code = 0;   // 8 indices of BITS bits, coordinate 8j + i at bit BITS * i
 #pragma unroll
             for (int i = 0; i < 8; ++i) code |= search_bits<BITS>(y[i] * inv, hp.bd) << (BITS * i);
-            const size_t rec_i = (((size_t)b * Hkv + h) * Tcap) + slot;
-            uint32_t* rec = reinterpret_cast<uint32_t*>(cbase + rec_i * cbytes);
+            const size_t rec_i = (((size_t)b * Hkv + h) * a.t_alloc) + slot;
+            uint32_t* const rb = recbuf[threadIdx.x >> 5][hv];
+            uint32_t* rec = a.tiled ? rb : reinterpret_cast<uint32_t*>(cbase + rec_i * cbytes);
             if (BITS == 4) {
                 rec[j] = code;
             } else {
@@ -530,9 +576,15 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_half(QuantArgs a) {
                 const int r = j & 3, m4 = j >> 2;
                 if (r < 3) rec[3 * m4 + r] = (code >> (8 * r)) | (nxt << (24 - 8 * r));
             }
+            if (a.tiled) {   // both records through shared memory, then the whole warp scatters each
+                __syncwarp();
+                store_tiled(a, 0, rec_i, recbuf[threadIdx.x >> 5][0], BITS, lane);
+                store_tiled(a, 1, rec_i, recbuf[threadIdx.x >> 5][1], BITS, lane);
+                __syncwarp();
+            }
             const float nv = ROT == TQ_ROT_WHT32 ? __shfl_sync(TQ_FULL_MASK, n, 16 * hv + 4 * (j & 3)) : n;
             if (j < slots) {
-                const size_t ni = rec_i * slots + j;
+                const size_t ni = norm_index(a, hv, rec_i, slots, j);
                 if (a.norm_f16) static_cast<__half*>(nbase)[ni] = __float2half_rn(nv);
                 else static_cast<float*>(nbase)[ni] = nv;
             }
@@ -798,23 +850,36 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
                 *reinterpret_cast<uint16_t*>(r + 1) = (uint16_t)(w >> 8);
             }
         }
-        const size_t rec_i = (((size_t)b * Hkv + h) * Tcap) + (slot < 0 ? 0 : slot);
+        const size_t rec_i = (((size_t)b * Hkv + h) * a.t_alloc) + (slot < 0 ? 0 : slot);
         __syncwarp();
+        if (a.tiled) {   // each record scattered into its tile by the whole warp
+#pragma unroll 1
+            for (int rr = 0; rr < 8; ++rr) {
+                const int slot_r = __shfl_sync(TQ_FULL_MASK, slot, 4 * rr);
+                const unsigned long long ri = __shfl_sync(TQ_FULL_MASK, (unsigned long long)rec_i, 4 * rr);
+                if (slot_r >= 0) {
+                    store_tiled(a, 0, ri, reinterpret_cast<const uint32_t*>(stage[2 * rr]), 3, lane);
+                    store_tiled(a, 1, ri, reinterpret_cast<const uint32_t*>(stage[2 * rr + 1]), 3, lane);
+                }
+            }
+        } else {
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {   // 48 chunks of 16 bytes: record q / 3, part q % 3
-            const int q = lane + 32 * k;
-            const int rr = (q < 48 ? q : 47) / 3, part = q - 3 * (q / 3);
-            const int src = 4 * (rr >> 1);
-            const int slot_r = __shfl_sync(TQ_FULL_MASK, slot, src);
-            const unsigned long long ri = __shfl_sync(TQ_FULL_MASK, (unsigned long long)rec_i, src);
-            if (q < 48 && slot_r >= 0) {
-                const uint4 v = *reinterpret_cast<const uint4*>(&stage[rr][16 * part]);
-                *reinterpret_cast<uint4*>(((rr & 1) ? a.codes[1] : a.codes[0]) + ri * 48 + 16 * part) = v;
+            for (int k = 0; k < 2; ++k) {   // 48 chunks of 16 bytes: record q / 3, part q % 3
+                const int q = lane + 32 * k;
+                const int rr = (q < 48 ? q : 47) / 3, part = q - 3 * (q / 3);
+                const int src = 4 * (rr >> 1);
+                const int slot_r = __shfl_sync(TQ_FULL_MASK, slot, src);
+                const unsigned long long ri = __shfl_sync(TQ_FULL_MASK, (unsigned long long)rec_i, src);
+                if (q < 48 && slot_r >= 0) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(&stage[rr][16 * part]);
+                    *reinterpret_cast<uint4*>(((rr & 1) ? a.codes[1] : a.codes[0]) + ri * 48 + 16 * part) = v;
+                }
             }
         }
         __syncwarp();
         if (slot >= 0 && c < 2)
-            static_cast<__half*>(c ? a.norms[1] : a.norms[0])[rec_i] = __float2half_rn(c ? vn : kn);
+            static_cast<__half*>(c ? a.norms[1] : a.norms[0])[norm_index(a, c, rec_i, 1, 0)] =
+                __float2half_rn(c ? vn : kn);
 
         if (!more) break;
         p = pn;
@@ -912,6 +977,8 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     a.n_new = n_new;
     a.Hkv = d->n_kv_heads;
     a.Tcap = d->t_capacity;
+    a.t_alloc = d->t_alloc;
+    a.tiled = d->layout == TQ_LAYOUT_TILE16;
     a.in_dtype = in_dtype;
     a.norm_f16 = d->norm_dtype == TQ_F16;
     a.rot = d->rot;

@@ -91,6 +91,166 @@ def oracle_encode(st: Setup, which: str, b: int, h: int, t0: int = 0, t1=None) -
     return OracleEnc(O.pack(idx, spec), idx, nrm, y)
 
 
+# ---------------------------------------------------------------- cache layouts
+# The two layouts of include/tq.h restated in numpy from that header's text (no
+# code of the library is used): TQ_LAYOUT_NATURAL keeps one record per position;
+# TQ_LAYOUT_TILE16 permutes the bits of every 16-token tile as documented there.
+
+_BIT_MAPS = {}
+
+
+def tile_bit_map(which: str, bits: int) -> np.ndarray:
+    """[16 tokens][64 fields][field bits] -> bit index within a code tile."""
+    key = (which, bits)
+    if key in _BIT_MAPS:
+        return _BIT_MAPS[key]
+    W = 3 if bits == 3 else 4
+    fb = 6 if bits == 3 else 8
+    X, Y = np.arange(6), np.array([0, 1, 4, 5, 6, 7])
+
+    def word_byte(L, i):
+        return 16 * L + 4 * i if i < 4 else 512 + 8 * (W - 2) * L + 4 * (i - 4)
+
+    M = np.full((16, 64, fb), -1, dtype=np.int64)
+    for t in range(16):
+        if which == "k":
+            r, first = t % 8, W * (t // 8)
+            for c in range(4):
+                L = 4 * r + c
+                for s in range(16):
+                    i = 8 * (s >> 1) + c + 4 * (s & 1)
+                    if bits == 4 or s < 12:
+                        base = 8 * (word_byte(L, first + (s >> 2)) + (s & 3))
+                        M[t, i] = base + (np.arange(8) if bits == 4 else (Y if (s >> 2) == 1 else X))
+                    else:
+                        g = s - 12
+                        b0, b1, b2 = (8 * (word_byte(L, first + w) + g) for w in range(3))
+                        M[t, i] = [b0 + 6, b0 + 7, b1 + 2, b1 + 3, b2 + 6, b2 + 7]
+        else:
+            c, first, hh = (t % 8) // 2, W * (t // 8), t % 2
+            for r in range(8):
+                L = 4 * r + c
+                for q in range(8):
+                    i = 16 * (q >> 1) + r + 8 * (q & 1)
+                    if bits == 4 or q < 6:
+                        base = 8 * (word_byte(L, first + (q >> 1)) + 2 * hh + (q & 1))
+                        M[t, i] = base + (np.arange(8) if bits == 4 else (Y if (q >> 1) == 1 else X))
+                    else:
+                        g = q - 6
+                        b0, b1, b2 = (8 * (word_byte(L, first + w) + 2 * hh + g) for w in range(3))
+                        M[t, i] = [b0 + 6, b0 + 7, b1 + 2, b1 + 3, b2 + 6, b2 + 7]
+    _BIT_MAPS[key] = M
+    return M
+
+
+def norm_positions(which: str, slots: int) -> np.ndarray:
+    """[16 tokens][slots] -> element index within a tile's norms."""
+    P = np.zeros((16, slots), dtype=np.int64)
+    for t in range(16):
+        for b in range(slots):
+            if slots == 1:
+                P[t, b] = 2 * (t & 7) + (t >> 3)
+            elif which == "k":
+                P[t, b] = (2 * (t & 7) + (t >> 3)) * 4 + b
+            else:
+                P[t, b] = ((((t & 7) >> 1) * 2 + (t >> 3)) * 4 + b) * 2 + (t & 1)
+    return P
+
+
+class CacheLayout:
+    """Conversions between one (batch, KV head) row of a device array, as stored,
+    and per-position records / norms."""
+
+    def __init__(self, desc):
+        self.tiled = int(desc.layout) == 1
+        self.t_alloc = int(desc.t_alloc)
+        self.nb = {"k": int(desc.k_code_bytes), "v": int(desc.v_code_bytes)}
+        self.slots = {"k": int(desc.k_norm_slots), "v": int(desc.v_norm_slots)}
+
+    def records(self, raw: np.ndarray, which: str) -> np.ndarray:
+        nb = self.nb[which]
+        if not self.tiled:
+            return raw.reshape(self.t_alloc, nb)
+        bits = 3 if nb == 48 else 4
+        M = tile_bit_map(which, bits)
+        fb = M.shape[2]
+        tb = np.unpackbits(raw.reshape(-1, 16 * nb), axis=1, bitorder="little")   # [tiles][tile bits]
+        nat = np.zeros((tb.shape[0], 16, nb * 8), dtype=np.uint8)
+        cols = (np.arange(64)[:, None] * fb + np.arange(fb)[None, :])              # record bit of (field, bit)
+        for t in range(16):
+            nat[:, t, cols.ravel()] = tb[:, M[t].ravel()]
+        return np.packbits(nat, axis=2, bitorder="little").reshape(self.t_alloc, nb)
+
+    def raw(self, records: np.ndarray, which: str) -> np.ndarray:
+        nb = self.nb[which]
+        if not self.tiled:
+            return np.ascontiguousarray(records, dtype=np.uint8).reshape(-1)
+        bits = 3 if nb == 48 else 4
+        M = tile_bit_map(which, bits)
+        fb = M.shape[2]
+        nat = np.unpackbits(records.reshape(-1, 16, nb), axis=2, bitorder="little")   # [tiles][16][bits]
+        tb = np.zeros((nat.shape[0], 16 * nb * 8), dtype=np.uint8)
+        cols = (np.arange(64)[:, None] * fb + np.arange(fb)[None, :])
+        for t in range(16):
+            tb[:, M[t].ravel()] = nat[:, t, cols.ravel()]
+        return np.packbits(tb, axis=1, bitorder="little").reshape(-1)
+
+    def norms(self, raw: np.ndarray, which: str) -> np.ndarray:
+        sl = self.slots[which]
+        if not self.tiled:
+            return raw.reshape(self.t_alloc, sl)
+        P = norm_positions(which, sl)
+        tiles = raw.reshape(-1, 16 * sl)
+        return tiles[:, P].reshape(self.t_alloc, sl)
+
+    def raw_norms(self, norms: np.ndarray, which: str) -> np.ndarray:
+        sl = self.slots[which]
+        if not self.tiled:
+            return np.ascontiguousarray(norms).reshape(-1)
+        P = norm_positions(which, sl)
+        out = np.zeros((self.t_alloc // 16, 16 * sl), dtype=norms.dtype)
+        out[:, P] = norms.reshape(-1, 16, sl)
+        return out.reshape(-1)
+
+
+def cache_records(cache, which: str) -> np.ndarray:
+    """[batch][n_kv][t_alloc][code_bytes] records of a device cache."""
+    lay = CacheLayout(cache.desc)
+    raw = cache.codes_view(which).cpu().numpy()
+    return np.stack([np.stack([lay.records(raw[b, h], which) for h in range(raw.shape[1])])
+                     for b in range(raw.shape[0])])
+
+
+def cache_norms(cache, which: str) -> np.ndarray:
+    """[batch][n_kv][t_alloc][slots] norms of a device cache."""
+    lay = CacheLayout(cache.desc)
+    raw = cache.norms_view(which).cpu().numpy()
+    return np.stack([np.stack([lay.norms(raw[b, h], which) for h in range(raw.shape[1])])
+                     for b in range(raw.shape[0])])
+
+
+def pair_records(cache, which: str, b: int, h: int) -> np.ndarray:
+    lay = CacheLayout(cache.desc)
+    return lay.records(cache.codes_view(which)[b, h].cpu().numpy(), which)
+
+
+def pair_norms(cache, which: str, b: int, h: int) -> np.ndarray:
+    lay = CacheLayout(cache.desc)
+    return lay.norms(cache.norms_view(which)[b, h].cpu().numpy(), which)
+
+
+def put_pair(torch, cache, which: str, b: int, h: int, records: np.ndarray, norms: np.ndarray, t0: int = 0):
+    """Write records / norms of positions t0 .. t0 + len - 1 of one pair into the
+    device cache (the rest of the pair's row is kept)."""
+    lay = CacheLayout(cache.desc)
+    rec = pair_records(cache, which, b, h)
+    nrm = pair_norms(cache, which, b, h)
+    rec[t0:t0 + records.shape[0]] = records
+    nrm[t0:t0 + norms.shape[0]] = norms.reshape(norms.shape[0], -1)
+    cache.codes_view(which)[b, h] = torch.from_numpy(lay.raw(rec, which))
+    cache.norms_view(which)[b, h] = torch.from_numpy(lay.raw_norms(nrm, which))
+
+
 def to_torch_input(torch, x: np.ndarray, dtype: int, device="cuda"):
     if dtype == W.BF16:
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)

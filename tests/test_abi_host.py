@@ -143,21 +143,32 @@ def test_params_blob_contents(tqlib):
 def test_decode_plan_host_only(tqlib):
     tq = tqlib
     d = tq.tq_cache_desc_init(128, 32, 8, 32, 8192, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
+    assert d.layout == tq.TQ_LAYOUT_TILE16 and d.t_alloc == 8192
     sp, vm = tq.tq_decode_plan(d, 8192)
-    # tensor-core path; 4 splits x 256 (batch, KV head) pairs = 1024 CTAs, 6.7 per SM,
-    # 32 tiles per warp: the cheapest ceil(CTAs / 152) x (tiles per warp + 2) + merge
-    assert (sp, vm) == (4, tq.TQ_VMODE_TENSOR)
-    sp, vm = tq.tq_decode_plan(d, 8192, tq.TQ_VMODE_DIM_PARALLEL)
-    assert 1 <= sp <= tq.TQ_MAX_SPLITS and vm == tq.TQ_VMODE_DIM_PARALLEL
-    d2 = tq.tq_cache_desc_init(128, 32, 8, 32, 8190, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
-    assert tq.tq_decode_plan(d2, 8190)[1] == tq.TQ_VMODE_DIM_PARALLEL   # fp16 norm rows not 16-byte aligned
-    with pytest.raises(tq.TQError) as e:
-        tq.tq_decode_plan(d2, 8190, tq.TQ_VMODE_TENSOR)
+    # tensor-core path: 131072 tiles over one wave of persistent CTAs (2 per SM)
+    assert (sp, vm) == (304, tq.TQ_VMODE_TENSOR)
+    with pytest.raises(tq.TQError) as e:   # no CUDA-core kernel reads the tile layout
+        tq.tq_decode_plan(d, 8192, tq.TQ_VMODE_DIM_PARALLEL)
     assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+    # any capacity: the tile layout pads it to whole tiles
+    d2 = tq.tq_cache_desc_init(128, 32, 8, 32, 8190, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
+    assert d2.layout == tq.TQ_LAYOUT_TILE16 and d2.t_alloc == 8192
+    assert tq.tq_cache_bytes(d2, tq.TQ_PART_K_CODES) == 32 * 8 * 8192 * 48
+    assert tq.tq_cache_bytes(d2, tq.TQ_PART_V_NORMS) == 32 * 8 * 8192 * 2
+    assert tq.tq_decode_plan(d2, 8190) == (304, tq.TQ_VMODE_TENSOR)
     sp, vm = tq.tq_decode_plan(d, 100)
-    assert vm == tq.TQ_VMODE_TENSOR and sp <= 2                         # the tensor path at every length
-    sp, vm = tq.tq_decode_plan(d2, 100)
-    assert vm == tq.TQ_VMODE_TOKEN_PARALLEL and sp <= 2                 # without it, token-parallel when short
+    assert vm == tq.TQ_VMODE_TENSOR and sp == 56                        # 1792 tiles, 32 per CTA
+    assert tq.tq_decode_plan(d, 100, tq.TQ_VMODE_TENSOR, 7) == (7, tq.TQ_VMODE_TENSOR)
+    # natural layout (16 query heads per KV head): token-parallel when short
+    d3 = tq.tq_cache_desc_init(128, 32, 2, 32, 8190, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
+    assert d3.layout == tq.TQ_LAYOUT_NATURAL and d3.t_alloc == 8190
+    sp, vm = tq.tq_decode_plan(d3, 100)
+    assert vm == tq.TQ_VMODE_TOKEN_PARALLEL and sp <= 2
+    sp, vm = tq.tq_decode_plan(d3, 8190)
+    assert vm == tq.TQ_VMODE_DIM_PARALLEL and 1 <= sp <= tq.TQ_MAX_SPLITS
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_decode_plan(d3, 8190, tq.TQ_VMODE_TENSOR)
+    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
     with pytest.raises(tq.TQError):
         tq.tq_decode_plan(d, 0)
     with pytest.raises(tq.TQError):

@@ -13,8 +13,9 @@ import pytest
 
 import workloads as W
 from oracle import tq_oracle as O
-from gpu_harness import (ATT_TOL, MAX_MISMATCH_FRAC, att_error, compare_codes, compare_norms, make_setup,
-                         oracle_attention, oracle_encode, to_torch_input)
+from gpu_harness import (ATT_TOL, MAX_MISMATCH_FRAC, att_error, cache_norms, cache_records, compare_codes,
+                         compare_norms, make_setup, oracle_attention, oracle_encode, pair_records, put_pair,
+                         to_torch_input)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +40,10 @@ def _workload(name):
         "block32_tq4": W.block32(4),
         "so4": W.so4_wht(),
         "mixed": W.mixed_rate_long(),
+        # natural-layout variants of the same formats (CUDA-core decode kernels):
+        # 16 query heads per KV head, and fp32 norms with 32-wide blocks
+        "llama8b_g16": W.llama8b_decode().with_(n_kv_heads=2),
+        "block32_f32": W.block32(3).with_(norm_dtype=W.F32),
     }[name]
 
 
@@ -49,7 +54,11 @@ SMALL = {  # (batch, T) element-wise cases: several tiles and a ragged tail
     "block32_tq4": (2, 333),
     "so4": (1, 333),
     "mixed": (1, 700),
+    "llama8b_g16": (2, 333),
+    "block32_f32": (2, 333),
 }
+TILED = ["tiny", "llama8b", "block32_tq3", "block32_tq4", "so4"]   # TQ_LAYOUT_TILE16 caches
+NATURAL = ["mixed", "llama8b_g16", "block32_f32"]                  # TQ_LAYOUT_NATURAL caches
 
 
 def _encode_on_gpu(tq, name, B, T, cap_extra=5, seq_lens=None):
@@ -70,10 +79,9 @@ def test_quantize_append_matches_oracle(tq, name):
     B, T = SMALL[name]
     st, cache = _encode_on_gpu(tq, name, B, T)
     assert int(cache.status.item()) == 0
-    kc = cache.codes_view("k").cpu().numpy()
-    vc = cache.codes_view("v").cpu().numpy()
-    kn = cache.norms_view("k").cpu().numpy()
-    vn = cache.norms_view("v").cpu().numpy()
+    assert st.desc.layout == (tq.TQ_LAYOUT_TILE16 if name in TILED else tq.TQ_LAYOUT_NATURAL)
+    kc, vc = cache_records(cache, "k"), cache_records(cache, "v")
+    kn, vn = cache_norms(cache, "k"), cache_norms(cache, "v")
     tot = bad = 0
     for b in range(B):
         for h in range(st.wl.n_kv_heads):
@@ -91,10 +99,8 @@ def test_quantize_append_matches_oracle(tq, name):
 
 
 def _check_codes_vs_oracle(st, cache, B, T):
-    kc = cache.codes_view("k").cpu().numpy()
-    vc = cache.codes_view("v").cpu().numpy()
-    kn = cache.norms_view("k").cpu().numpy()
-    vn = cache.norms_view("v").cpu().numpy()
+    kc, vc = cache_records(cache, "k"), cache_records(cache, "v")
+    kn, vn = cache_norms(cache, "k"), cache_norms(cache, "v")
     tot = bad = 0
     for b in range(B):
         for h in range(st.wl.n_kv_heads):
@@ -175,8 +181,8 @@ def test_quantize_tc_heads_and_tails(tq, in_dtype, B, T, pairs):
     c.append(K, V, torch.full((B,), 2, dtype=torch.int32, device="cuda"))   # slots 2 .. T+1
     torch.cuda.synchronize()
     assert int(c.status.item()) == 0
-    kc, vc = c.codes_view("k").cpu().numpy(), c.codes_view("v").cpu().numpy()
-    kn, vn = c.norms_view("k").cpu().numpy(), c.norms_view("v").cpu().numpy()
+    kc, vc = cache_records(c, "k"), cache_records(c, "v")
+    kn, vn = cache_norms(c, "k"), cache_norms(c, "v")
     bad = tot = 0
     for (b, h) in pairs or [(b, h) for b in range(B) for h in range(3)]:
         for which, codes, norms in (("k", kc, kn), ("v", vc, vn)):
@@ -223,18 +229,15 @@ def test_quantize_tc_search_without_shared_table(tq):
 
 
 def _upload_oracle_cache(tq, st, cache, B, T):
-    """Write the oracle's records into the device cache; returns the encodings."""
+    """Write the oracle's records into the device cache (in the cache's layout,
+    converted by the harness); returns the encodings."""
     encs = {}
-    kcv, vcv = cache.codes_view("k"), cache.codes_view("v")
-    knv, vnv = cache.norms_view("k"), cache.norms_view("v")
     for b in range(B):
         for h in range(st.wl.n_kv_heads):
             ek = oracle_encode(st, "k", b, h, 0, T)
             ev = oracle_encode(st, "v", b, h, 0, T)
-            kcv[b, h, :T] = torch.from_numpy(ek.codes)
-            vcv[b, h, :T] = torch.from_numpy(ev.codes)
-            knv[b, h, :T] = torch.from_numpy(ek.norms)
-            vnv[b, h, :T] = torch.from_numpy(ev.norms)
+            put_pair(torch, cache, "k", b, h, ek.codes, ek.norms)
+            put_pair(torch, cache, "v", b, h, ev.codes, ev.norms)
             encs[(b, h)] = (ek, ev)
     torch.cuda.synchronize()
     return encs
@@ -259,10 +262,27 @@ def _check_decode(tq, st, cache, encs, q, seq_lens, max_seq, v_mode, n_splits, p
     return err, scale
 
 
-@pytest.mark.parametrize("v_mode", [0, 1])
 @pytest.mark.parametrize("n_splits", [1, 3, 0])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_decode_matches_oracle(tq, name, v_mode, n_splits):
+def test_decode_matches_oracle(tq, name, n_splits):
+    """The automatic kernel of every format (tensor cores on the tile layout, the
+    crossover's CUDA-core kernel on the natural layout) with 1, 3 and the
+    automatic number of splits (tensor cores: CTAs over all tiles)."""
+    B, T = SMALL[name]
+    seq_lens = W.ragged_lengths(B, T, 3) if B > 1 else None
+    st, cache = _encode_on_gpu(tq, name, B, T, seq_lens=seq_lens)
+    encs = _upload_oracle_cache(tq, st, cache, B, T)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    sl = torch.from_numpy(st.inp.seq_lens).cuda()
+    _check_decode(tq, st, cache, encs, q, sl, T, -1, n_splits)
+    assert int(cache.status.item()) == 0
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+@pytest.mark.parametrize("n_splits", [1, 3, 0])
+@pytest.mark.parametrize("name", NATURAL)
+def test_decode_cuda_core_modes(tq, name, v_mode, n_splits):
+    """Token- and dimension-parallel V accumulation on natural-layout caches."""
     B, T = SMALL[name]
     seq_lens = W.ragged_lengths(B, T, 3) if B > 1 else None
     st, cache = _encode_on_gpu(tq, name, B, T, seq_lens=seq_lens)
@@ -274,69 +294,78 @@ def test_decode_matches_oracle(tq, name, v_mode, n_splits):
 
 
 @pytest.mark.parametrize("T", [1, 2, 31, 127, 128, 129, 511, 512])
-def test_decode_short_and_tile_edges(tq, T):
-    st, cache = _encode_on_gpu(tq, "so4", 1, T)
+@pytest.mark.parametrize("name", ["so4", "llama8b_g16"])
+def test_decode_short_and_tile_edges(tq, name, T):
+    st, cache = _encode_on_gpu(tq, name, 1, T)
     encs = _upload_oracle_cache(tq, st, cache, 1, T)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
     sl = torch.full((1,), T, dtype=torch.int32, device="cuda")
-    for v_mode in (0, 1, -1):
+    modes = (-1, 2, 3) if name in TILED else (0, 1, -1)
+    for v_mode in modes:
         _check_decode(tq, st, cache, encs, q, sl, T, v_mode, 0)
 
 
-def test_v_mode_switch_at_crossover(tq):
-    st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=600)          # capacity 608: tensor path available
-    assert tq.tq_decode_plan(st.desc, 8)[1] == tq.TQ_VMODE_TENSOR     # at every length
-    assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TENSOR
-    assert tq.tq_decode_plan(st.desc, 512)[1] == tq.TQ_VMODE_TENSOR
-    st, _ = _encode_on_gpu(tq, "so4", 1, 8, cap_extra=601)          # unaligned capacity: CUDA-core path
-    assert tq.tq_decode_plan(st.desc, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
-    assert tq.tq_decode_plan(st.desc, 512)[1] == tq.TQ_VMODE_DIM_PARALLEL
-    st, _ = _encode_on_gpu(tq, "block32_tq3", 1, 8, cap_extra=600)  # no tensor kernel for this format
-    with pytest.raises(tq.TQError) as e:
-        tq.tq_decode_plan(st.desc, 512, tq.TQ_VMODE_TENSOR)
-    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+def test_v_mode_plan(tq):
+    """Tile-layout caches take the tensor-core kernel at every length (and no
+    CUDA-core kernel); natural-layout caches switch from token- to
+    dimension-parallel V accumulation at the crossover length."""
+    for name in ("so4", "block32_tq3", "block32_tq4", "tiny"):
+        st, _ = _encode_on_gpu(tq, name, 1, 8, cap_extra=601)     # any capacity (tiles are padded)
+        for T in (8, 511, 512, 600):
+            assert tq.tq_decode_plan(st.desc, T)[1] == tq.TQ_VMODE_TENSOR
+        for vm in (tq.TQ_VMODE_TOKEN_PARALLEL, tq.TQ_VMODE_DIM_PARALLEL):
+            with pytest.raises(tq.TQError) as e:
+                tq.tq_decode_plan(st.desc, 512, vm)
+            assert e.value.status == tq.TQ_ERR_UNSUPPORTED
+    for name in ("llama8b_g16", "block32_f32"):
+        st, _ = _encode_on_gpu(tq, name, 1, 8, cap_extra=600)
+        X = 512   # the crossover length (TQ_V_CROSSOVER unset)
+        assert tq.tq_decode_plan(st.desc, X - 1)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
+        assert tq.tq_decode_plan(st.desc, X)[1] == tq.TQ_VMODE_DIM_PARALLEL
+        with pytest.raises(tq.TQError) as e:
+            tq.tq_decode_plan(st.desc, 512, tq.TQ_VMODE_TENSOR)
+        assert e.value.status == tq.TQ_ERR_UNSUPPORTED
 
 
-TC_NAMES = ["tiny", "llama8b", "so4"]
-
-
-def _aligned_cap(T):
-    return (T + 5 + 7) // 8 * 8 - T
-
-
-@pytest.mark.parametrize("n_splits", [1, 3, 0])
-@pytest.mark.parametrize("name", TC_NAMES)
-def test_decode_tensor_matches_oracle(tq, name, n_splits):
+@pytest.mark.parametrize("grid", [1, 3, 0])
+@pytest.mark.parametrize("name", TILED)
+def test_decode_tensor_matches_oracle(tq, name, grid):
+    """Tensor-core kernel with 1, 3 and the automatic number of CTAs; ragged
+    lengths and a capacity that is not a whole number of tiles."""
     B, T = SMALL[name]
     seq_lens = W.ragged_lengths(B, T, 4) if B > 1 else None
-    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=_aligned_cap(T), seq_lens=seq_lens)
+    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=3, seq_lens=seq_lens)
+    assert st.desc.t_alloc % 16 == 0 and st.desc.t_alloc >= st.desc.t_capacity
     encs = _upload_oracle_cache(tq, st, cache, B, T)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
     sl = torch.from_numpy(st.inp.seq_lens).cuda()
-    _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, n_splits)
+    _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, grid)
     assert int(cache.status.item()) == 0
 
 
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 64, 100, 512, 1000])
-@pytest.mark.parametrize("name", ["llama8b", "so4"])
+@pytest.mark.parametrize("name", ["llama8b", "so4", "block32_tq3", "block32_tq4"])
 def test_decode_tensor_tile_edges(tq, name, T):
-    st, cache = _encode_on_gpu(tq, name, 1, T, cap_extra=_aligned_cap(T))
+    st, cache = _encode_on_gpu(tq, name, 1, T, cap_extra=1)
     encs = _upload_oracle_cache(tq, st, cache, 1, T)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
     sl = torch.full((1,), T, dtype=torch.int32, device="cuda")
-    for n_splits in (0, 1, 2):
-        _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, n_splits)
+    for grid in (0, 1, 2):
+        _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR, grid)
 
 
 @pytest.mark.parametrize("n_splits", [77, 300])
-@pytest.mark.parametrize("name,v_mode", [("so4", 2), ("block32_tq4", 1), ("llama8b", 0)])
+@pytest.mark.parametrize("name,v_mode", [("so4", 2), ("block32_tq4", 2), ("llama8b", 2), ("block32_f32", 1),
+                                         ("llama8b_g16", 0)])
 def test_decode_many_splits(tq, name, v_mode, n_splits):
-    """Key-axis splits well beyond a warp's width (the merge walks the partials
-    32 at a time for the weights, 8 at a time for the outputs), many of them
-    empty (sections of a few tokens, rounded to whole tiles), ragged lengths."""
+    """Many partials per pair: CUDA-core kernels with key-axis splits well beyond
+    a warp's width (the merge walks the partials 32 at a time for the weights, 8
+    at a time for the outputs), many of them empty; the tensor-core kernel with
+    77 or 300 CTAs over few tiles (most CTAs hold a piece of one tile or none).
+    Ragged lengths."""
     B, T = 2, 1000
     seq_lens = W.ragged_lengths(B, T, 7)
-    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=_aligned_cap(T), seq_lens=seq_lens)
+    st, cache = _encode_on_gpu(tq, name, B, T, seq_lens=seq_lens)
     encs = _upload_oracle_cache(tq, st, cache, B, T)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
     sl = torch.from_numpy(st.inp.seq_lens).cuda()
@@ -344,24 +373,24 @@ def test_decode_many_splits(tq, name, v_mode, n_splits):
     assert int(cache.status.item()) == 0
 
 
-@pytest.mark.parametrize("name", TC_NAMES)
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "so4", "block32_tq3"])
 def test_decode_streamk_matches_oracle(tq, name):
-    """Stream-K partition: every tile of every pair spread over one wave of
-    CTAs; ragged lengths put pair boundaries anywhere inside a CTA's range."""
+    """Ragged lengths put pair boundaries anywhere inside a CTA's range."""
     B, T = SMALL[name]
     B = max(B, 5)
     seq_lens = W.ragged_lengths(B, T, 6)
-    st, cache = _encode_on_gpu(tq, name, B, T, cap_extra=_aligned_cap(T), seq_lens=seq_lens)
+    st, cache = _encode_on_gpu(tq, name, B, T, seq_lens=seq_lens)
     encs = _upload_oracle_cache(tq, st, cache, B, T)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
     sl = torch.from_numpy(st.inp.seq_lens).cuda()
-    _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR_STREAMK, 0)
+    for grid in (0, 7, 40):
+        _check_decode(tq, st, cache, encs, q, sl, T, tq.TQ_VMODE_TENSOR_STREAMK, grid)
     assert int(cache.status.item()) == 0
 
 
 def test_decode_streamk_empty_and_clamped(tq):
     B, T = 4, 200
-    st, cache = _encode_on_gpu(tq, "llama8b", B, T, cap_extra=_aligned_cap(T))
+    st, cache = _encode_on_gpu(tq, "llama8b", B, T)
     encs = _upload_oracle_cache(tq, st, cache, B, T)
     q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
     sl = torch.tensor([0, T + 50, 0, 77], dtype=torch.int32, device="cuda")
@@ -409,6 +438,8 @@ def test_append_positions_and_incremental(tq):
     st, cache = _encode_on_gpu(tq, "llama8b", B, T)
     whole_k = cache.codes_view("k").clone()
     whole_kn = cache.norms_view("k").clone()
+    whole_v = cache.codes_view("v").clone()
+    whole_vn = cache.norms_view("v").clone()
     cache2 = tq.PackedKVCache(st.desc, st.blob)
     K = to_torch_input(torch, st.inp.K, st.wl.in_dtype)
     V = to_torch_input(torch, st.inp.V, st.wl.in_dtype)
@@ -419,17 +450,20 @@ def test_append_positions_and_incremental(tq):
     torch.cuda.synchronize()
     assert torch.equal(cache2.codes_view("k"), whole_k)
     assert torch.equal(cache2.norms_view("k"), whole_kn)
+    assert torch.equal(cache2.codes_view("v"), whole_v)   # value halves of one token never touch another's
+    assert torch.equal(cache2.norms_view("v"), whole_vn)
     assert int(cache2.status.item()) == 0
     # out-of-range start position: skipped and flagged; n_new = 0 is a no-op
-    before = cache2.codes_view("v").clone()
+    before = cache_records(cache2, "v")
     cache2.append(K[:, :3].contiguous(), V[:, :3].contiguous(),
                   torch.tensor([st.desc.t_capacity - 1, -5], dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert int(cache2.status.item()) & tq.TQ_DEV_BAD_POSITION
-    after = cache2.codes_view("v")
+    after = cache_records(cache2, "v")
     cap = st.desc.t_capacity
-    assert torch.equal(after[1], before[1])             # batch 1 entirely skipped
-    assert torch.equal(after[0, :, :cap - 1], before[0, :, :cap - 1])
+    assert np.array_equal(after[1], before[1])             # batch 1 entirely skipped
+    assert np.array_equal(after[0, :, :cap - 1], before[0, :, :cap - 1])
+    assert np.array_equal(after[0, :, cap:], before[0, :, cap:])   # tile padding untouched
     tq.tq_quantize_append(st.desc, cache2.ptrs, K[:, :0].contiguous(), V[:, :0].contiguous(),
                           torch.zeros(B, dtype=torch.int32, device="cuda"), 0)
 
@@ -450,8 +484,8 @@ def test_quantize_tc_positions_outside_capacity(tq):
     torch.cuda.synchronize()
     assert int(c.status.item()) & tq.TQ_DEV_BAD_POSITION
     for which in ("k", "v"):
-        codes = c.codes_view(which).cpu().numpy()
-        norms = c.norms_view(which).cpu().numpy()
+        codes = cache_records(c, which)
+        norms = cache_norms(c, which)
         assert not codes[0, :, :start].any() and not norms[0, :, :start].any()
         assert not codes[1, :, T - 5:].any() and not norms[1, :, T - 5:].any()
         for h in range(wl.n_kv_heads):
@@ -472,9 +506,12 @@ def test_argument_errors(tq):
         tq.tq_decode_attention(st.desc, cache.ptrs, q, sl, 10 ** 6, out, cache.workspace)
     assert e.value.status == tq.TQ_ERR_INVALID_ARG
     small_ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    with pytest.raises(tq.TQError) as e:          # workspace too small for 4 splits
-        tq.tq_decode_attention_ex(st.desc, cache.ptrs, q, sl, 8, out, small_ws, None, None, 1, 4)
+    with pytest.raises(tq.TQError) as e:          # workspace too small for 4 CTAs
+        tq.tq_decode_attention_ex(st.desc, cache.ptrs, q, sl, 8, out, small_ws, None, None, 2, 4)
     assert e.value.status == tq.TQ_ERR_WORKSPACE
+    with pytest.raises(tq.TQError) as e:          # a CUDA-core kernel on a tile-layout cache
+        tq.tq_decode_attention_ex(st.desc, cache.ptrs, q, sl, 8, out, cache.workspace, None, None, 1, 1)
+    assert e.value.status == tq.TQ_ERR_UNSUPPORTED
     big = torch.empty(128 + 4, dtype=torch.float32, device="cuda")
     with pytest.raises(tq.TQError) as e:          # output not 16-byte aligned
         tq.tq_decode_attention(st.desc, cache.ptrs, q, sl, 8, big[1:129].view(1, 1, 128), cache.workspace)
@@ -485,9 +522,13 @@ def test_argument_errors(tq):
 # full sizes, in the launch configuration the benchmark times (automatic plan)
 FULL = {
     "llama8b": (W.llama8b_decode(), [(0, 0), (13, 5), (31, 7)]),
+    "block32_tq3": (W.block32(3), [(0, 0), (5, 3), (7, 7)]),
     "block32_tq4": (W.block32(4), [(0, 0), (7, 7)]),
+    "so4_2k": (W.so4_wht(seq_len=2048), [(0, 0), (0, 3)]),
+    "so4_8k": (W.so4_wht(seq_len=8192), [(0, 1), (0, 2)]),
     "so4_32k": (W.so4_wht(seq_len=32768), [(0, 0), (0, 3)]),
     "mixed_131k": (W.mixed_rate_long(131072), [(0, 0), (0, 1)]),
+    "mixed_524k": (W.mixed_rate_long(524288), [(0, 1)]),
 }
 
 
@@ -504,26 +545,23 @@ def test_full_size_sampled(tq, name):
     torch.cuda.synchronize()
     del K, V
     # write side on the sampled pairs
-    kc, vc = cache.codes_view("k"), cache.codes_view("v")
     encs = {}
     bad = tot = 0
     for (b, h) in pairs:
         ek = oracle_encode(st, "k", b, h)
         ev = oracle_encode(st, "v", b, h)
-        for enc, codes, which in ((ek, kc, 0), (ev, vc, 1)):
-            nb, n, _, _, ok = compare_codes(codes[b, h].cpu().numpy(), enc, st.specs[h][which])
+        for enc, which in ((ek, "k"), (ev, "v")):
+            rec = pair_records(cache, which, b, h)[:T]
+            nb, n, _, _, ok = compare_codes(rec, enc, st.specs[h][0 if which == "k" else 1])
             assert ok
             bad += nb
             tot += n
         encs[(b, h)] = (ek, ev)
     assert bad / tot <= MAX_MISMATCH_FRAC
     # read side: the sampled pairs carry the oracle's records
-    knv, vnv = cache.norms_view("k"), cache.norms_view("v")
     for (b, h), (ek, ev) in encs.items():
-        kc[b, h] = torch.from_numpy(ek.codes)
-        vc[b, h] = torch.from_numpy(ev.codes)
-        knv[b, h] = torch.from_numpy(ek.norms)
-        vnv[b, h] = torch.from_numpy(ev.norms)
+        put_pair(torch, cache, "k", b, h, ek.codes, ek.norms)
+        put_pair(torch, cache, "v", b, h, ev.codes, ev.norms)
     q = to_torch_input(torch, inp.q, wl.in_dtype)
     sl = torch.from_numpy(inp.seq_lens).cuda()
     _check_decode(tq, st, cache, encs, q, sl, T, -1, 0, pairs=pairs)

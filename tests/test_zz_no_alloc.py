@@ -5,13 +5,15 @@ an allocation would synchronise the device).  Its split-K scratch is a fixed
 array in the library's device image instead of a caller workspace.
 
 It is called through the C ABI and compared with tq_decode_attention (the
-entry point that takes a workspace) on two calls in a row, with a call on a
-different cache shape in between so that the shared array holds another
-call's leftovers.  This file is collected last on purpose."""
+entry point that takes a workspace) and with the fp64 oracle on the same packed
+cache, on two calls in a row, with a call on a different cache shape in between
+so that the shared array holds another call's leftovers.  This file is
+collected last on purpose."""
+import numpy as np
 import pytest
 
 import workloads as W
-from gpu_harness import ATT_TOL, make_setup, to_torch_input
+from gpu_harness import ATT_TOL, att_error, make_setup, oracle_attention, oracle_encode, put_pair, to_torch_input
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +39,26 @@ def _cache(tq, wl, B, T):
                  torch.zeros(B, dtype=torch.int32, device="cuda"))
     q = to_torch_input(torch, inp.q, wl.in_dtype)
     sl = torch.from_numpy(inp.seq_lens).cuda()
+    # the oracle's records in the device cache, so that the oracle's attention on
+    # them is the reference
+    encs = {}
+    for b in range(B):
+        for h in range(wl.n_kv_heads):
+            ek, ev = oracle_encode(st, "k", b, h), oracle_encode(st, "v", b, h)
+            put_pair(torch, cache, "k", b, h, ek.codes, ek.norms)
+            put_pair(torch, cache, "v", b, h, ev.codes, ev.norms)
+            encs[(b, h)] = (ek, ev)
+    cache.encs = encs
     return st, cache, q, sl
+
+
+def _vs_oracle(st, cache, out, seq_lens):
+    o = out.cpu().numpy()
+    G = st.wl.group
+    for (b, h), (ek, ev) in cache.encs.items():
+        ref = oracle_attention(st, ek, ev, b, h, int(seq_lens[b]))
+        err, scale = att_error(o[b, h * G:(h + 1) * G], ref)
+        assert err <= ATT_TOL * scale, (b, h, err, scale)
 
 
 def _close(a, ref):
@@ -67,6 +88,8 @@ def test_noalloc_matches_workspace_entry_point(tq):
     for o1, o2 in outs:
         _close(o1, ref1)
         _close(o2, ref2)
+        _vs_oracle(st1, c1, o1, l1.cpu().numpy())
+        _vs_oracle(st2, c2, o2, l2.cpu().numpy())
     assert int(c1.status.item()) == 0 and int(c2.status.item()) == 0
 
 
