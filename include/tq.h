@@ -62,6 +62,7 @@ typedef int32_t tq_status;
 #define TQ_DEV_SEQ_OVER_CAPACITY  1  /* seq_len > t_capacity: clamped          */
 #define TQ_DEV_SEQ_OVER_MAX       2  /* seq_len > max_seq_len: clamped         */
 #define TQ_DEV_BAD_POSITION       4  /* append position outside [0, capacity): skipped */
+#define TQ_DEV_INTERNAL           8  /* a kernel's own layout check failed: output not written */
 
 /* ---------------------------------------------------------------- enums */
 #define TQ_F32   0

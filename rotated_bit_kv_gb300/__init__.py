@@ -18,7 +18,7 @@ import numpy as np
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_NO_CONVERGENCE, TQ_ERR_WORKSPACE = range(6)
-TQ_DEV_SEQ_OVER_CAPACITY, TQ_DEV_SEQ_OVER_MAX, TQ_DEV_BAD_POSITION = 1, 2, 4
+TQ_DEV_SEQ_OVER_CAPACITY, TQ_DEV_SEQ_OVER_MAX, TQ_DEV_BAD_POSITION, TQ_DEV_INTERNAL = 1, 2, 4, 8
 TQ_F32, TQ_F16, TQ_BF16 = 0, 1, 2
 TQ_ROT_WHT128, TQ_ROT_WHT32, TQ_ROT_SO4_WHT128 = 0, 1, 2
 TQ_PART_K_CODES, TQ_PART_K_NORMS, TQ_PART_V_CODES, TQ_PART_V_NORMS, TQ_PART_PARAMS = range(5)

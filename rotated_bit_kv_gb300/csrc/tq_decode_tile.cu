@@ -48,6 +48,26 @@ using tqtile::kTok;
 constexpr int kNW = TQ_TILE_WARPS;       // warps per CTA
 constexpr int kNThr = kNW * 32;
 constexpr int kMaxGrid = 152 * 8;        // bound on CTAs (sizes the partial slots)
+// The code-pair table is the first member of the dynamic shared memory, which
+// starts after the 1 KB the CUDA runtime reserves per block: its shared address
+// is this constant, folded into every lookup's immediate offset (the kernel
+// checks it at entry).
+constexpr uint32_t kTabShared = 1024;
+#ifndef TQ_TILE_LAZYMAX
+#define TQ_TILE_LAZYMAX 1
+#endif
+#ifndef TQ_TILE_DEPTH
+#define TQ_TILE_DEPTH 1   // tiles a warp has in flight ahead of the one it processes (1 or 2)
+#endif
+#ifndef TQ_TILE_PIPE
+#define TQ_TILE_PIPE 0
+#endif
+#ifndef TQ_TILE_VHOIST
+#define TQ_TILE_VHOIST 0
+#endif
+#ifndef TQ_TILE_QKCH
+#define TQ_TILE_QKCH 2   // QK accumulator chains of the one-norm formats (2 or 4)
+#endif
 
 template <int GPE>
 constexpr int pieces_per_round() { return GPE <= 4 ? 8 : 2; }
@@ -67,6 +87,7 @@ struct TileSmem {
     float wm[kNW][8], wl[kNW][8];
     float ot[8][128];
     float mm[8], ll[8];
+    float pm[8], pl[8];          // merge of a pair's pieces: max and sum per head
     Seg seg[NP + 1];
     long long scan[kNW];
     long long b_base, next_pos, cur_base;
@@ -175,45 +196,48 @@ __device__ __forceinline__ void build_table(const tq_head_params& P0, uint32_t* 
     }
 }
 
-__device__ __forceinline__ uint32_t lk(const uint32_t* tab, uint32_t addr) {
-    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(tab) + addr);
+// table word at byte offset `addr` of the table
+__device__ __forceinline__ uint32_t lk(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1+1024];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 // table word of byte K of w: the byte goes to bits 8-15, the lane's column
 // offset (4 lane, + 128 for table Y) comes from byte 0 of `col`
 template <int K>
-__device__ __forceinline__ uint32_t lkb(const uint32_t* tab, uint32_t w, uint32_t col) {
-    return lk(tab, prmt(w, col, 0x5504u | (K << 4)));
+__device__ __forceinline__ uint32_t lkb(uint32_t w, uint32_t col) {
+    return lk(prmt(w, col, 0x5504u | (K << 4)));
 }
 
 // Table words of a three-word group of 3-bit codes: o[4 w + k] for byte k of word
 // w, o[12 + g] for the field spread over byte lane g of the three words.
-__device__ __forceinline__ void group3(const uint32_t* tab, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cx,
-                                       uint32_t cy, uint32_t (&o)[16]) {
+__device__ __forceinline__ void group3(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t cx, uint32_t cy,
+                                       uint32_t (&o)[16]) {
     unroll<4>([&](auto k_c) {
         constexpr int k = decltype(k_c)::value;
-        o[k] = lkb<k>(tab, w0, cx);
-        o[4 + k] = lkb<k>(tab, w1, cy);
-        o[8 + k] = lkb<k>(tab, w2, cx);
+        o[k] = lkb<k>(w0, cx);
+        o[4 + k] = lkb<k>(w1, cy);
+        o[8 + k] = lkb<k>(w2, cx);
     });
     const uint32_t m1 = 0x03030303u, m2 = 0x0F0F0F0Fu;
     const uint32_t s1 = ((w0 >> 6) & m1) | (w1 & ~m1);
     const uint32_t s2 = (s1 & m2) | ((w2 >> 2) & ~m2);
     unroll<4>([&](auto g_c) {
         constexpr int g = decltype(g_c)::value;
-        o[12 + g] = lkb<g>(tab, s2, cx);
+        o[12 + g] = lkb<g>(s2, cx);
     });
 }
 
 // ... of a four-word group of 4-bit codes: o[4 w + k] for byte k of word w.
-__device__ __forceinline__ void group4(const uint32_t* tab, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                       uint32_t cx, uint32_t (&o)[16]) {
+__device__ __forceinline__ void group4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t cx,
+                                       uint32_t (&o)[16]) {
     unroll<4>([&](auto k_c) {
         constexpr int k = decltype(k_c)::value;
-        o[k] = lkb<k>(tab, w0, cx);
-        o[4 + k] = lkb<k>(tab, w1, cx);
-        o[8 + k] = lkb<k>(tab, w2, cx);
-        o[12 + k] = lkb<k>(tab, w3, cx);
+        o[k] = lkb<k>(w0, cx);
+        o[4 + k] = lkb<k>(w1, cx);
+        o[8 + k] = lkb<k>(w2, cx);
+        o[12 + k] = lkb<k>(w3, cx);
     });
 }
 
@@ -253,11 +277,19 @@ __device__ __forceinline__ Lane lane_ctx() {
     return l;
 }
 
+// A lane's part of one tile: key words and norms (KRegs), value words and norms
+// (VRegs); loaded separately so that a warp can keep two tiles in flight in two
+// register sets.
 template <int BITS, int NSEG>
-struct TileRegs {
+struct KRegs {
     static constexpr int W = tqtile::group_words(BITS);
-    uint32_t k[2 * W], v[2 * W];
+    uint32_t k[2 * W];
     uint32_t kn[NSEG == 1 ? 2 : 4];   // one slot: (n_r, n_r+8) as fp16 pair or two fp32
+};
+template <int BITS, int NSEG>
+struct VRegs {
+    static constexpr int W = tqtile::group_words(BITS);
+    uint32_t v[2 * W];
     uint32_t vn[NSEG == 1 ? 2 : 8];
 };
 
@@ -283,37 +315,54 @@ __device__ __forceinline__ PairPtr pair_ptr(const DecodeArgs& a, int b, int h) {
 }
 
 template <int BITS, int NSEG>
-__device__ __forceinline__ void load_tile(TileRegs<BITS, NSEG>& td, const PairPtr& pp, int t, const Lane& ln,
-                                          bool f16n) {
+__device__ __forceinline__ void load_k(KRegs<BITS, NSEG>& td, const PairPtr& pp, int t, const Lane& ln, bool f16n) {
     const int lane = threadIdx.x & 31;
     const uint8_t* kt = pp.k + (size_t)t * tqtile::tile_bytes(BITS);
-    const uint8_t* vt = pp.v + (size_t)t * tqtile::tile_bytes(BITS);
-    const uint4 k0 = ldg_stream4(kt + 16 * lane), v0 = ldg_stream4(vt + 16 * lane);
+    const uint4 k0 = ldg_stream4(kt + 16 * lane);
     td.k[0] = k0.x; td.k[1] = k0.y; td.k[2] = k0.z; td.k[3] = k0.w;
-    td.v[0] = v0.x; td.v[1] = v0.y; td.v[2] = v0.z; td.v[3] = v0.w;
     if constexpr (BITS == 3) {
-        const uint2 k1 = ldg_stream2(kt + 512 + 8 * lane), v1 = ldg_stream2(vt + 512 + 8 * lane);
+        const uint2 k1 = ldg_stream2(kt + 512 + 8 * lane);
         td.k[4] = k1.x; td.k[5] = k1.y;
-        td.v[4] = v1.x; td.v[5] = v1.y;
     } else {
-        const uint4 k1 = ldg_stream4(kt + 512 + 16 * lane), v1 = ldg_stream4(vt + 512 + 16 * lane);
+        const uint4 k1 = ldg_stream4(kt + 512 + 16 * lane);
         td.k[4] = k1.x; td.k[5] = k1.y; td.k[6] = k1.z; td.k[7] = k1.w;
-        td.v[4] = v1.x; td.v[5] = v1.y; td.v[6] = v1.z; td.v[7] = v1.w;
     }
     if constexpr (NSEG == 1) {
         if (f16n) {
             td.kn[0] = ldg_u32(pp.kn + ((size_t)t * kTok + 2 * ln.r) * 2);
-            td.vn[0] = ldg_u32(pp.vn + ((size_t)t * kTok + 2 * ln.r) * 2);
-            td.kn[1] = td.vn[1] = 0;
+            td.kn[1] = 0;
         } else {
             const uint2 kk = ldg_u64(pp.kn + ((size_t)t * kTok + 2 * ln.r) * 4);
-            const uint2 vv = ldg_u64(pp.vn + ((size_t)t * kTok + 2 * ln.r) * 4);
             td.kn[0] = kk.x; td.kn[1] = kk.y;
-            td.vn[0] = vv.x; td.vn[1] = vv.y;
         }
-    } else {   // fp16 block norms: keys of tokens r, r + 8; values of tokens 2c, 2c+1, 2c+8, 2c+9
+    } else {   // fp16 block norms of tokens r, r + 8
         const uint4 kk = ldg_u128(pp.kn + ((size_t)t * kTok * 4 + 8 * ln.r) * 2);
         td.kn[0] = kk.x; td.kn[1] = kk.y; td.kn[2] = kk.z; td.kn[3] = kk.w;
+    }
+}
+
+template <int BITS, int NSEG>
+__device__ __forceinline__ void load_v(VRegs<BITS, NSEG>& td, const PairPtr& pp, int t, const Lane& ln, bool f16n) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t* vt = pp.v + (size_t)t * tqtile::tile_bytes(BITS);
+    const uint4 v0 = ldg_stream4(vt + 16 * lane);
+    td.v[0] = v0.x; td.v[1] = v0.y; td.v[2] = v0.z; td.v[3] = v0.w;
+    if constexpr (BITS == 3) {
+        const uint2 v1 = ldg_stream2(vt + 512 + 8 * lane);
+        td.v[4] = v1.x; td.v[5] = v1.y;
+    } else {
+        const uint4 v1 = ldg_stream4(vt + 512 + 16 * lane);
+        td.v[4] = v1.x; td.v[5] = v1.y; td.v[6] = v1.z; td.v[7] = v1.w;
+    }
+    if constexpr (NSEG == 1) {
+        if (f16n) {
+            td.vn[0] = ldg_u32(pp.vn + ((size_t)t * kTok + 2 * ln.r) * 2);
+            td.vn[1] = 0;
+        } else {
+            const uint2 vv = ldg_u64(pp.vn + ((size_t)t * kTok + 2 * ln.r) * 4);
+            td.vn[0] = vv.x; td.vn[1] = vv.y;
+        }
+    } else {   // fp16 block norms of tokens 2c, 2c+1, 2c+8, 2c+9
         const uint4 v0n = ldg_u128(pp.vn + ((size_t)t * kTok * 4 + 16 * ln.c) * 2);
         const uint4 v1n = ldg_u128(pp.vn + ((size_t)t * kTok * 4 + 16 * ln.c + 8) * 2);
         td.vn[0] = v0n.x; td.vn[1] = v0n.y; td.vn[2] = v0n.z; td.vn[3] = v0n.w;
@@ -371,15 +420,13 @@ __device__ __forceinline__ void load_bq(const float (*qts)[128], const Lane& ln,
     }
 }
 
-// QK, online softmax and PV for one tile of `nval` valid tokens.
+// QK of one tile: scores (log2 units) s0 / s8 of tokens r and r + 8 for head 4j + c.
 template <int NT, int BITS, int NSEG>
-__device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nval, const uint32_t* tab,
-                                          const Lane& ln, const uint32_t (&bq)[NT][8][2], bool f16n,
-                                          WState<NT>& ws) {
-    const int r = ln.r;
+__device__ __forceinline__ void qk_phase(const KRegs<BITS, NSEG>& kd, const Lane& ln, const uint32_t (&bq)[NT][8][2],
+                                         bool f16n, float (&s0)[NT], float (&s8)[NT]) {
     // ---- QK: rows = tokens r (kr) and r + 8 (k8); accumulator chains: k steps of
     // even / odd index (one norm) or one chain per 32-wide block (k steps 2b, 2b+1)
-    constexpr int CH = NSEG == 1 ? 2 : 4;
+    constexpr int CH = NSEG == 1 ? TQ_TILE_QKCH : 4;
     float acc[NT][CH][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -388,15 +435,15 @@ __device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nv
     {
         uint32_t kr[16], k8[16];
         if constexpr (BITS == 3) {
-            group3(tab, td.k[0], td.k[1], td.k[2], ln.cx, ln.cy, kr);
-            group3(tab, td.k[3], td.k[4], td.k[5], ln.cx, ln.cy, k8);
+            group3(kd.k[0], kd.k[1], kd.k[2], ln.cx, ln.cy, kr);
+            group3(kd.k[3], kd.k[4], kd.k[5], ln.cx, ln.cy, k8);
         } else {
-            group4(tab, td.k[0], td.k[1], td.k[2], td.k[3], ln.cx, kr);
-            group4(tab, td.k[4], td.k[5], td.k[6], td.k[7], ln.cx, k8);
+            group4(kd.k[0], kd.k[1], kd.k[2], kd.k[3], ln.cx, kr);
+            group4(kd.k[4], kd.k[5], kd.k[6], kd.k[7], ln.cx, k8);
         }
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
-            const int ch = NSEG == 1 ? (st & 1) : (st >> 1);
+            const int ch = NSEG == 1 ? (st & (CH - 1)) : (st >> 1);
 #pragma unroll
             for (int j = 0; j < NT; ++j)
                 mma16816(acc[j][ch], kr[2 * st], k8[2 * st], kr[2 * st + 1], k8[2 * st + 1], bq[j][st][0],
@@ -405,19 +452,24 @@ __device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nv
     }
 
     // ---- scores (log2 units) of tokens r and r + 8 for head 4j + c
-    float s0[NT], s8[NT];
     if constexpr (NSEG == 1) {
-        const float kn0 = f16n ? h_lo(td.kn[0]) : __uint_as_float(td.kn[0]);
-        const float kn8 = f16n ? h_hi(td.kn[0]) : __uint_as_float(td.kn[1]);
+        const float kn0 = f16n ? h_lo(kd.kn[0]) : __uint_as_float(kd.kn[0]);
+        const float kn8 = f16n ? h_hi(kd.kn[0]) : __uint_as_float(kd.kn[1]);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {   // both columns: rounded q~ and its remainder
-            s0[j] = ((acc[j][0][0] + acc[j][1][0]) + (acc[j][0][1] + acc[j][1][1])) * kn0;
-            s8[j] = ((acc[j][0][2] + acc[j][1][2]) + (acc[j][0][3] + acc[j][1][3])) * kn8;
+        for (int j = 0; j < NT; ++j) {   // both columns (rounded q~ and its remainder), every chain
+            float a0 = acc[j][0][0] + acc[j][0][1], a8 = acc[j][0][2] + acc[j][0][3];
+#pragma unroll
+            for (int q = 1; q < CH; ++q) {
+                a0 += acc[j][q][0] + acc[j][q][1];
+                a8 += acc[j][q][2] + acc[j][q][3];
+            }
+            s0[j] = a0 * kn0;
+            s8[j] = a8 * kn8;
         }
     } else {
         float n0[4], n8[4];
-        n0[0] = h_lo(td.kn[0]); n0[1] = h_hi(td.kn[0]); n0[2] = h_lo(td.kn[1]); n0[3] = h_hi(td.kn[1]);
-        n8[0] = h_lo(td.kn[2]); n8[1] = h_hi(td.kn[2]); n8[2] = h_lo(td.kn[3]); n8[3] = h_hi(td.kn[3]);
+        n0[0] = h_lo(kd.kn[0]); n0[1] = h_hi(kd.kn[0]); n0[2] = h_lo(kd.kn[1]); n0[3] = h_hi(kd.kn[1]);
+        n8[0] = h_lo(kd.kn[2]); n8[1] = h_hi(kd.kn[2]); n8[2] = h_lo(kd.kn[3]); n8[3] = h_hi(kd.kn[3]);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {   // per block: rounded q~ and its remainder, then the block's norm
             float a0 = n0[0] * (acc[j][0][0] + acc[j][0][1]), a8 = n8[0] * (acc[j][0][2] + acc[j][0][3]);
@@ -430,19 +482,50 @@ __device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nv
             s8[j] = a8;
         }
     }
-    const bool ragged = nval < kTok;
-    if (ragged) {   // tokens past the end take no weight
+}
+
+// Online softmax and PV of one tile of `nval` valid tokens (past-the-end tokens of
+// a short last tile take no weight), from its scores.
+template <int NT, int BITS, int NSEG>
+__device__ __forceinline__ void pv_phase(const VRegs<BITS, NSEG>& td, float (&s0)[NT], float (&s8)[NT], int nval,
+                                         const Lane& ln, bool f16n, WState<NT>& ws) {
+    const int r = ln.r;
+    constexpr int W = tqtile::group_words(BITS);
+    uint32_t vg[2][16];
+    auto vlookups = [&](auto u_c) {
+        constexpr int u = decltype(u_c)::value;
+        if constexpr (BITS == 3) group3(td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], ln.cx, ln.cy, vg[u]);
+        else group4(td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], td.v[W * u + 3], ln.cx, vg[u]);
+    };
+#if TQ_TILE_VHOIST
+    unroll<2>(vlookups);   // value operands first: they depend on nothing of the softmax
+#endif
+    const bool in0 = r < nval, in8 = r + 8 < nval;
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            if (r >= nval) s0[j] = -INFINITY;
-            if (r + 8 >= nval) s8[j] = -INFINITY;
-        }
+    for (int j = 0; j < NT; ++j) {
+        s0[j] = in0 ? s0[j] : -INFINITY;
+        s8[j] = in8 ? s8[j] : -INFINITY;
     }
 
     // ---- online softmax: the base moves only when the tile maximum exceeds it by
     // more than 4 (log2 units), so p <= 16 and rescales are rare
-    float mn[NT];
     bool move = false;
+#if TQ_TILE_LAZYMAX
+    // a tile needs the maximum only when one of its scores passes the base + 4
+#pragma unroll
+    for (int j = 0; j < NT; ++j) move = move || s0[j] > ws.m[j] + 4.f || s8[j] > ws.m[j] + 4.f;
+    if (__any_sync(TQ_FULL_MASK, move)) {
+        float mn[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            float mt = fmaxf(s0[j], s8[j]);
+            mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 4));
+            mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 8));
+            mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 16));
+            mn[j] = mt > ws.m[j] + 4.f ? mt : ws.m[j];
+        }
+#else
+    float mn[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         float mt = fmaxf(s0[j], s8[j]);
@@ -453,6 +536,7 @@ __device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nv
         move = move || mn[j] != ws.m[j];
     }
     if (__any_sync(TQ_FULL_MASK, move)) {
+#endif
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const float cf = ex2(ws.m[j] - mn[j]);   // 0 on the first tile (m = -inf)
@@ -477,10 +561,8 @@ __device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nv
         if constexpr (NSEG == 1) {
             float vn0 = f16n ? h_lo(td.vn[0]) : __uint_as_float(td.vn[0]);
             float vn8 = f16n ? h_hi(td.vn[0]) : __uint_as_float(td.vn[1]);
-            if (ragged) {   // past the end: zero weight even if the stored norm is not finite
-                vn0 = r < nval ? vn0 : 0.f;
-                vn8 = r + 8 < nval ? vn8 : 0.f;
-            }
+            vn0 = in0 ? vn0 : 0.f;   // past the end: zero weight even if the stored norm is not finite
+            vn8 = in8 ? vn8 : 0.f;
             p0 *= vn0;
             p8 *= vn8;
         }
@@ -494,28 +576,27 @@ __device__ __forceinline__ void tile_step(const TileRegs<BITS, NSEG>& td, int nv
     // ---- PV: group u of the values holds tokens 2c + 8u (A) and 2c + 1 + 8u (B)
     unroll<2>([&](auto u_c) {
         constexpr int u = decltype(u_c)::value;
-        constexpr int W = tqtile::group_words(BITS);
-        uint32_t vg[16];
-        if constexpr (BITS == 3) group3(tab, td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], ln.cx, ln.cy, vg);
-        else group4(tab, td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], td.v[W * u + 3], ln.cx, vg);
+#if !TQ_TILE_VHOIST
+        vlookups(u_c);
+#endif
         // four blocks: each m tile is one block; its value norms scale the P operand
         uint32_t wa[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};
+        (void)wa;
+        (void)wb;
         if constexpr (NSEG == 4) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 uint32_t w = td.vn[4 * u + b];   // (n_b(2c + 8u), n_b(2c + 1 + 8u))
-                if (ragged) {
-                    const int ta = 2 * ln.c + 8 * u;
-                    w = (ta < nval ? (w & 0xFFFFu) : 0u) | (ta + 1 < nval ? (w & 0xFFFF0000u) : 0u);
-                }
+                const int ta = 2 * ln.c + 8 * u;
+                w = (ta < nval ? (w & 0xFFFFu) : 0u) | (ta + 1 < nval ? (w & 0xFFFF0000u) : 0u);
                 wa[b] = prmt(w, w, ln.sw_a);
                 wb[b] = prmt(w, w, ln.sw_b);
             }
         }
         unroll<4>([&](auto mt_c) {
             constexpr int mt = decltype(mt_c)::value;
-            const uint32_t a0 = vg[vA<BITS>(2 * mt)], a1 = vg[vA<BITS>(2 * mt + 1)];
-            const uint32_t a2 = vg[vB<BITS>(2 * mt)], a3 = vg[vB<BITS>(2 * mt + 1)];
+            const uint32_t a0 = vg[u][vA<BITS>(2 * mt)], a1 = vg[u][vA<BITS>(2 * mt + 1)];
+            const uint32_t a2 = vg[u][vB<BITS>(2 * mt)], a3 = vg[u][vB<BITS>(2 * mt + 1)];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 if constexpr (NSEG == 1) {
@@ -572,12 +653,63 @@ __device__ __forceinline__ void merge_warps(const float (*wo)[GPE][128], const f
     }
 }
 
+// Log-sum-exp merge of `parts` published partials (rows [part t][head g] of
+// kPartStride floats: o~[128], m, l) into ot[g][0..127], normalised  [Block-GTQ].
+// A warp per head finds M_g = max_t m_t and L_g = sum_t 2^(m_t - M_g) l_t (into
+// pm, pl); then each thread accumulates four coordinates of one head over the
+// parts.  Empty parts (m = -inf) weigh 0; a pair with no tokens gives 0.
+template <int GP>
+__device__ __forceinline__ void merge_pieces(const float* base, int parts, float (*ot)[128], float* pm, float* pl) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int g = warp; g < GP; g += kNW) {
+        float M = -INFINITY;
+        for (int t = lane; t < parts; t += 32) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(TQ_FULL_MASK, M, o));
+        float L = 0.f;
+        for (int t = lane; t < parts; t += 32) {
+            const float* pr = base + ((size_t)t * GP + g) * kPartStride;
+            const float mt = __ldcg(pr + 128);
+            L = fmaf(mt == -INFINITY ? 0.f : exp2f(mt - M), __ldcg(pr + 129), L);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(TQ_FULL_MASK, L, o);
+        if (lane == 0) {
+            pm[g] = M;
+            pl[g] = L;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < GP * 32; i += kNThr) {
+        const int g = i >> 5, d4 = i & 31;
+        const float M = pm[g];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int t = 0; t < parts; ++t) {
+            const float* pr = base + ((size_t)t * GP + g) * kPartStride;
+            const float mt = __ldcg(pr + 128);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(pr) + d4);
+            const float w = mt == -INFINITY ? 0.f : exp2f(mt - M);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        const float L = pl[g];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        ot[g][4 * d4] = acc.x * inv;
+        ot[g][4 * d4 + 1] = acc.y * inv;
+        ot[g][4 * d4 + 2] = acc.z * inv;
+        ot[g][4 * d4 + 3] = acc.w * inv;
+    }
+}
+
 // Finish a piece: ot[g][c] holds its unnormalised o~, (mm[g], ll[g]) its softmax
 // state (shared memory).  One part: normalise and write; else publish the partial
 // and let the last CTA of the pair merge all of them.
 template <int GP>
 __device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const float* mm,
-                             const float* ll, int* is_last, const Seg& sg) {
+                             const float* ll, float* pm, float* pl, int* is_last, const Seg& sg) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int pair = sg.b * a.Hkv + sg.h;
     if (sg.parts > 1) {
@@ -597,7 +729,7 @@ __device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float
         if (!*is_last) return;
         __threadfence();
         // log-sum-exp merge over the pair's parts  [Block-GTQ]
-        merge_parts<GP, kNThr>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot);
+        merge_pieces<GP>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot, pm, pl);
         if (tid == 0) a.tickets[pair] = 0;   // ready for the next call
         __syncthreads();
     } else {
@@ -643,8 +775,11 @@ __device__ __forceinline__ int seq_len_of(const DecodeArgs& a, int b, bool repor
     return L;
 }
 
+#ifndef TQ_TILE_MINB
+#define TQ_TILE_MINB 2
+#endif
 template <int NT, int BITS, int NSEG>
-__global__ void __launch_bounds__(kNThr, NT == 1 ? 2 : 1) decode_tile(DecodeArgs a) {
+__global__ void __launch_bounds__(kNThr, NT == 1 ? TQ_TILE_MINB : 1) decode_tile(DecodeArgs a) {
     constexpr int GPE = 4 * NT;
     constexpr int NP = pieces_per_round<GPE>();
     extern __shared__ __align__(128) unsigned char tile_smem_raw[];
@@ -653,6 +788,13 @@ __global__ void __launch_bounds__(kNThr, NT == 1 ? 2 : 1) decode_tile(DecodeArgs
     // launched as a programmatic dependent of the previous kernel in the stream:
     // nothing is read before that kernel has completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the lookups address the table at a fixed shared offset: check it (no static
+    // shared memory in this kernel, so the dynamic block starts after the
+    // reserved 1 KB); on a mismatch nothing is read or written but the flag
+    if ((uint32_t)__cvta_generic_to_shared(S.tab) != kTabShared) {
+        if (tid == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, TQ_DEV_INTERNAL);
+        return;
+    }
     build_table<BITS>(a.params[0], S.tab);
     const bool f16n = a.norm_f16 != 0;
 
@@ -746,13 +888,14 @@ __global__ void __launch_bounds__(kNThr, NT == 1 ? 2 : 1) decode_tile(DecodeArgs
         const int nseg = S.nseg;
         if (nseg == 0) break;
 
-        // first tile of the round, in flight while the queries are rotated
-        TileRegs<BITS, NSEG> ta, tb;
+        // first keys of the round, in flight while the queries are rotated
+        KRegs<BITS, NSEG> kA, kB;
+        VRegs<BITS, NSEG> vA, vB;
         PairPtr pp = pair_ptr<BITS, NSEG>(a, S.seg[0].b, S.seg[0].h);
-        bool a_loaded = false;
+        bool k_loaded = false;
         if (S.seg[0].t_lo + warp < S.seg[0].t_hi) {
-            load_tile(ta, pp, S.seg[0].t_lo + warp, ln, f16n);
-            a_loaded = true;
+            load_k(kA, pp, S.seg[0].t_lo + warp, ln, f16n);
+            k_loaded = true;
         }
         for (int i = warp; i < nseg * GPE; i += kNW) {
             const Seg& sg = S.seg[i / GPE];
@@ -767,33 +910,96 @@ __global__ void __launch_bounds__(kNThr, NT == 1 ? 2 : 1) decode_tile(DecodeArgs
             load_bq<NT>(S.qts[k], ln, kinv, bq);
             WState<NT> ws;
             ws.reset();
-            // this warp's tiles of the piece: t_lo + warp + kNW i; tile 0 is in ta
+            // this warp's tiles of the piece: t_lo + warp + kNW i
             const int n = sg.t_hi - sg.t_lo > warp ? (sg.t_hi - sg.t_lo - warp + kNW - 1) / kNW : 0;
             auto tile_at = [&](int i) { return sg.t_lo + warp + kNW * i; };
             auto nval_at = [&](int i) { return min(kTok, sg.L - tile_at(i) * kTok); };
-            if (n > 0 && !a_loaded) load_tile(ta, pp, tile_at(0), ln, f16n);
-            for (int i = 0; i < n; i += 2) {
-                if (i + 1 < n) load_tile(tb, pp, tile_at(i + 1), ln, f16n);
-                tile_step<NT, BITS, NSEG>(ta, nval_at(i), S.tab, ln, bq, f16n, ws);
-                if (i + 1 >= n) break;
-                if (i + 2 < n) load_tile(ta, pp, tile_at(i + 2), ln, f16n);
-                tile_step<NT, BITS, NSEG>(tb, nval_at(i + 1), S.tab, ln, bq, f16n, ws);
+#if TQ_TILE_PIPE
+            // software pipeline: the QK of tile i + 1 goes before the softmax and PV of
+            // tile i (they are independent); keys of tile i + 2 load as soon as the key
+            // registers of tile i are free, values of tile i + 2 after the PV of tile i
+            if (n > 0) {
+                if (!k_loaded) load_k(kA, pp, tile_at(0), ln, f16n);
+                load_v(vA, pp, tile_at(0), ln, f16n);
             }
-            // the next piece's first tile, in flight during the merge
-            a_loaded = false;
+            if (n > 1) {
+                load_k(kB, pp, tile_at(1), ln, f16n);
+                load_v(vB, pp, tile_at(1), ln, f16n);
+            }
+            float sA0[NT], sA8[NT], sB0[NT], sB8[NT];
+            if (n > 0) qk_phase<NT, BITS, NSEG>(kA, ln, bq, f16n, sA0, sA8);
+            if (n > 2) load_k(kA, pp, tile_at(2), ln, f16n);
+            for (int i = 0; i < n; i += 2) {
+                if (i + 1 < n) qk_phase<NT, BITS, NSEG>(kB, ln, bq, f16n, sB0, sB8);
+                if (i + 3 < n) load_k(kB, pp, tile_at(i + 3), ln, f16n);
+                pv_phase<NT, BITS, NSEG>(vA, sA0, sA8, nval_at(i), ln, f16n, ws);
+                if (i + 2 < n) load_v(vA, pp, tile_at(i + 2), ln, f16n);
+                if (i + 1 >= n) break;
+                if (i + 2 < n) qk_phase<NT, BITS, NSEG>(kA, ln, bq, f16n, sA0, sA8);
+                if (i + 4 < n) load_k(kA, pp, tile_at(i + 4), ln, f16n);
+                pv_phase<NT, BITS, NSEG>(vB, sB0, sB8, nval_at(i + 1), ln, f16n, ws);
+                if (i + 3 < n) load_v(vB, pp, tile_at(i + 3), ln, f16n);
+            }
+#else
+            // tile i + 1 loads while tile i is processed
+            auto step = [&](const KRegs<BITS, NSEG>& kd, const VRegs<BITS, NSEG>& vd, int nv) {
+                float s0[NT], s8[NT];
+                qk_phase<NT, BITS, NSEG>(kd, ln, bq, f16n, s0, s8);
+                pv_phase<NT, BITS, NSEG>(vd, s0, s8, nv, ln, f16n, ws);
+            };
+            if (n > 0) {
+                if (!k_loaded) load_k(kA, pp, tile_at(0), ln, f16n);
+                load_v(vA, pp, tile_at(0), ln, f16n);
+            }
+#if TQ_TILE_DEPTH == 2
+            // tiles i + 1 and i + 2 in flight while tile i is processed
+            KRegs<BITS, NSEG> kC;
+            VRegs<BITS, NSEG> vC;
+            if (n > 1) {
+                load_k(kB, pp, tile_at(1), ln, f16n);
+                load_v(vB, pp, tile_at(1), ln, f16n);
+            }
+            for (int i = 0; i < n; i += 3) {
+                if (i + 2 < n) { load_k(kC, pp, tile_at(i + 2), ln, f16n); load_v(vC, pp, tile_at(i + 2), ln, f16n); }
+                step(kA, vA, nval_at(i));
+                if (i + 1 >= n) break;
+                if (i + 3 < n) { load_k(kA, pp, tile_at(i + 3), ln, f16n); load_v(vA, pp, tile_at(i + 3), ln, f16n); }
+                step(kB, vB, nval_at(i + 1));
+                if (i + 2 >= n) break;
+                if (i + 4 < n) { load_k(kB, pp, tile_at(i + 4), ln, f16n); load_v(vB, pp, tile_at(i + 4), ln, f16n); }
+                step(kC, vC, nval_at(i + 2));
+            }
+#else
+            for (int i = 0; i < n; i += 2) {
+                if (i + 1 < n) {
+                    load_k(kB, pp, tile_at(i + 1), ln, f16n);
+                    load_v(vB, pp, tile_at(i + 1), ln, f16n);
+                }
+                step(kA, vA, nval_at(i));
+                if (i + 1 >= n) break;
+                if (i + 2 < n) {
+                    load_k(kA, pp, tile_at(i + 2), ln, f16n);
+                    load_v(vA, pp, tile_at(i + 2), ln, f16n);
+                }
+                step(kB, vB, nval_at(i + 1));
+            }
+#endif
+#endif
+            // the next piece's first keys, in flight during the merge
+            k_loaded = false;
             if (k + 1 < nseg) {
                 const Seg& sn = S.seg[k + 1];
                 pp = pair_ptr<BITS, NSEG>(a, sn.b, sn.h);
                 if (sn.t_lo + warp < sn.t_hi) {
-                    load_tile(ta, pp, sn.t_lo + warp, ln, f16n);
-                    a_loaded = true;
+                    load_k(kA, pp, sn.t_lo + warp, ln, f16n);
+                    k_loaded = true;
                 }
             }
             warp_state_out<NT>(ws, ln, S.wo[warp], S.wm[warp], S.wl[warp]);
             __syncthreads();
             merge_warps<GPE, GPE>(S.wo, S.wm, S.wl, vinv, S.ot, S.mm, S.ll);
             __syncthreads();
-            finish_piece<GPE>(a, P, S.ot, S.mm, S.ll, &S.is_last, sg);
+            finish_piece<GPE>(a, P, S.ot, S.mm, S.ll, S.pm, S.pl, &S.is_last, sg);
             __syncthreads();
         }
     }
@@ -854,7 +1060,7 @@ int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len) {
     // resident CTAs on this device; without one, the design's: 2 (4 query heads
     // per KV head) or 1 (8) CTAs per SM on 152 SMs
     int cap = grid_cap(d);
-    if (cap <= 0) cap = (d->group <= 4 ? 2 : 1) * 152;
+    if (cap <= 0) cap = (d->group <= 4 ? TQ_TILE_MINB : 1) * 152;
     // at least 4 tiles per warp of a CTA on average
     const long long tiles = (long long)d->batch * d->n_kv_heads * ((max_seq_len + kTok - 1) / kTok);
     long long g = (tiles + 4 * kNW - 1) / (4 * kNW);
