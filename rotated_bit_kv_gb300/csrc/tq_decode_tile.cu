@@ -56,6 +56,9 @@ constexpr uint32_t kTabShared = 1024;
 #ifndef TQ_TILE_LAZYMAX
 #define TQ_TILE_LAZYMAX 1
 #endif
+#ifndef TQ_TILE_BQSMEM
+#define TQ_TILE_BQSMEM 0
+#endif
 #ifndef TQ_TILE_DEPTH
 #define TQ_TILE_DEPTH 1   // tiles a warp has in flight ahead of the one it processes (1 or 2)
 #endif
@@ -83,6 +86,9 @@ struct TileSmem {
     static constexpr int NP = pieces_per_round<GPE>();
     uint32_t tab[256 * 64];      // row e: 32 lane columns of table X, then 32 of table Y
     float qts[NP][GPE][128];     // rotated queries of the round's pieces (log2 units)
+#if TQ_TILE_BQSMEM
+    uint32_t bqs[NP][GPE / 4][8][32][2];   // QK operand B per piece, head group, k step, lane
+#endif
     float wo[kNW][GPE][128];     // warp states
     float wm[kNW][8], wl[kNW][8];
     float ot[8][128];
@@ -391,6 +397,22 @@ struct WState {
 __device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
 __device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
 
+// The QK operand B of a lane: in registers, or (TQ_TILE_BQSMEM) read from the
+// piece's fragment table in shared memory at each k step.
+#if TQ_TILE_BQSMEM
+template <int NT>
+struct BqT {
+    const uint2* base;   // [NT][8][32] fragments of this piece, + lane
+    __device__ __forceinline__ uint2 get(int j, int st) const { return base[(j * 8 + st) * 32]; }
+};
+#else
+template <int NT>
+struct BqT {
+    uint32_t r[NT][8][2];
+    __device__ __forceinline__ uint2 get(int j, int st) const { return make_uint2(r[j][st][0], r[j][st][1]); }
+};
+#endif
+
 // fp16 pair of (x, y) (hi = false) or of what the fp16 rounding of (x, y) leaves
 // (hi = true gives the rounded pair itself)
 __device__ __forceinline__ uint32_t pack_part(float x, float y, bool lo) {
@@ -422,7 +444,7 @@ __device__ __forceinline__ void load_bq(const float (*qts)[128], const Lane& ln,
 
 // QK of one tile: scores (log2 units) s0 / s8 of tokens r and r + 8 for head 4j + c.
 template <int NT, int BITS, int NSEG>
-__device__ __forceinline__ void qk_phase(const KRegs<BITS, NSEG>& kd, const Lane& ln, const uint32_t (&bq)[NT][8][2],
+__device__ __forceinline__ void qk_phase(const KRegs<BITS, NSEG>& kd, const Lane& ln, const BqT<NT>& bq,
                                          bool f16n, float (&s0)[NT], float (&s8)[NT]) {
     // ---- QK: rows = tokens r (kr) and r + 8 (k8); accumulator chains: k steps of
     // even / odd index (one norm) or one chain per 32-wide block (k steps 2b, 2b+1)
@@ -446,8 +468,10 @@ __device__ __forceinline__ void qk_phase(const KRegs<BITS, NSEG>& kd, const Lane
             const int ch = NSEG == 1 ? (st & (CH - 1)) : (st >> 1);
 #pragma unroll
             for (int j = 0; j < NT; ++j)
-                mma16816(acc[j][ch], kr[2 * st], k8[2 * st], kr[2 * st + 1], k8[2 * st + 1], bq[j][st][0],
-                         bq[j][st][1]);
+            {
+                const uint2 b = bq.get(j, st);
+                mma16816(acc[j][ch], kr[2 * st], k8[2 * st], kr[2 * st + 1], k8[2 * st + 1], b.x, b.y);
+            }
         }
     }
 
@@ -778,8 +802,13 @@ __device__ __forceinline__ int seq_len_of(const DecodeArgs& a, int b, bool repor
 #ifndef TQ_TILE_MINB
 #define TQ_TILE_MINB 2
 #endif
+#ifdef TQ_TILE_MAXNREG
+#define TQ_TILE_BOUNDS __maxnreg__(TQ_TILE_MAXNREG)
+#else
+#define TQ_TILE_BOUNDS __launch_bounds__(kNThr, NT == 1 ? TQ_TILE_MINB : 1)
+#endif
 template <int NT, int BITS, int NSEG>
-__global__ void __launch_bounds__(kNThr, NT == 1 ? TQ_TILE_MINB : 1) decode_tile(DecodeArgs a) {
+__global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
     constexpr int GPE = 4 * NT;
     constexpr int NP = pieces_per_round<GPE>();
     extern __shared__ __align__(128) unsigned char tile_smem_raw[];
@@ -902,12 +931,27 @@ __global__ void __launch_bounds__(kNThr, NT == 1 ? TQ_TILE_MINB : 1) decode_tile
             rotate_q(a, a.params[sg.h], sg.b, sg.h, i % GPE, S.qts[i / GPE][i % GPE]);
         }
         __syncthreads();
+#if TQ_TILE_BQSMEM
+        for (int i = tid; i < nseg * NT * 8 * 32; i += kNThr) {   // (piece, head group, k step, lane)
+            const int L = i & 31, st = (i >> 5) & 7, j = (i >> 8) % NT, kk = i / (NT * 256);
+            const int r = L >> 2, c = L & 3;
+            const float* qh = S.qts[kk][4 * j + (r >> 1)];
+            const int d0 = 16 * st + 2 * c, d1 = d0 + 8;
+            S.bqs[kk][j][st][L][0] = pack_part(qh[d0] * kinv, qh[d0 + 1] * kinv, r & 1);
+            S.bqs[kk][j][st][L][1] = pack_part(qh[d1] * kinv, qh[d1 + 1] * kinv, r & 1);
+        }
+        __syncthreads();
+#endif
 
         for (int k = 0; k < nseg; ++k) {
             const Seg sg = S.seg[k];
             const tq_head_params& P = a.params[sg.h];
-            uint32_t bq[NT][8][2];
-            load_bq<NT>(S.qts[k], ln, kinv, bq);
+            BqT<NT> bq;
+#if TQ_TILE_BQSMEM
+            bq.base = reinterpret_cast<const uint2*>(S.bqs[k]) + lane;
+#else
+            load_bq<NT>(S.qts[k], ln, kinv, bq.r);
+#endif
             WState<NT> ws;
             ws.reset();
             // this warp's tiles of the piece: t_lo + warp + kNW i

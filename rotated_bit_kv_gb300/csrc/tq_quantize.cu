@@ -835,31 +835,77 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
                 slot = -1;
             }
         }
-        const bool odd = c & 1;
-        uint8_t* sr = &stage[2 * g + (odd ? 1 : 0)][3 * (c >> 1)];
+        if (!a.tiled) {   // the natural layout's records, assembled in shared memory
+            const bool odd = c & 1;
+            uint8_t* sr = &stage[2 * g + (odd ? 1 : 0)][3 * (c >> 1)];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const uint32_t o = __shfl_xor_sync(TQ_FULL_MASK, pc[u], 1);
-            const uint32_t w = odd ? ((o >> 12) & 0xFFFu) | (pc[u] & 0xFFF000u) : (pc[u] & 0xFFFu) | ((o & 0xFFFu) << 12);
-            uint8_t* r = sr + 6 * u;
-            if (c < 2) {
-                *reinterpret_cast<uint16_t*>(r) = (uint16_t)w;
-                r[2] = (uint8_t)(w >> 16);
-            } else {
-                r[0] = (uint8_t)w;
-                *reinterpret_cast<uint16_t*>(r + 1) = (uint16_t)(w >> 8);
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t o = __shfl_xor_sync(TQ_FULL_MASK, pc[u], 1);
+                const uint32_t w = odd ? ((o >> 12) & 0xFFFu) | (pc[u] & 0xFFF000u) : (pc[u] & 0xFFFu) | ((o & 0xFFFu) << 12);
+                uint8_t* r = sr + 6 * u;
+                if (c < 2) {
+                    *reinterpret_cast<uint16_t*>(r) = (uint16_t)w;
+                    r[2] = (uint8_t)(w >> 16);
+                } else {
+                    r[0] = (uint8_t)w;
+                    *reinterpret_cast<uint16_t*>(r + 1) = (uint16_t)(w >> 8);
+                }
             }
         }
         const size_t rec_i = (((size_t)b * Hkv + h) * a.t_alloc) + (slot < 0 ? 0 : slot);
         __syncwarp();
-        if (a.tiled) {   // each record scattered into its tile by the whole warp
-#pragma unroll 1
-            for (int rr = 0; rr < 8; ++rr) {
-                const int slot_r = __shfl_sync(TQ_FULL_MASK, slot, 4 * rr);
-                const unsigned long long ri = __shfl_sync(TQ_FULL_MASK, (unsigned long long)rec_i, 4 * rr);
-                if (slot_r >= 0) {
-                    store_tiled(a, 0, ri, reinterpret_cast<const uint32_t*>(stage[2 * rr]), 3, lane);
-                    store_tiled(a, 1, ri, reinterpret_cast<const uint32_t*>(stage[2 * rr + 1]), 3, lane);
+        if (a.tiled) {
+            // Tile layout, from the codes in registers.  Lane (g, c) holds, for u = 0..7 and
+            // e = 0, 1, the key and value fields of pairs 8u + 2c + e (pc[u] bits 6e.. and
+            // 12 + 6e..).  Keys: such a field is slot 2u + (c >> 1) of lane column
+            // 2 (c & 1) + e, so a key word holds fields of lanes c and c ^ 2: each builds
+            // its bytes, one shuffle merges them, lane c stores column 2 (c & 1) + (c >> 1).
+            // Values: the field is slot u of lane row 2c + e, so lane (g, c) builds the
+            // whole value halves of rows 2c and 2c + 1.
+            const int t = (int)(rec_i & 15);
+            const size_t tile = rec_i >> 4;
+            const int ch = c >> 1;
+            uint32_t kw[2][3];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                for (int w = 0; w < 3; ++w) {
+                    uint32_t x = 0;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t f = (pc[2 * w + kk] >> (6 * e)) & 63u;
+                        const uint32_t F = (pc[6 + kk] >> (6 * e)) & 63u;
+                        x |= (tqtile::byte3(f, w) | tqtile::piece3(F, w)) << (8 * (ch + 2 * kk));
+                    }
+                    kw[e][w] = x;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int w = 0; w < 3; ++w) kw[e][w] |= __shfl_xor_sync(TQ_FULL_MASK, kw[e][w], 2);
+            if (slot >= 0) {
+                uint8_t* kt = a.codes[0] + tile * tqtile::tile_bytes(3);
+                const int L = 4 * (t & 7) + 2 * (c & 1) + ch;
+#pragma unroll
+                for (int w = 0; w < 3; ++w)
+                    *reinterpret_cast<uint32_t*>(kt + tqtile::word_off(3, L, 3 * (t >> 3) + w)) = ch ? kw[1][w] : kw[0][w];
+                uint8_t* vt = a.codes[1] + tile * tqtile::tile_bytes(3);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int Lv = 4 * (2 * c + e) + ((t & 7) >> 1);
+#pragma unroll
+                    for (int w = 0; w < 3; ++w) {
+                        uint32_t x = 0;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t f = (pc[2 * w + j] >> (12 + 6 * e)) & 63u;
+                            const uint32_t F = (pc[6 + j] >> (12 + 6 * e)) & 63u;
+                            x |= (tqtile::byte3(f, w) | tqtile::piece3(F, w)) << (8 * j);
+                        }
+                        *reinterpret_cast<uint16_t*>(vt + tqtile::word_off(3, Lv, 3 * (t >> 3) + w) + 2 * (t & 1)) =
+                            (uint16_t)x;
+                    }
                 }
             }
         } else {

@@ -36,3 +36,15 @@ def tqlib():
     tq.build()
     tq.lib()
     return tq
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Write-side statistics the GPU parity tests collected (if they ran)."""
+    mod = sys.modules.get("test_gpu_parity") or sys.modules.get("tests.test_gpu_parity")
+    rows = getattr(mod, "STATS", None) if mod else None
+    if not rows:
+        return
+    terminalreporter.write_line("write side vs oracle: workload, B, T, mismatch frac, near-boundary frac "
+                                "(normalised), near-boundary frac (scaled)")
+    for r in rows:
+        terminalreporter.write_line("  %-12s %3d %6d  %.2e  %.2e  %.2e" % r)

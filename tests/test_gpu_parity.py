@@ -19,6 +19,10 @@ from gpu_harness import (ATT_TOL, MAX_MISMATCH_FRAC, att_error, cache_norms, cac
 
 pytestmark = pytest.mark.gpu
 
+# (workload, batch, T, mismatch fraction, near-boundary fraction normalised / scaled),
+# printed at the end of the session
+STATS = []
+
 torch = pytest.importorskip("torch")
 
 
@@ -83,6 +87,7 @@ def test_quantize_append_matches_oracle(tq, name):
     kc, vc = cache_records(cache, "k"), cache_records(cache, "v")
     kn, vn = cache_norms(cache, "k"), cache_norms(cache, "v")
     tot = bad = 0
+    fws_all, fw_all = [], []
     for b in range(B):
         for h in range(st.wl.n_kv_heads):
             for which, codes, norms in (("k", kc, kn), ("v", vc, vn)):
@@ -92,10 +97,19 @@ def test_quantize_append_matches_oracle(tq, name):
                 assert ok, f"{which} b={b} h={h}: a mismatch outside the near-boundary window"
                 bad += nbad
                 tot += n
+                fw_all.append(fw)
+                fws_all.append(fws)
                 assert compare_norms(norms[b, h, :T], enc), f"{which} norms b={b} h={h}"
                 # slots beyond T stay untouched (zero)
                 assert not codes[b, h, T:].any()
     assert bad / tot <= MAX_MISMATCH_FRAC, (bad, tot)
+    # the near-boundary fraction, in the frame of the stored value n * y (|n (y - b)| <= 1e-5):
+    # at most 1e-4 for uniform-rate caches; mixed-rate keys normalise small low-energy
+    # groups whose norms are tiny, so there it is reported only (their mismatch fraction
+    # is gated above like every other format's)
+    if not st.wl.mixed_k:
+        assert np.mean(fws_all) <= 1e-4, np.mean(fws_all)
+    STATS.append((name, B, T, bad / tot, float(np.mean(fw_all)), float(np.mean(fws_all))))
 
 
 def _check_codes_vs_oracle(st, cache, B, T):
