@@ -585,6 +585,58 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_crossover(args):
+    """Token- against dimension-parallel V accumulation on the caches that use those
+    kernels (natural layout: mixed-rate keys, 16 query heads per KV head, fp32 norms
+    with 32-wide blocks): decode time of each kernel over a range of lengths (one
+    cache per workload filled to its longest length, the same launches as the sweep)."""
+    import torch
+
+    import rotated_bit_kv_gb300 as tq
+
+    tq.build()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    lengths = [64, 128, 256, 384, 512, 768, 1024, 2048, 4096]
+    cases = [W.mixed_rate_long(seq_len=max(lengths)), W.llama8b_decode(seq_len=max(lengths), batch=8).with_(n_kv_heads=2),
+             W.block32(3, seq_len=max(lengths), batch=8).with_(norm_dtype=W.F32)]
+    print("| workload | B | T | token-parallel us | dimension-parallel us | faster |")
+    print("|---|---|---|---|---|---|")
+    for wl in cases:
+        Tm = max(lengths)
+        inp = W.make_inputs(wl, seq_len=Tm)
+        desc, blob = library_setup(tq, wl, inp, Tm)
+        assert desc.layout == tq.TQ_LAYOUT_NATURAL
+        cache = tq.PackedKVCache(desc, blob, device=dev)
+        K = _to_torch(torch, inp.K, wl.in_dtype, dev)
+        V = _to_torch(torch, inp.V, wl.in_dtype, dev)
+        cache.append(K, V, torch.zeros(wl.batch, dtype=torch.int32, device=dev))
+        del K, V
+        q = _to_torch(torch, inp.q, wl.in_dtype, dev)
+        out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+        name = wl.name + ("" if wl.mixed_k else f" (G={wl.group}, {'fp32' if wl.norm_dtype == W.F32 else 'fp16'} norms)")
+        for T in lengths:
+            seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
+            res = []
+            for vm in (tq.TQ_VMODE_TOKEN_PARALLEL, tq.TQ_VMODE_DIM_PARALLEL):
+                for _ in range(3):
+                    cache.decode(q, seq, T, out=out, v_mode=vm)
+                times = []
+                for _ in range(args.steps):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    cache.decode(q, seq, T, out=out, v_mode=vm)
+                    b.record()
+                    times.append((a, b))
+                torch.cuda.synchronize()
+                res.append(statistics.median(x.elapsed_time(y) for x, y in times) * 1e3)
+            print(f"| {name} | {wl.batch} | {T} | {res[0]:.1f} | {res[1]:.1f} | "
+                  f"{'token' if res[0] < res[1] else 'dimension'} |", flush=True)
+        del cache, q, out
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -599,9 +651,14 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="decode time on every synthetic workload (a table, not the bench line)")
     ap.add_argument("--only", default="", help="sweep: workloads whose name contains this")
+    ap.add_argument("--crossover", action="store_true",
+                    help="token- against dimension-parallel decode on natural-layout caches (a table)")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.crossover:
+        run_crossover(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -1105,9 +1105,9 @@ int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len) {
     // per KV head) or 1 (8) CTAs per SM on 152 SMs
     int cap = grid_cap(d);
     if (cap <= 0) cap = (d->group <= 4 ? TQ_TILE_MINB : 1) * 152;
-    // at least 4 tiles per warp of a CTA on average
+    // one wave of resident CTAs, each warp with at least one tile
     const long long tiles = (long long)d->batch * d->n_kv_heads * ((max_seq_len + kTok - 1) / kTok);
-    long long g = (tiles + 4 * kNW - 1) / (4 * kNW);
+    long long g = (tiles + kNW - 1) / kNW;
     if (g > cap) g = cap;
     if (g > kMaxGrid) g = kMaxGrid;
     return g < 1 ? 1 : (int)g;

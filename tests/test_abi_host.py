@@ -157,7 +157,7 @@ def test_decode_plan_host_only(tqlib):
     assert tq.tq_cache_bytes(d2, tq.TQ_PART_V_NORMS) == 32 * 8 * 8192 * 2
     assert tq.tq_decode_plan(d2, 8190) == (304, tq.TQ_VMODE_TENSOR)
     sp, vm = tq.tq_decode_plan(d, 100)
-    assert vm == tq.TQ_VMODE_TENSOR and sp == 56                        # 1792 tiles, 32 per CTA
+    assert vm == tq.TQ_VMODE_TENSOR and sp == 224                       # 1792 tiles, 8 per CTA (one a warp)
     assert tq.tq_decode_plan(d, 100, tq.TQ_VMODE_TENSOR, 7) == (7, tq.TQ_VMODE_TENSOR)
     # natural layout (16 query heads per KV head): token-parallel when short
     d3 = tq.tq_cache_desc_init(128, 32, 2, 32, 8190, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
