@@ -231,7 +231,7 @@ def accuracy_stats(tq, wl, T, inp, cache, out, pairs):
         for which in ("k", "v"):
             enc = oracle_encode(st, which, b, h, 0, T)
             spec = st.specs[h][0 if which == "k" else 1]
-            rec = pair_records(cache, which, b, h)[:T]
+            rec = pair_records(cache, which, b, h, st)[:T]
             nb_, n_, f1, f2, _ = compare_codes(rec, enc, spec)
             nbad, ntot = nbad + nb_, ntot + n_
             fw.append(f1)
@@ -530,6 +530,27 @@ def library_setup(tq, wl, inp, t_capacity):
     return desc, blob
 
 
+def _cold_launch_us(torch, flush, launch, steps):
+    """Median device time of one launch with a cold L2: each timed launch follows
+    a write of a buffer larger than L2, then a device-side wait of about 50 us so
+    that the host has queued the start event and the launch before the device
+    reaches them (the interval then holds the kernel alone, not the host's
+    submission latency).  CUDA events on the current stream."""
+    for _ in range(3):
+        launch()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(100_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) for x, y in times) * 1e3
+
+
 def run_sweep(args):
     """Decode time on every synthetic workload (not the bench line): one cache
     filled by a whole-prompt append, the library's plan, L2 flushed before each
@@ -563,20 +584,9 @@ def run_sweep(args):
         seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
         out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
         splits, vmode = tq.tq_decode_plan(desc, T, tq.TQ_VMODE_AUTO, args.splits)
-        for _ in range(3):
-            cache.decode(q, seq, T, out=out, n_splits=args.splits)
-        times = []
-        for _ in range(args.steps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            cache.decode(q, seq, T, out=out, n_splits=args.splits)
-            b.record()
-            times.append((a, b))
-        torch.cuda.synchronize()
+        us = _cold_launch_us(torch, flush, lambda: cache.decode(q, seq, T, out=out, n_splits=args.splits), args.steps)
         if int(cache.status.item()) != 0:
             raise RuntimeError(f"device status {int(cache.status.item())}")
-        us = statistics.median(x.elapsed_time(y) for x, y in times) * 1e3
         nbytes = step_bytes(wl, T, desc)["decode"]
         gbs = nbytes / (us * 1e-6) / 1e9
         print(f"| {wl.name} | {wl.batch} | {T} | {splits}, {vmode} | {us:.1f} | {gbs:.0f} | {100 * gbs / peak:.1f} % |",
@@ -587,8 +597,8 @@ def run_sweep(args):
 
 def run_crossover(args):
     """Token- against dimension-parallel V accumulation on the caches that use those
-    kernels (natural layout: mixed-rate keys, 16 query heads per KV head, fp32 norms
-    with 32-wide blocks): decode time of each kernel over a range of lengths (one
+    kernels (natural layout: 16 query heads per KV head, fp32 norms with mixed-rate
+    keys or with 32-wide blocks): decode time of each kernel over a range of lengths (one
     cache per workload filled to its longest length, the same launches as the sweep)."""
     import torch
 
@@ -598,7 +608,8 @@ def run_crossover(args):
     dev = torch.device("cuda", 0)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     lengths = [64, 128, 256, 384, 512, 768, 1024, 2048, 4096]
-    cases = [W.mixed_rate_long(seq_len=max(lengths)), W.llama8b_decode(seq_len=max(lengths), batch=8).with_(n_kv_heads=2),
+    cases = [W.mixed_rate_long(seq_len=max(lengths)).with_(norm_dtype=W.F32),
+             W.llama8b_decode(seq_len=max(lengths), batch=8).with_(n_kv_heads=2),
              W.block32(3, seq_len=max(lengths), batch=8).with_(norm_dtype=W.F32)]
     print("| workload | B | T | token-parallel us | dimension-parallel us | faster |")
     print("|---|---|---|---|---|---|")
@@ -614,23 +625,13 @@ def run_crossover(args):
         del K, V
         q = _to_torch(torch, inp.q, wl.in_dtype, dev)
         out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
-        name = wl.name + ("" if wl.mixed_k else f" (G={wl.group}, {'fp32' if wl.norm_dtype == W.F32 else 'fp16'} norms)")
+        name = wl.name + f" (G={wl.group}, {'fp32' if wl.norm_dtype == W.F32 else 'fp16'} norms)"
         for T in lengths:
             seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
             res = []
             for vm in (tq.TQ_VMODE_TOKEN_PARALLEL, tq.TQ_VMODE_DIM_PARALLEL):
-                for _ in range(3):
-                    cache.decode(q, seq, T, out=out, v_mode=vm)
-                times = []
-                for _ in range(args.steps):
-                    flush.zero_()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record()
-                    cache.decode(q, seq, T, out=out, v_mode=vm)
-                    b.record()
-                    times.append((a, b))
-                torch.cuda.synchronize()
-                res.append(statistics.median(x.elapsed_time(y) for x, y in times) * 1e3)
+                res.append(_cold_launch_us(torch, flush, lambda: cache.decode(q, seq, T, out=out, v_mode=vm),
+                                           args.steps))
             print(f"| {name} | {wl.batch} | {T} | {res[0]:.1f} | {res[1]:.1f} | "
                   f"{'token' if res[0] < res[1] else 'dimension'} |", flush=True)
         del cache, q, out

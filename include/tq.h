@@ -125,8 +125,9 @@ typedef int32_t tq_status;
  *   k_codes, v_codes  k_code_bytes / v_code_bytes per position, uint8
  *   k_norms, v_norms  k_norm_slots / v_norm_slots per position, norm_dtype
  *
- * TQ_LAYOUT_NATURAL (mixed-rate keys, or more than 8 query heads per KV head,
- * or fp32 norms with WHT32): position t holds the record and norms of token t.
+ * TQ_LAYOUT_NATURAL (more than 8 query heads per KV head, or fp32 norms with
+ * four slots: WHT32 or mixed-rate keys): position t holds the record and norms
+ * of token t.
  *
  * TQ_LAYOUT_TILE16 (every other cache): positions come in tiles of 16; tile j of
  * a (batch, KV head) holds tokens 16j .. 16j+15 in 16 * code_bytes bytes of codes
@@ -151,6 +152,9 @@ typedef int32_t tq_status;
  *           lane g = s-12 (q-6) of the token's three words: field bits 0-1 in
  *           bits 6-7 of the first word's byte, bits 2-3 in bits 2-3 of the
  *           second's, bits 4-5 in bits 6-7 of the third's.
+ *   mixed-rate keys: the 4-bit key layout, with a b-bit code c of a group of
+ *           width b < 4 stored as c + 2^b (so its nibble, 2-3, 4-7 or 8-15,
+ *           names its width); codes of the 4-bit group are stored as they are.
  *   norms:  one slot: token t at element 2(t&7) + (t>>3) of the tile; four
  *           slots: keys (2(t&7) + (t>>3))*4 + b, values
  *           ((((t&7)>>1)*2 + (t>>3))*4 + b)*2 + (t&1).

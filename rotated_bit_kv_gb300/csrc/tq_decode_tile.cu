@@ -1,6 +1,8 @@
 // Tensor-core decode attention on the 16-token tile layout (tq_tile.cuh): 3- or
 // 4-bit codes, one 128-wide rotation segment (WHT128, SO(4) o WHT128) or four
-// 32-wide blocks with a norm each (WHT32), up to 8 query heads per KV head.
+// 32-wide blocks with a norm each (WHT32), or mixed-rate keys (up to four
+// same-width groups with a norm each) over uniform values; up to 8 query heads
+// per KV head.
 //
 // [RotaryQuant] Key design 3 and [TQ-MNN] §3.3: the QK dot products and the V
 // accumulation run in the rotated domain directly on the packed codes; q is
@@ -33,6 +35,7 @@
 #include <stddef.h>
 
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "tq_decode_common.cuh"
@@ -56,24 +59,12 @@ constexpr uint32_t kTabShared = 1024;
 #ifndef TQ_TILE_LAZYMAX
 #define TQ_TILE_LAZYMAX 1
 #endif
-#ifndef TQ_TILE_BQSMEM
-#define TQ_TILE_BQSMEM 0
-#endif
-#ifndef TQ_TILE_DEPTH
-#define TQ_TILE_DEPTH 1   // tiles a warp has in flight ahead of the one it processes (1 or 2)
-#endif
-#ifndef TQ_TILE_PIPE
-#define TQ_TILE_PIPE 0
-#endif
-#ifndef TQ_TILE_VHOIST
-#define TQ_TILE_VHOIST 0
-#endif
 #ifndef TQ_TILE_QKCH
 #define TQ_TILE_QKCH 2   // QK accumulator chains of the one-norm formats (2 or 4)
 #endif
 
-template <int GPE>
-constexpr int pieces_per_round() { return GPE <= 4 ? 8 : 2; }
+template <int GPE, bool KMIX>
+constexpr int pieces_per_round() { return (GPE <= 4 && !KMIX) ? 8 : 2; }
 
 // A piece: tiles [t_lo, t_hi) of pair (b, h) whose sequence has L tokens.  Its
 // partial goes to slot `slot`; the pair's partials are slots [first, first + parts).
@@ -81,24 +72,38 @@ struct Seg {
     int b, h, L, t_lo, t_hi, slot, first, parts;
 };
 
-template <int GPE>
+template <int GPE, bool KMIX>
 struct TileSmem {
-    static constexpr int NP = pieces_per_round<GPE>();
+    static constexpr int NP = pieces_per_round<GPE, KMIX>();
+    static constexpr int NT = GPE / 4;
     uint32_t tab[256 * 64];      // row e: 32 lane columns of table X, then 32 of table Y
-    float qts[NP][GPE][128];     // rotated queries of the round's pieces (log2 units)
-#if TQ_TILE_BQSMEM
-    uint32_t bqs[NP][GPE / 4][8][32][2];   // QK operand B per piece, head group, k step, lane
-#endif
-    float wo[kNW][GPE][128];     // warp states
+    // mixed-rate keys: the key tables (KX: the 1..3-bit groups, KY: the 4-bit
+    // group), 64 KB above the value tables; the QK operand B of each (k step,
+    // group) of the current piece; the groups each k step touches (bit 4 st + s)
+    uint32_t ktab[KMIX ? 256 * 64 : 1];
+    std::conditional_t<KMIX, uint2[1][8][4][NT][32], uint2[1]> bm;
+    uint32_t kmask[1];
+    alignas(16) float qts[NP][GPE][128];     // rotated queries of the round's pieces (log2 units)
+    alignas(16) float wo[kNW][GPE][128];     // warp states (float2 stores)
     float wm[kNW][8], wl[kNW][8];
-    float ot[8][128];
+    alignas(16) float ot[8][128];
     float mm[8], ll[8];
-    float pm[8], pl[8];          // merge of a pair's pieces: max and sum per head
     Seg seg[NP + 1];
     long long scan[kNW];
     long long b_base, next_pos, cur_base;
-    int b_first, cur_b, nseg, is_last;
+    int b_first, cur_b, nseg;
+    int last[NP];                // this CTA published the last partial of piece k's pair
 };
+
+// the key tables sit 64 KB above the value tables (the lookups put the block in
+// address byte 2); float2 / float4 accesses need the 16-byte alignment
+using SmemMix1 = TileSmem<4, true>;
+using SmemMix2 = TileSmem<8, true>;
+using SmemUni1 = TileSmem<4, false>;
+static_assert(offsetof(SmemMix1, ktab) == 65536 && offsetof(SmemMix2, ktab) == 65536,
+              "key tables must follow the value tables");
+static_assert(offsetof(SmemUni1, wo) % 16 == 0 && offsetof(SmemMix2, wo) % 16 == 0,
+              "warp state rows must be 16-byte aligned");
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
@@ -210,10 +215,35 @@ __device__ __forceinline__ uint32_t lk(uint32_t addr) {
 }
 
 // table word of byte K of w: the byte goes to bits 8-15, the lane's column
-// offset (4 lane, + 128 for table Y) comes from byte 0 of `col`
+// offset (4 lane, + 128 for table Y) comes from byte 0 of `col` and the table
+// block (0: values, 1: mixed-rate keys, 64 KB above) from byte 2
 template <int K>
 __device__ __forceinline__ uint32_t lkb(uint32_t w, uint32_t col) {
-    return lk(prmt(w, col, 0x5504u | (K << 4)));
+    return lk(prmt(w, col, 0x7604u | (K << 4)));
+}
+
+// Key tables of mixed-rate keys, for the head whose parameters are P.  In the
+// tile layout a b-bit code c of the 1..3-bit groups is stored as c + 2^b, so the
+// two nibbles of a byte tell its width: 2-3 (1 bit), 4-7 (2 bits), 8-15 (3
+// bits).  Row e of KX holds (s_g c_g[lo], s_g c_g[hi]) for the group g both
+// nibbles name; KY holds the pairs of the 4-bit group (codes stored as is).
+__device__ __forceinline__ void build_ktable(const tq_head_params& P, uint32_t* ktab) {
+    for (int i = threadIdx.x; i < 256 * 16; i += kNThr) {
+        const int e = i >> 4, part = i & 15;
+        const int lo = e & 15, hi = e >> 4;
+        uint32_t v = 0u;
+        if (part >= 8) {
+            v = pack_h2(P.k_h_scale[3] * P.k_cent[3][lo], P.k_h_scale[3] * P.k_cent[3][hi]);
+        } else {
+            const int g = lo >= 8 ? 2 : lo >= 4 ? 1 : lo >= 2 ? 0 : -1;
+            const int gh = hi >= 8 ? 2 : hi >= 4 ? 1 : hi >= 2 ? 0 : -1;
+            if (g >= 0 && g == gh) {
+                const int off = 2 << g;
+                v = pack_h2(P.k_h_scale[g] * P.k_cent[g][lo - off], P.k_h_scale[g] * P.k_cent[g][hi - off]);
+            }
+        }
+        reinterpret_cast<uint4*>(ktab)[i] = make_uint4(v, v, v, v);
+    }
 }
 
 // Table words of a three-word group of 3-bit codes: o[4 w + k] for byte k of word
@@ -244,6 +274,18 @@ __device__ __forceinline__ void group4(uint32_t w0, uint32_t w1, uint32_t w2, ui
         o[4 + k] = lkb<k>(w1, cx);
         o[8 + k] = lkb<k>(w2, cx);
         o[12 + k] = lkb<k>(w3, cx);
+    });
+}
+
+// ... of a four-word group of mixed-rate key codes, field f through column col[f]
+__device__ __forceinline__ void group4m(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                        const uint32_t (&col)[16], uint32_t (&o)[16]) {
+    unroll<4>([&](auto k_c) {
+        constexpr int k = decltype(k_c)::value;
+        o[k] = lkb<k>(w0, col[k]);
+        o[4 + k] = lkb<k>(w1, col[4 + k]);
+        o[8 + k] = lkb<k>(w2, col[8 + k]);
+        o[12 + k] = lkb<k>(w3, col[12 + k]);
     });
 }
 
@@ -307,16 +349,18 @@ struct PairPtr {
     const uint8_t* vn;
 };
 
-template <int BITS, int NSEG>
+// KB / KN: key code bits (4 for the nibble containers of mixed-rate keys) and
+// key norm slots; VB / VN: the same for the values.
+template <int KB, int KN, int VB, int VN>
 __device__ __forceinline__ PairPtr pair_ptr(const DecodeArgs& a, int b, int h) {
     const size_t pair = (size_t)b * a.Hkv + h;
     const size_t tiles = (size_t)(a.Tcap / kTok);   // Tcap here is the allocated (tile-rounded) length
     const int nb = a.norm_f16 ? 2 : 4;
     PairPtr p;
-    p.k = a.k_codes + pair * tiles * tqtile::tile_bytes(BITS);
-    p.v = a.v_codes + pair * tiles * tqtile::tile_bytes(BITS);
-    p.kn = static_cast<const uint8_t*>(a.k_norms) + pair * tiles * kTok * NSEG * nb;
-    p.vn = static_cast<const uint8_t*>(a.v_norms) + pair * tiles * kTok * NSEG * nb;
+    p.k = a.k_codes + pair * tiles * tqtile::tile_bytes(KB);
+    p.v = a.v_codes + pair * tiles * tqtile::tile_bytes(VB);
+    p.kn = static_cast<const uint8_t*>(a.k_norms) + pair * tiles * kTok * KN * nb;
+    p.vn = static_cast<const uint8_t*>(a.v_norms) + pair * tiles * kTok * VN * nb;
     return p;
 }
 
@@ -397,21 +441,12 @@ struct WState {
 __device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
 __device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
 
-// The QK operand B of a lane: in registers, or (TQ_TILE_BQSMEM) read from the
-// piece's fragment table in shared memory at each k step.
-#if TQ_TILE_BQSMEM
-template <int NT>
-struct BqT {
-    const uint2* base;   // [NT][8][32] fragments of this piece, + lane
-    __device__ __forceinline__ uint2 get(int j, int st) const { return base[(j * 8 + st) * 32]; }
-};
-#else
+// The QK operand B of a lane (uniform-rate keys), in registers.
 template <int NT>
 struct BqT {
     uint32_t r[NT][8][2];
     __device__ __forceinline__ uint2 get(int j, int st) const { return make_uint2(r[j][st][0], r[j][st][1]); }
 };
-#endif
 
 // fp16 pair of (x, y) (hi = false) or of what the fp16 rounding of (x, y) leaves
 // (hi = true gives the rounded pair itself)
@@ -508,6 +543,61 @@ __device__ __forceinline__ void qk_phase(const KRegs<BITS, NSEG>& kd, const Lane
     }
 }
 
+// QK of one tile of mixed-rate keys.  Group s of the head (the 2^(s+1)-level
+// codes) accumulates in chain s over the k steps it touches (bit 4 st + s of
+// `mask`); the operand B of (k step st, group s) holds q~ on the group's
+// coordinates over the group's table scale, zero elsewhere (bm: this lane's
+// entry of [st][s][head group j] for the piece).  Each chain is weighed by the
+// token's norm of its group [Block-GTQ, per-group norms].  colpack: the lane's
+// key-table column per field (byte f & 3 of word f >> 2; + 128 for table KY).
+template <int NT>
+__device__ __forceinline__ void qk_phase_mix(const KRegs<4, 4>& kd, const uint32_t (&colpack)[4], const uint2* bm,
+                                             uint32_t mask, float (&s0)[NT], float (&s8)[NT]) {
+    float acc[NT][4][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q][0] = acc[j][q][1] = acc[j][q][2] = acc[j][q][3] = 0.f;
+    {
+        uint32_t col[16];
+        unroll<16>([&](auto f_c) {
+            constexpr int f = decltype(f_c)::value;
+            // byte f & 3 of the field's word, key-table block 1 in byte 2
+            col[f] = prmt(colpack[f >> 2], 0x00010000u, 0x7640u | (f & 3));
+        });
+        uint32_t kr[16], k8[16];
+        group4m(kd.k[0], kd.k[1], kd.k[2], kd.k[3], col, kr);
+        group4m(kd.k[4], kd.k[5], kd.k[6], kd.k[7], col, k8);
+        unroll<8>([&](auto st_c) {
+            constexpr int st = decltype(st_c)::value;
+            unroll<4>([&](auto g_c) {
+                constexpr int g = decltype(g_c)::value;
+                if (mask & (1u << (4 * st + g))) {
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const uint2 b = bm[((st * 4 + g) * NT + j) * 32];
+                        mma16816(acc[j][g], kr[2 * st], k8[2 * st], kr[2 * st + 1], k8[2 * st + 1], b.x, b.y);
+                    }
+                }
+            });
+        });
+    }
+    float n0[4], n8[4];
+    n0[0] = h_lo(kd.kn[0]); n0[1] = h_hi(kd.kn[0]); n0[2] = h_lo(kd.kn[1]); n0[3] = h_hi(kd.kn[1]);
+    n8[0] = h_lo(kd.kn[2]); n8[1] = h_hi(kd.kn[2]); n8[2] = h_lo(kd.kn[3]); n8[3] = h_hi(kd.kn[3]);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {   // per group: rounded q~ and its remainder, then the group's norm
+        float a0 = n0[0] * (acc[j][0][0] + acc[j][0][1]), a8 = n8[0] * (acc[j][0][2] + acc[j][0][3]);
+#pragma unroll
+        for (int g = 1; g < 4; ++g) {
+            a0 = fmaf(n0[g], acc[j][g][0] + acc[j][g][1], a0);
+            a8 = fmaf(n8[g], acc[j][g][2] + acc[j][g][3], a8);
+        }
+        s0[j] = a0;
+        s8[j] = a8;
+    }
+}
+
 // Online softmax and PV of one tile of `nval` valid tokens (past-the-end tokens of
 // a short last tile take no weight), from its scores.
 template <int NT, int BITS, int NSEG>
@@ -521,9 +611,6 @@ __device__ __forceinline__ void pv_phase(const VRegs<BITS, NSEG>& td, float (&s0
         if constexpr (BITS == 3) group3(td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], ln.cx, ln.cy, vg[u]);
         else group4(td.v[W * u], td.v[W * u + 1], td.v[W * u + 2], td.v[W * u + 3], ln.cx, vg[u]);
     };
-#if TQ_TILE_VHOIST
-    unroll<2>(vlookups);   // value operands first: they depend on nothing of the softmax
-#endif
     const bool in0 = r < nval, in8 = r + 8 < nval;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -600,9 +687,7 @@ __device__ __forceinline__ void pv_phase(const VRegs<BITS, NSEG>& td, float (&s0
     // ---- PV: group u of the values holds tokens 2c + 8u (A) and 2c + 1 + 8u (B)
     unroll<2>([&](auto u_c) {
         constexpr int u = decltype(u_c)::value;
-#if !TQ_TILE_VHOIST
         vlookups(u_c);
-#endif
         // four blocks: each m tile is one block; its value norms scale the P operand
         uint32_t wa[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};
         (void)wa;
@@ -679,63 +764,78 @@ __device__ __forceinline__ void merge_warps(const float (*wo)[GPE][128], const f
 
 // Log-sum-exp merge of `parts` published partials (rows [part t][head g] of
 // kPartStride floats: o~[128], m, l) into ot[g][0..127], normalised  [Block-GTQ].
-// A warp per head finds M_g = max_t m_t and L_g = sum_t 2^(m_t - M_g) l_t (into
-// pm, pl); then each thread accumulates four coordinates of one head over the
-// parts.  Empty parts (m = -inf) weigh 0; a pair with no tokens gives 0.
+// The partials sit in L2, a round trip away, so the merge is one online sweep:
+// thread (g, d4) takes four coordinates of head g and, per batch of MB parts,
+// issues all of the batch's loads (m_t, l_t and its o~ quadruple) at once, then
+// moves its running maximum M to the batch's and folds the batch in:
+//   acc = 2^(M_old - M) acc + sum_t 2^(m_t - M) o~_t,  L likewise with l_t.
+// Empty parts (m = -inf) weigh 0; a pair with no tokens gives 0.
 template <int GP>
-__device__ __forceinline__ void merge_pieces(const float* base, int parts, float (*ot)[128], float* pm, float* pl) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int g = warp; g < GP; g += kNW) {
-        float M = -INFINITY;
-        for (int t = lane; t < parts; t += 32) M = fmaxf(M, __ldcg(base + ((size_t)t * GP + g) * kPartStride + 128));
+__device__ __forceinline__ void merge_pieces(const float* base, int parts, float (*ot)[128]) {
+    static_assert(GP * 32 <= kNThr, "one coordinate quadruple per thread");
+    constexpr int MB = GP <= 4 ? 8 : 16;   // parts in flight (the 4-head kernels' register budget)
+    const int tid = threadIdx.x, g = tid >> 5, d4 = tid & 31;
+    if (g >= GP) return;
+    const float* pr = base + (size_t)g * kPartStride;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = 0; t < parts; t += MB) {
+        float4 v[MB];
+        float2 ml[MB];
 #pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(TQ_FULL_MASK, M, o));
-        float L = 0.f;
-        for (int t = lane; t < parts; t += 32) {
-            const float* pr = base + ((size_t)t * GP + g) * kPartStride;
-            const float mt = __ldcg(pr + 128);
-            L = fmaf(mt == -INFINITY ? 0.f : exp2f(mt - M), __ldcg(pr + 129), L);
+        for (int u = 0; u < MB; ++u) {
+            const float* row = pr + (size_t)(t + u) * GP * kPartStride;
+            const bool in = t + u < parts;
+            v[u] = in ? __ldcg(reinterpret_cast<const float4*>(row) + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ml[u] = in ? __ldcg(reinterpret_cast<const float2*>(row + 128)) : make_float2(-INFINITY, 0.f);
         }
+        float Mb = M;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(TQ_FULL_MASK, L, o);
-        if (lane == 0) {
-            pm[g] = M;
-            pl[g] = L;
+        for (int u = 0; u < MB; ++u) Mb = fmaxf(Mb, ml[u].x);
+        if (Mb == -INFINITY) continue;   // nothing but empty parts so far
+        const float cf = M == -INFINITY ? 0.f : exp2f(M - Mb);
+        L *= cf;
+        acc.x *= cf; acc.y *= cf; acc.z *= cf; acc.w *= cf;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+            const float w = ml[u].x == -INFINITY ? 0.f : exp2f(ml[u].x - Mb);
+            L = fmaf(w, ml[u].y, L);
+            acc.x = fmaf(w, v[u].x, acc.x);
+            acc.y = fmaf(w, v[u].y, acc.y);
+            acc.z = fmaf(w, v[u].z, acc.z);
+            acc.w = fmaf(w, v[u].w, acc.w);
         }
+        M = Mb;
     }
-    __syncthreads();
-    for (int i = tid; i < GP * 32; i += kNThr) {
-        const int g = i >> 5, d4 = i & 31;
-        const float M = pm[g];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int t = 0; t < parts; ++t) {
-            const float* pr = base + ((size_t)t * GP + g) * kPartStride;
-            const float mt = __ldcg(pr + 128);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(pr) + d4);
-            const float w = mt == -INFINITY ? 0.f : exp2f(mt - M);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
-        }
-        const float L = pl[g];
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        ot[g][4 * d4] = acc.x * inv;
-        ot[g][4 * d4 + 1] = acc.y * inv;
-        ot[g][4 * d4 + 2] = acc.z * inv;
-        ot[g][4 * d4 + 3] = acc.w * inv;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    ot[g][4 * d4] = acc.x * inv;
+    ot[g][4 * d4 + 1] = acc.y * inv;
+    ot[g][4 * d4 + 2] = acc.z * inv;
+    ot[g][4 * d4 + 3] = acc.w * inv;
+}
+
+// o = R_V^T o~ for the pair's query heads from ot (normalised), into out
+// [RotaryQuant Key design 3, Kernel D]
+__device__ __forceinline__ void store_out(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const Seg& sg) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int g = warp; g < a.G; g += kNW) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ot[g][4 * lane + i];
+        tq::rotate_inverse(a.rot, P, v);
+        float4* o4 = reinterpret_cast<float4*>(a.out + ((size_t)sg.b * a.Hq + (size_t)sg.h * a.G + g) * 128) + lane;
+        *o4 = make_float4(v[0], v[1], v[2], v[3]);
     }
 }
 
 // Finish a piece: ot[g][c] holds its unnormalised o~, (mm[g], ll[g]) its softmax
-// state (shared memory).  One part: normalise and write; else publish the partial
-// and let the last CTA of the pair merge all of them.
+// state (shared memory).  One part: normalise, rotate back and write.  Else
+// publish the partial and take a ticket; *last tells whether this CTA's partial
+// was the pair's last (its merge comes after the CTA's other pieces of the round).
 template <int GP>
 __device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const float* mm,
-                             const float* ll, float* pm, float* pl, int* is_last, const Seg& sg) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int pair = sg.b * a.Hkv + sg.h;
+                             const float* ll, int* last, const Seg& sg) {
+    const int tid = threadIdx.x;
     if (sg.parts > 1) {
         float* part = a.ws_part + (size_t)sg.slot * GP * kPartStride;
         for (int i = tid; i < GP * 128; i += kNThr) part[(i >> 7) * kPartStride + (i & 127)] = ot[i >> 7][i & 127];
@@ -746,32 +846,29 @@ __device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float
         __threadfence();
         __syncthreads();
         if (tid == 0) {
-            const int ticket = atomicAdd(a.tickets + pair, 1);
-            *is_last = ticket == sg.parts - 1;
+            const int ticket = atomicAdd(a.tickets + sg.b * a.Hkv + sg.h, 1);
+            *last = ticket == sg.parts - 1;
         }
-        __syncthreads();
-        if (!*is_last) return;
-        __threadfence();
-        // log-sum-exp merge over the pair's parts  [Block-GTQ]
-        merge_pieces<GP>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot, pm, pl);
-        if (tid == 0) a.tickets[pair] = 0;   // ready for the next call
-        __syncthreads();
     } else {
         for (int i = tid; i < GP * 128; i += kNThr) {
             const int g = i >> 7;
             ot[g][i & 127] = ll[g] > 0.f ? ot[g][i & 127] / ll[g] : 0.f;
         }
         __syncthreads();
+        store_out(a, P, ot, sg);
+        if (tid == 0) *last = 0;
     }
-    // o = R_V^T o~, once per query head  [RotaryQuant Key design 3, Kernel D]
-    for (int g = warp; g < a.G; g += kNW) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = ot[g][4 * lane + i];
-        tq::rotate_inverse(a.rot, P, v);
-        float4* o4 = reinterpret_cast<float4*>(a.out + ((size_t)sg.b * a.Hq + (size_t)sg.h * a.G + g) * 128) + lane;
-        *o4 = make_float4(v[0], v[1], v[2], v[3]);
-    }
+}
+
+// The merge of a pair whose last partial this CTA published: all partials by
+// log-sum-exp, the ticket reset for the next call, then R_V^T and the write.
+template <int GP>
+__device__ void merge_pair(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const Seg& sg) {
+    __threadfence();
+    merge_pieces<GP>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot);
+    if (threadIdx.x == 0) a.tickets[sg.b * a.Hkv + sg.h] = 0;   // ready for the next call
+    __syncthreads();
+    store_out(a, P, ot, sg);
 }
 
 // q~ = R_K q of head g of pair (b, h) into dst[128] (log2 units); one warp
@@ -786,6 +883,93 @@ __device__ __forceinline__ void rotate_q(const DecodeArgs& a, const tq_head_para
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[4 * lane + i] = v[i] * (kLog2e * kInvSqrtD);
+}
+
+// Mixed-rate keys: q~ = R_K q for every query head of the round's nseg pieces,
+// R_K the head's block-diagonal matrix of group rotations over the grouped
+// coordinates [Block-GTQ, physical encoding and grouping]:
+//   q~[r] = sum over c in r's group of kmat[r][c] q[gcoord[c]].
+// The whole CTA.  One round trip of loads: the raw queries into qts, each piece's
+// gcoord into gco, the first piece's matrix (16 float4 per thread) staged
+// transposed in kt (kt[c][r]: conflict-free reads).  Then the queries gathered
+// into group order in xg ([piece][c][head]), and row r of each piece formed by
+// two threads, each over half of r's group.
+template <int GPE>
+__device__ __forceinline__ void stage_kmat(const DecodeArgs& a, int h, float* kt) {
+    const int tid = threadIdx.x;
+    const float4* km = reinterpret_cast<const float4*>(a.kmat + (size_t)h * 128 * 128);
+    constexpr int PER = 128 * 32 / kNThr;
+    float4 v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int i = tid + u * kNThr;
+        v[u] = __ldg(km + (size_t)(i & 127) * 32 + (i >> 7));   // row i & 127, columns 4 (i >> 7) ..
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int i = tid + u * kNThr, r = i & 127, c4 = i >> 7;
+        kt[(4 * c4) * 128 + r] = v[u].x;
+        kt[(4 * c4 + 1) * 128 + r] = v[u].y;
+        kt[(4 * c4 + 2) * 128 + r] = v[u].z;
+        kt[(4 * c4 + 3) * 128 + r] = v[u].w;
+    }
+}
+
+template <int GPE>
+__device__ __forceinline__ void rotate_q_mix(const DecodeArgs& a, const Seg* seg, int nseg, float (*qts)[GPE][128],
+                                             float* xg, int* gco, float* kt) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = warp; i < nseg * GPE; i += kNW) {
+        const Seg& sg = seg[i / GPE];
+        const int g = i % GPE;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (g < a.G) tq::load4(a.q, ((size_t)sg.b * a.Hq + (size_t)sg.h * a.G + g) * 128 + 4 * lane, a.q_dtype, v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qts[i / GPE][g][4 * lane + e] = v[e];
+    }
+    for (int i = tid; i < nseg * 128; i += kNThr) gco[i] = a.params[seg[i >> 7].h].k_gcoord[i & 127];
+    stage_kmat<GPE>(a, seg[0].h, kt);
+    int staged = seg[0].h;
+    __syncthreads();
+    for (int i = tid; i < nseg * 128 * GPE; i += kNThr) {
+        const int g = i % GPE, c = (i / GPE) & 127, kk = i / (GPE * 128);
+        xg[i] = qts[kk][g][gco[kk * 128 + c]];
+    }
+    __syncthreads();
+    for (int kk = 0; kk < nseg; ++kk) {
+        const int h = seg[kk].h;
+        const tq_head_params& P = a.params[h];
+        if (h != staged) {
+            stage_kmat<GPE>(a, h, kt);
+            staged = h;
+            __syncthreads();
+        }
+        const int r = tid & 127, half = tid >> 7;   // kNThr = 256: two threads per row
+        int sr = 0;
+        while (sr < 3 && r >= P.k_seg_start[sr + 1]) ++sr;
+        const int g0 = P.k_seg_start[sr], g1 = P.k_seg_start[sr + 1];
+        const int mid = g0 + ((g1 - g0) >> 1);
+        const int c0 = half ? mid : g0, c1 = half ? g1 : mid;
+        float acc[GPE];
+#pragma unroll
+        for (int g = 0; g < GPE; ++g) acc[g] = 0.f;
+        for (int c = c0; c < c1; ++c) {
+            const float kv = kt[c * 128 + r];
+            const float* x0 = xg + ((size_t)kk * 128 + c) * GPE;
+#pragma unroll
+            for (int g = 0; g < GPE; ++g) acc[g] = fmaf(kv, x0[g], acc[g]);
+        }
+        if (half) {
+#pragma unroll
+            for (int g = 0; g < GPE; ++g) qts[kk][g][r] = acc[g];
+        }
+        __syncthreads();
+        if (!half) {
+#pragma unroll
+            for (int g = 0; g < GPE; ++g) qts[kk][g][r] = (acc[g] + qts[kk][g][r]) * (kLog2e * kInvSqrtD);
+        }
+        __syncthreads();   // the rows of this piece are complete; kt may be restaged
+    }
 }
 
 // clamped length of batch b's sequences (flags raised when asked)
@@ -805,14 +989,19 @@ __device__ __forceinline__ int seq_len_of(const DecodeArgs& a, int b, bool repor
 #ifdef TQ_TILE_MAXNREG
 #define TQ_TILE_BOUNDS __maxnreg__(TQ_TILE_MAXNREG)
 #else
-#define TQ_TILE_BOUNDS __launch_bounds__(kNThr, NT == 1 ? TQ_TILE_MINB : 1)
+#define TQ_TILE_BOUNDS __launch_bounds__(kNThr, (NT == 1 && !KMIX) ? TQ_TILE_MINB : 1)
 #endif
-template <int NT, int BITS, int NSEG>
+// NT: groups of four query heads; BITS, NSEG: code width and norm segments of the
+// values (and of the keys unless KMIX: mixed-rate keys in nibble containers with
+// four group norms).
+template <int NT, int BITS, int NSEG, bool KMIX>
 __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
     constexpr int GPE = 4 * NT;
-    constexpr int NP = pieces_per_round<GPE>();
+    using Smem = TileSmem<GPE, KMIX>;
+    constexpr int NP = Smem::NP;
+    constexpr int KB = KMIX ? 4 : BITS, KN = KMIX ? 4 : NSEG;
     extern __shared__ __align__(128) unsigned char tile_smem_raw[];
-    TileSmem<GPE>& S = *reinterpret_cast<TileSmem<GPE>*>(tile_smem_raw);
+    Smem& S = *reinterpret_cast<Smem*>(tile_smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // launched as a programmatic dependent of the previous kernel in the stream:
     // nothing is read before that kernel has completed and its writes are visible
@@ -820,18 +1009,20 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
     // the lookups address the table at a fixed shared offset: check it (no static
     // shared memory in this kernel, so the dynamic block starts after the
     // reserved 1 KB); on a mismatch nothing is read or written but the flag
-    if ((uint32_t)__cvta_generic_to_shared(S.tab) != kTabShared) {
+    if ((uint32_t)__cvta_generic_to_shared(S.tab) != kTabShared ||
+        (KMIX && (uint32_t)__cvta_generic_to_shared(S.ktab) != kTabShared + 65536u)) {
         if (tid == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, TQ_DEV_INTERNAL);
         return;
     }
-    build_table<BITS>(a.params[0], S.tab);
     const bool f16n = a.norm_f16 != 0;
 
     // ---- the CTA's range of tile positions: all tiles of all pairs in pair order
+    // (the lengths are read before the table is built, so that both loads overlap)
     const int per = (a.B + kNThr - 1) / kNThr;   // batches summed by each thread, in order
     const int bt0 = min(a.B, tid * per), bt1 = min(a.B, bt0 + per);
     long long loc = 0;
     for (int bb = bt0; bb < bt1; ++bb) loc += (seq_len_of(a, bb, blockIdx.x == 0) + kTok - 1) / kTok;
+    build_table<BITS>(a.params[0], S.tab);
     long long inc = loc;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -918,102 +1109,107 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
         if (nseg == 0) break;
 
         // first keys of the round, in flight while the queries are rotated
-        KRegs<BITS, NSEG> kA, kB;
+        KRegs<KB, KN> kA, kB;
         VRegs<BITS, NSEG> vA, vB;
-        PairPtr pp = pair_ptr<BITS, NSEG>(a, S.seg[0].b, S.seg[0].h);
+        PairPtr pp = pair_ptr<KB, KN, BITS, NSEG>(a, S.seg[0].b, S.seg[0].h);
         bool k_loaded = false;
         if (S.seg[0].t_lo + warp < S.seg[0].t_hi) {
             load_k(kA, pp, S.seg[0].t_lo + warp, ln, f16n);
             k_loaded = true;
         }
-        for (int i = warp; i < nseg * GPE; i += kNW) {
-            const Seg& sg = S.seg[i / GPE];
-            rotate_q(a, a.params[sg.h], sg.b, sg.h, i % GPE, S.qts[i / GPE][i % GPE]);
+        if constexpr (!KMIX) {
+            for (int i = warp; i < nseg * GPE; i += kNW) {
+                const Seg& sg = S.seg[i / GPE];
+                rotate_q(a, a.params[sg.h], sg.b, sg.h, i % GPE, S.qts[i / GPE][i % GPE]);
+            }
+            __syncthreads();
         }
-        __syncthreads();
-#if TQ_TILE_BQSMEM
-        for (int i = tid; i < nseg * NT * 8 * 32; i += kNThr) {   // (piece, head group, k step, lane)
-            const int L = i & 31, st = (i >> 5) & 7, j = (i >> 8) % NT, kk = i / (NT * 256);
-            const int r = L >> 2, c = L & 3;
-            const float* qh = S.qts[kk][4 * j + (r >> 1)];
-            const int d0 = 16 * st + 2 * c, d1 = d0 + 8;
-            S.bqs[kk][j][st][L][0] = pack_part(qh[d0] * kinv, qh[d0 + 1] * kinv, r & 1);
-            S.bqs[kk][j][st][L][1] = pack_part(qh[d1] * kinv, qh[d1 + 1] * kinv, r & 1);
-        }
-        __syncthreads();
-#endif
 
         for (int k = 0; k < nseg; ++k) {
             const Seg sg = S.seg[k];
             const tq_head_params& P = a.params[sg.h];
             BqT<NT> bq;
-#if TQ_TILE_BQSMEM
-            bq.base = reinterpret_cast<const uint2*>(S.bqs[k]) + lane;
-#else
-            load_bq<NT>(S.qts[k], ln, kinv, bq.r);
-#endif
+            uint32_t colpack[4];
+            uint32_t kmask = 0u;
+            const uint2* bmp = nullptr;
+            if constexpr (KMIX) {
+                // per piece (so that a CTA's second piece never delays its first):
+                // q~ of the piece's heads, staging the group rotations in the key
+                // tables' space; the k steps each group touches (warp 0, lane
+                // 4 st + g); operand B of every (k step, group, head group, lane);
+                // then the key tables of the piece's head
+                static_assert(kNThr == 256, "two threads per rotated row");
+                static_assert(kNW * GPE * 128 >= 128 * GPE + 128, "scratch for the gathered queries and gcoord");
+                float* xg = &S.wo[0][0][0];
+                rotate_q_mix<GPE>(a, &S.seg[k], 1, S.qts, xg, reinterpret_cast<int*>(xg + 128 * GPE),
+                                  reinterpret_cast<float*>(S.ktab));
+                if (warp == 0) {
+                    const int st = lane >> 2, g = lane & 3;
+                    const int glo = P.k_seg_start[g] >> 1, ghi = P.k_seg_start[g + 1] >> 1;
+                    const bool touch = ghi > glo && glo < 8 * st + 8 && ghi > 8 * st;
+                    const uint32_t m = __ballot_sync(TQ_FULL_MASK, touch);
+                    if (lane == 0) S.kmask[0] = m;
+                }
+                // lane (r, c) holds head 4j + r/2, coordinates of pairs 8 st + c (b0)
+                // and 8 st + c + 4 (b1) when they lie in group g, as the rounded q~
+                // (r even) or its rounding remainder (r odd), over the group's
+                // table scale
+                for (int i = tid; i < 8 * 4 * NT * 32; i += kNThr) {
+                    const int L = i & 31;
+                    int rest = i >> 5;
+                    const int j = rest % NT;
+                    rest /= NT;
+                    const int g = rest & 3, st = rest >> 2;
+                    const int glo = P.k_seg_start[g] >> 1, ghi = P.k_seg_start[g + 1] >> 1;
+                    const int r = L >> 2, c = L & 3;
+                    const float* qh = S.qts[0][4 * j + (r >> 1)];
+                    const int p0 = 8 * st + c, p1 = p0 + 4;
+                    uint32_t b0 = 0u, b1 = 0u;
+                    if (ghi > glo) {
+                        const float ki = 1.0f / P.k_h_scale[g];
+                        if (p0 >= glo && p0 < ghi) b0 = pack_part(qh[2 * p0] * ki, qh[2 * p0 + 1] * ki, r & 1);
+                        if (p1 >= glo && p1 < ghi) b1 = pack_part(qh[2 * p1] * ki, qh[2 * p1 + 1] * ki, r & 1);
+                    }
+                    S.bm[0][st][g][j][L] = make_uint2(b0, b1);
+                }
+                build_ktable(P, S.ktab);   // rotate_q_mix ended with a barrier: the staging is done
+                __syncthreads();
+                const int p4 = P.k_seg_start[3] >> 1;   // first pair of the 4-bit group
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t x = 0u;
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+                        const int pr = tqtile::k_pair(ln.c, 4 * w + kb);
+                        x |= (4u * lane + (pr >= p4 ? 128u : 0u)) << (8 * kb);
+                    }
+                    colpack[w] = x;
+                }
+                kmask = S.kmask[0];
+                bmp = &S.bm[0][0][0][0][lane];
+            } else {
+                load_bq<NT>(S.qts[k], ln, kinv, bq.r);
+            }
+            (void)colpack;
+            (void)kmask;
+            (void)bmp;
             WState<NT> ws;
             ws.reset();
             // this warp's tiles of the piece: t_lo + warp + kNW i
             const int n = sg.t_hi - sg.t_lo > warp ? (sg.t_hi - sg.t_lo - warp + kNW - 1) / kNW : 0;
             auto tile_at = [&](int i) { return sg.t_lo + warp + kNW * i; };
             auto nval_at = [&](int i) { return min(kTok, sg.L - tile_at(i) * kTok); };
-#if TQ_TILE_PIPE
-            // software pipeline: the QK of tile i + 1 goes before the softmax and PV of
-            // tile i (they are independent); keys of tile i + 2 load as soon as the key
-            // registers of tile i are free, values of tile i + 2 after the PV of tile i
-            if (n > 0) {
-                if (!k_loaded) load_k(kA, pp, tile_at(0), ln, f16n);
-                load_v(vA, pp, tile_at(0), ln, f16n);
-            }
-            if (n > 1) {
-                load_k(kB, pp, tile_at(1), ln, f16n);
-                load_v(vB, pp, tile_at(1), ln, f16n);
-            }
-            float sA0[NT], sA8[NT], sB0[NT], sB8[NT];
-            if (n > 0) qk_phase<NT, BITS, NSEG>(kA, ln, bq, f16n, sA0, sA8);
-            if (n > 2) load_k(kA, pp, tile_at(2), ln, f16n);
-            for (int i = 0; i < n; i += 2) {
-                if (i + 1 < n) qk_phase<NT, BITS, NSEG>(kB, ln, bq, f16n, sB0, sB8);
-                if (i + 3 < n) load_k(kB, pp, tile_at(i + 3), ln, f16n);
-                pv_phase<NT, BITS, NSEG>(vA, sA0, sA8, nval_at(i), ln, f16n, ws);
-                if (i + 2 < n) load_v(vA, pp, tile_at(i + 2), ln, f16n);
-                if (i + 1 >= n) break;
-                if (i + 2 < n) qk_phase<NT, BITS, NSEG>(kA, ln, bq, f16n, sA0, sA8);
-                if (i + 4 < n) load_k(kA, pp, tile_at(i + 4), ln, f16n);
-                pv_phase<NT, BITS, NSEG>(vB, sB0, sB8, nval_at(i + 1), ln, f16n, ws);
-                if (i + 3 < n) load_v(vB, pp, tile_at(i + 3), ln, f16n);
-            }
-#else
             // tile i + 1 loads while tile i is processed
-            auto step = [&](const KRegs<BITS, NSEG>& kd, const VRegs<BITS, NSEG>& vd, int nv) {
+            auto step = [&](const KRegs<KB, KN>& kd, const VRegs<BITS, NSEG>& vd, int nv) {
                 float s0[NT], s8[NT];
-                qk_phase<NT, BITS, NSEG>(kd, ln, bq, f16n, s0, s8);
+                if constexpr (KMIX) qk_phase_mix<NT>(kd, colpack, bmp, kmask, s0, s8);
+                else qk_phase<NT, BITS, NSEG>(kd, ln, bq, f16n, s0, s8);
                 pv_phase<NT, BITS, NSEG>(vd, s0, s8, nv, ln, f16n, ws);
             };
             if (n > 0) {
                 if (!k_loaded) load_k(kA, pp, tile_at(0), ln, f16n);
                 load_v(vA, pp, tile_at(0), ln, f16n);
             }
-#if TQ_TILE_DEPTH == 2
-            // tiles i + 1 and i + 2 in flight while tile i is processed
-            KRegs<BITS, NSEG> kC;
-            VRegs<BITS, NSEG> vC;
-            if (n > 1) {
-                load_k(kB, pp, tile_at(1), ln, f16n);
-                load_v(vB, pp, tile_at(1), ln, f16n);
-            }
-            for (int i = 0; i < n; i += 3) {
-                if (i + 2 < n) { load_k(kC, pp, tile_at(i + 2), ln, f16n); load_v(vC, pp, tile_at(i + 2), ln, f16n); }
-                step(kA, vA, nval_at(i));
-                if (i + 1 >= n) break;
-                if (i + 3 < n) { load_k(kA, pp, tile_at(i + 3), ln, f16n); load_v(vA, pp, tile_at(i + 3), ln, f16n); }
-                step(kB, vB, nval_at(i + 1));
-                if (i + 2 >= n) break;
-                if (i + 4 < n) { load_k(kB, pp, tile_at(i + 4), ln, f16n); load_v(vB, pp, tile_at(i + 4), ln, f16n); }
-                step(kC, vC, nval_at(i + 2));
-            }
-#else
             for (int i = 0; i < n; i += 2) {
                 if (i + 1 < n) {
                     load_k(kB, pp, tile_at(i + 1), ln, f16n);
@@ -1027,13 +1223,11 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
                 }
                 step(kB, vB, nval_at(i + 1));
             }
-#endif
-#endif
             // the next piece's first keys, in flight during the merge
             k_loaded = false;
             if (k + 1 < nseg) {
                 const Seg& sn = S.seg[k + 1];
-                pp = pair_ptr<BITS, NSEG>(a, sn.b, sn.h);
+                pp = pair_ptr<KB, KN, BITS, NSEG>(a, sn.b, sn.h);
                 if (sn.t_lo + warp < sn.t_hi) {
                     load_k(kA, pp, sn.t_lo + warp, ln, f16n);
                     k_loaded = true;
@@ -1043,41 +1237,49 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
             __syncthreads();
             merge_warps<GPE, GPE>(S.wo, S.wm, S.wl, vinv, S.ot, S.mm, S.ll);
             __syncthreads();
-            finish_piece<GPE>(a, P, S.ot, S.mm, S.ll, S.pm, S.pl, &S.is_last, sg);
+            finish_piece<GPE>(a, P, S.ot, S.mm, S.ll, &S.last[k], sg);
+            __syncthreads();
+        }
+        // merges of the pairs whose last partial this CTA published, after all of
+        // the round's tiles (a merge never delays the CTA's own partial of a pair)
+        for (int k = 0; k < nseg; ++k) {
+            if (!S.last[k]) continue;
+            const Seg sg = S.seg[k];
+            merge_pair<GPE>(a, a.params[sg.h], S.ot, sg);
             __syncthreads();
         }
     }
 }
 
-template <int NT, int BITS, int NSEG>
-constexpr size_t smem_bytes() { return sizeof(TileSmem<4 * NT>); }
-
 using KernelPtr = void (*)(DecodeArgs);
 
-template <int NT, int BITS, int NSEG>
-KernelPtr kernel_of() { return decode_tile<NT, BITS, NSEG>; }
+template <int NT, int BITS, int NSEG, bool KMIX>
+KernelPtr kernel_of(size_t* smem) {
+    *smem = sizeof(TileSmem<4 * NT, KMIX>);
+    return decode_tile<NT, BITS, NSEG, KMIX>;
+}
+
+template <int NT>
+KernelPtr pick_nt(const tq_cache_desc* d, size_t* smem) {
+    const bool v4 = d->v_bits == 4;
+    if (d->k_mixed) return v4 ? kernel_of<NT, 4, 1, true>(smem) : kernel_of<NT, 3, 1, true>(smem);
+    if (d->rot == TQ_ROT_WHT32) return v4 ? kernel_of<NT, 4, 4, false>(smem) : kernel_of<NT, 3, 4, false>(smem);
+    return v4 ? kernel_of<NT, 4, 1, false>(smem) : kernel_of<NT, 3, 1, false>(smem);
+}
 
 KernelPtr pick(const tq_cache_desc* d, size_t* smem) {
-    const bool b4 = d->k_bits == 4;
-    const bool blk = d->rot == TQ_ROT_WHT32;
-    if (d->group <= 4) {
-        *smem = sizeof(TileSmem<4>);
-        if (blk) return b4 ? kernel_of<1, 4, 4>() : kernel_of<1, 3, 4>();
-        return b4 ? kernel_of<1, 4, 1>() : kernel_of<1, 3, 1>();
-    }
-    *smem = sizeof(TileSmem<8>);
-    if (blk) return b4 ? kernel_of<2, 4, 4>() : kernel_of<2, 3, 4>();
-    return b4 ? kernel_of<2, 4, 1>() : kernel_of<2, 3, 1>();
+    return d->group <= 4 ? pick_nt<1>(d, smem) : pick_nt<2>(d, smem);
 }
 
 // resident CTAs of the kernel for this format (CTAs per SM x SMs), looked up once
 // per device and kernel
 int grid_cap(const tq_cache_desc* d) {
     static std::mutex mu;
-    static int cache[64][8];
+    static int cache[64][16];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const int which = (d->group <= 4 ? 0 : 4) + (d->k_bits == 4 ? 2 : 0) + (d->rot == TQ_ROT_WHT32 ? 1 : 0);
+    const int which = (d->group <= 4 ? 0 : 8) + (d->v_bits == 4 ? 4 : 0) + (d->rot == TQ_ROT_WHT32 ? 2 : 0) +
+                      (d->k_mixed ? 1 : 0);
     std::lock_guard<std::mutex> lk(mu);
     if (!cache[dev][which]) {
         size_t smem = 0;
@@ -1104,7 +1306,7 @@ int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len) {
     // resident CTAs on this device; without one, the design's: 2 (4 query heads
     // per KV head) or 1 (8) CTAs per SM on 152 SMs
     int cap = grid_cap(d);
-    if (cap <= 0) cap = (d->group <= 4 ? TQ_TILE_MINB : 1) * 152;
+    if (cap <= 0) cap = (d->group <= 4 && !d->k_mixed ? TQ_TILE_MINB : 1) * 152;
     // one wave of resident CTAs, each warp with at least one tile
     const long long tiles = (long long)d->batch * d->n_kv_heads * ((max_seq_len + kTok - 1) / kTok);
     long long g = (tiles + kNW - 1) / kNW;

@@ -293,9 +293,9 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     d->v_norm_slots = rot == TQ_ROT_WHT32 ? 4 : 1;
     d->norm_bytes = norm_dtype == TQ_F16 ? 2 : 4;
     // the tile layout (read by the tensor-core decode kernel) for every format it
-    // covers: no mixed-rate keys, at most 8 query heads per KV head, fp16 norms
-    // for the four-block format
-    const bool tile = !k_mixed && d->group <= 8 && !(rot == TQ_ROT_WHT32 && norm_dtype != TQ_F16);
+    // covers: at most 8 query heads per KV head, fp16 norms where a vector has
+    // four (the 32-wide blocks, mixed-rate keys)
+    const bool tile = d->group <= 8 && !((rot == TQ_ROT_WHT32 || k_mixed) && norm_dtype != TQ_F16);
     d->layout = tile ? TQ_LAYOUT_TILE16 : TQ_LAYOUT_NATURAL;
     const int64_t alloc = tile ? ((int64_t)t_capacity + 15) / 16 * 16 : t_capacity;
     if (alloc > 0x7fffffff) return TQ_ERR_INVALID_ARG;

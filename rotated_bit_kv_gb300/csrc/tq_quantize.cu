@@ -184,8 +184,18 @@ __device__ __forceinline__ void encode_vector(const QuantArgs& a, const VecId& i
         }
     }
 
+    // tile layout: a b-bit code of mixed-rate keys' 1..3-bit groups is stored as
+    // code + 2^b, so that its nibble names its group
+    if (mixed && a.tiled) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int bw = seg_bits[segi[i]];
+            idx[i] += bw < 4 ? (1u << bw) : 0u;
+        }
+    }
     // pack and store (tile layout: the record goes through the warp's staging
-    // buffer, free here since mixed-rate keys never use that layout)
+    // buffer, once every lane is done reading the staged input)
+    if (a.tiled) __syncwarp();
     const size_t pos = (((size_t)b * a.Hkv + h) * a.t_alloc) + slot;
     uint8_t* rec = a.tiled ? reinterpret_cast<uint8_t*>(xs)
                            : (which ? a.codes[1] : a.codes[0]) + pos * (which ? a.code_bytes[1] : a.code_bytes[0]);

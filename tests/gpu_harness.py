@@ -157,17 +157,50 @@ def norm_positions(which: str, slots: int) -> np.ndarray:
     return P
 
 
+def key_code_offsets(spec) -> np.ndarray:
+    """[d] offset added to each key code in the tile layout of a cache with
+    mixed-rate keys: 2^b for a coordinate of a b-bit group, b < 4; 0 for the
+    4-bit group (include/tq.h)."""
+    off = np.zeros(128, dtype=np.uint8)
+    for sg in spec.segments:
+        if sg.bits < 4:
+            off[sg.start:sg.start + sg.length] = 1 << sg.bits
+    return off
+
+
 class CacheLayout:
     """Conversions between one (batch, KV head) row of a device array, as stored,
     and per-position records / norms."""
 
     def __init__(self, desc):
         self.tiled = int(desc.layout) == 1
+        self.mixed = int(desc.k_mixed) == 1
         self.t_alloc = int(desc.t_alloc)
         self.nb = {"k": int(desc.k_code_bytes), "v": int(desc.v_code_bytes)}
         self.slots = {"k": int(desc.k_norm_slots), "v": int(desc.v_norm_slots)}
 
-    def records(self, raw: np.ndarray, which: str) -> np.ndarray:
+    def _offsets(self, which, kspec):
+        if not (self.tiled and self.mixed and which == "k"):
+            return None
+        if kspec is None:
+            raise ValueError("mixed-rate keys in the tile layout: the head's key spec is needed")
+        return key_code_offsets(kspec)
+
+    @staticmethod
+    def _shift_nibbles(records, off, sign):
+        """Add (sign = 1) or remove (sign = -1) per-coordinate offsets of nibble
+        codes.  On removal a zero nibble (a position never written: a stored code
+        of a 1..3-bit group is at least 2) reads back as zero."""
+        out = []
+        for nib, o in ((records & 15, off[0::2]), (records >> 4, off[1::2])):
+            x = nib.astype(np.int16)
+            y = (x + sign * o.astype(np.int16)) & 15
+            if sign < 0:
+                y = np.where(x == 0, 0, y)
+            out.append(y)
+        return (out[0] | (out[1] << 4)).astype(np.uint8)
+
+    def records(self, raw: np.ndarray, which: str, kspec=None) -> np.ndarray:
         nb = self.nb[which]
         if not self.tiled:
             return raw.reshape(self.t_alloc, nb)
@@ -179,12 +212,17 @@ class CacheLayout:
         cols = (np.arange(64)[:, None] * fb + np.arange(fb)[None, :])              # record bit of (field, bit)
         for t in range(16):
             nat[:, t, cols.ravel()] = tb[:, M[t].ravel()]
-        return np.packbits(nat, axis=2, bitorder="little").reshape(self.t_alloc, nb)
+        rec = np.packbits(nat, axis=2, bitorder="little").reshape(self.t_alloc, nb)
+        off = self._offsets(which, kspec)
+        return rec if off is None else self._shift_nibbles(rec, off, -1)
 
-    def raw(self, records: np.ndarray, which: str) -> np.ndarray:
+    def raw(self, records: np.ndarray, which: str, kspec=None) -> np.ndarray:
         nb = self.nb[which]
         if not self.tiled:
             return np.ascontiguousarray(records, dtype=np.uint8).reshape(-1)
+        off = self._offsets(which, kspec)
+        if off is not None:
+            records = self._shift_nibbles(np.asarray(records, dtype=np.uint8), off, 1)
         bits = 3 if nb == 48 else 4
         M = tile_bit_map(which, bits)
         fb = M.shape[2]
@@ -213,11 +251,16 @@ class CacheLayout:
         return out.reshape(-1)
 
 
-def cache_records(cache, which: str) -> np.ndarray:
-    """[batch][n_kv][t_alloc][code_bytes] records of a device cache."""
+def _kspec(st, h):
+    return None if st is None else st.specs[h][0]
+
+
+def cache_records(cache, which: str, st=None) -> np.ndarray:
+    """[batch][n_kv][t_alloc][code_bytes] records of a device cache (st: the
+    Setup, needed for mixed-rate keys in the tile layout)."""
     lay = CacheLayout(cache.desc)
     raw = cache.codes_view(which).cpu().numpy()
-    return np.stack([np.stack([lay.records(raw[b, h], which) for h in range(raw.shape[1])])
+    return np.stack([np.stack([lay.records(raw[b, h], which, _kspec(st, h)) for h in range(raw.shape[1])])
                      for b in range(raw.shape[0])])
 
 
@@ -229,9 +272,9 @@ def cache_norms(cache, which: str) -> np.ndarray:
                      for b in range(raw.shape[0])])
 
 
-def pair_records(cache, which: str, b: int, h: int) -> np.ndarray:
+def pair_records(cache, which: str, b: int, h: int, st=None) -> np.ndarray:
     lay = CacheLayout(cache.desc)
-    return lay.records(cache.codes_view(which)[b, h].cpu().numpy(), which)
+    return lay.records(cache.codes_view(which)[b, h].cpu().numpy(), which, _kspec(st, h))
 
 
 def pair_norms(cache, which: str, b: int, h: int) -> np.ndarray:
@@ -239,15 +282,15 @@ def pair_norms(cache, which: str, b: int, h: int) -> np.ndarray:
     return lay.norms(cache.norms_view(which)[b, h].cpu().numpy(), which)
 
 
-def put_pair(torch, cache, which: str, b: int, h: int, records: np.ndarray, norms: np.ndarray, t0: int = 0):
+def put_pair(torch, cache, which: str, b: int, h: int, records: np.ndarray, norms: np.ndarray, t0: int = 0, st=None):
     """Write records / norms of positions t0 .. t0 + len - 1 of one pair into the
     device cache (the rest of the pair's row is kept)."""
     lay = CacheLayout(cache.desc)
-    rec = pair_records(cache, which, b, h)
+    rec = pair_records(cache, which, b, h, st)
     nrm = pair_norms(cache, which, b, h)
     rec[t0:t0 + records.shape[0]] = records
     nrm[t0:t0 + norms.shape[0]] = norms.reshape(norms.shape[0], -1)
-    cache.codes_view(which)[b, h] = torch.from_numpy(lay.raw(rec, which))
+    cache.codes_view(which)[b, h] = torch.from_numpy(lay.raw(rec, which, _kspec(st, h)))
     cache.norms_view(which)[b, h] = torch.from_numpy(lay.raw_norms(nrm, which))
 
 

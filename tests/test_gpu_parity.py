@@ -44,10 +44,14 @@ def _workload(name):
         "block32_tq4": W.block32(4),
         "so4": W.so4_wht(),
         "mixed": W.mixed_rate_long(),
+        # mixed-rate keys with four query heads per KV head
+        "mixed_g4": W.mixed_rate_long().with_(n_q_heads=8),
         # natural-layout variants of the same formats (CUDA-core decode kernels):
-        # 16 query heads per KV head, and fp32 norms with 32-wide blocks
+        # 16 query heads per KV head, and fp32 norms with 32-wide blocks or with
+        # mixed-rate keys
         "llama8b_g16": W.llama8b_decode().with_(n_kv_heads=2),
         "block32_f32": W.block32(3).with_(norm_dtype=W.F32),
+        "mixed_f32": W.mixed_rate_long().with_(norm_dtype=W.F32),
     }[name]
 
 
@@ -58,11 +62,15 @@ SMALL = {  # (batch, T) element-wise cases: several tiles and a ragged tail
     "block32_tq4": (2, 333),
     "so4": (1, 333),
     "mixed": (1, 700),
+    "mixed_g4": (2, 600),
     "llama8b_g16": (2, 333),
     "block32_f32": (2, 333),
+    "mixed_f32": (1, 600),
 }
-TILED = ["tiny", "llama8b", "block32_tq3", "block32_tq4", "so4"]   # TQ_LAYOUT_TILE16 caches
-NATURAL = ["mixed", "llama8b_g16", "block32_f32"]                  # TQ_LAYOUT_NATURAL caches
+# TQ_LAYOUT_TILE16 caches (tensor-core decode kernel)
+TILED = ["tiny", "llama8b", "block32_tq3", "block32_tq4", "so4", "mixed", "mixed_g4"]
+# TQ_LAYOUT_NATURAL caches (CUDA-core decode kernels)
+NATURAL = ["llama8b_g16", "block32_f32", "mixed_f32"]
 
 
 def _encode_on_gpu(tq, name, B, T, cap_extra=5, seq_lens=None):
@@ -84,7 +92,7 @@ def test_quantize_append_matches_oracle(tq, name):
     st, cache = _encode_on_gpu(tq, name, B, T)
     assert int(cache.status.item()) == 0
     assert st.desc.layout == (tq.TQ_LAYOUT_TILE16 if name in TILED else tq.TQ_LAYOUT_NATURAL)
-    kc, vc = cache_records(cache, "k"), cache_records(cache, "v")
+    kc, vc = cache_records(cache, "k", st), cache_records(cache, "v", st)
     kn, vn = cache_norms(cache, "k"), cache_norms(cache, "v")
     tot = bad = 0
     fws_all, fw_all = [], []
@@ -113,7 +121,7 @@ def test_quantize_append_matches_oracle(tq, name):
 
 
 def _check_codes_vs_oracle(st, cache, B, T):
-    kc, vc = cache_records(cache, "k"), cache_records(cache, "v")
+    kc, vc = cache_records(cache, "k", st), cache_records(cache, "v", st)
     kn, vn = cache_norms(cache, "k"), cache_norms(cache, "v")
     tot = bad = 0
     for b in range(B):
@@ -195,7 +203,7 @@ def test_quantize_tc_heads_and_tails(tq, in_dtype, B, T, pairs):
     c.append(K, V, torch.full((B,), 2, dtype=torch.int32, device="cuda"))   # slots 2 .. T+1
     torch.cuda.synchronize()
     assert int(c.status.item()) == 0
-    kc, vc = cache_records(c, "k"), cache_records(c, "v")
+    kc, vc = cache_records(c, "k", st), cache_records(c, "v", st)
     kn, vn = cache_norms(c, "k"), cache_norms(c, "v")
     bad = tot = 0
     for (b, h) in pairs or [(b, h) for b in range(B) for h in range(3)]:
@@ -250,8 +258,8 @@ def _upload_oracle_cache(tq, st, cache, B, T):
         for h in range(st.wl.n_kv_heads):
             ek = oracle_encode(st, "k", b, h, 0, T)
             ev = oracle_encode(st, "v", b, h, 0, T)
-            put_pair(torch, cache, "k", b, h, ek.codes, ek.norms)
-            put_pair(torch, cache, "v", b, h, ev.codes, ev.norms)
+            put_pair(torch, cache, "k", b, h, ek.codes, ek.norms, st=st)
+            put_pair(torch, cache, "v", b, h, ev.codes, ev.norms, st=st)
             encs[(b, h)] = (ek, ev)
     torch.cuda.synchronize()
     return encs
@@ -468,12 +476,12 @@ def test_append_positions_and_incremental(tq):
     assert torch.equal(cache2.norms_view("v"), whole_vn)
     assert int(cache2.status.item()) == 0
     # out-of-range start position: skipped and flagged; n_new = 0 is a no-op
-    before = cache_records(cache2, "v")
+    before = cache_records(cache2, "v", st)
     cache2.append(K[:, :3].contiguous(), V[:, :3].contiguous(),
                   torch.tensor([st.desc.t_capacity - 1, -5], dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert int(cache2.status.item()) & tq.TQ_DEV_BAD_POSITION
-    after = cache_records(cache2, "v")
+    after = cache_records(cache2, "v", st)
     cap = st.desc.t_capacity
     assert np.array_equal(after[1], before[1])             # batch 1 entirely skipped
     assert np.array_equal(after[0, :, :cap - 1], before[0, :, :cap - 1])
@@ -498,7 +506,7 @@ def test_quantize_tc_positions_outside_capacity(tq):
     torch.cuda.synchronize()
     assert int(c.status.item()) & tq.TQ_DEV_BAD_POSITION
     for which in ("k", "v"):
-        codes = cache_records(c, which)
+        codes = cache_records(c, which, st)
         norms = cache_norms(c, which)
         assert not codes[0, :, :start].any() and not norms[0, :, :start].any()
         assert not codes[1, :, T - 5:].any() and not norms[1, :, T - 5:].any()
@@ -565,7 +573,7 @@ def test_full_size_sampled(tq, name):
         ek = oracle_encode(st, "k", b, h)
         ev = oracle_encode(st, "v", b, h)
         for enc, which in ((ek, "k"), (ev, "v")):
-            rec = pair_records(cache, which, b, h)[:T]
+            rec = pair_records(cache, which, b, h, st)[:T]
             nb, n, _, _, ok = compare_codes(rec, enc, st.specs[h][0 if which == "k" else 1])
             assert ok
             bad += nb
@@ -574,8 +582,8 @@ def test_full_size_sampled(tq, name):
     assert bad / tot <= MAX_MISMATCH_FRAC
     # read side: the sampled pairs carry the oracle's records
     for (b, h), (ek, ev) in encs.items():
-        put_pair(torch, cache, "k", b, h, ek.codes, ek.norms)
-        put_pair(torch, cache, "v", b, h, ev.codes, ev.norms)
+        put_pair(torch, cache, "k", b, h, ek.codes, ek.norms, st=st)
+        put_pair(torch, cache, "v", b, h, ev.codes, ev.norms, st=st)
     q = to_torch_input(torch, inp.q, wl.in_dtype)
     sl = torch.from_numpy(inp.seq_lens).cuda()
     _check_decode(tq, st, cache, encs, q, sl, T, -1, 0, pairs=pairs)

@@ -57,8 +57,9 @@ def test_norm_positions_are_a_permutation(which, slots):
 
 
 class _Desc:
-    def __init__(self, bits, slots, t_alloc):
+    def __init__(self, bits, slots, t_alloc, k_mixed=0):
         self.layout = 1
+        self.k_mixed = k_mixed
         self.t_alloc = t_alloc
         self.k_code_bytes = self.v_code_bytes = 48 if bits == 3 else 64
         self.k_norm_slots = self.v_norm_slots = slots
@@ -76,3 +77,39 @@ def test_round_trip(bits, slots):
         assert np.array_equal(lay.records(raw, which), rec)
         nrm = rng.standard_normal((48, slots)).astype(np.float16)
         assert np.array_equal(lay.norms(lay.raw_norms(nrm, which), which), nrm)
+
+
+class _Seg:
+    def __init__(self, start, length, bits):
+        self.start, self.length, self.bits = start, length, bits
+
+
+class _Spec:
+    def __init__(self, segs):
+        self.segments = segs
+
+
+def test_mixed_key_offsets():
+    """Mixed-rate keys in the tile layout: a b-bit code c (b < 4) is stored as
+    c + 2^b, so every stored nibble of a 1..3-bit group lies in [2^b, 2^(b+1))
+    and names its group; 4-bit codes are stored as they are."""
+    rng = np.random.default_rng(5)
+    segs = [_Seg(0, 10, 1), _Seg(10, 30, 2), _Seg(40, 50, 3), _Seg(90, 38, 4)]
+    spec = _Spec(segs)
+    width = np.zeros(128, dtype=np.int64)
+    for sg in segs:
+        width[sg.start:sg.start + sg.length] = sg.bits
+    codes = rng.integers(0, 1 << width, size=(48, 128)).astype(np.uint8)   # [T][d] codes of each width
+    rec = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)        # nibble records
+    mixed = CacheLayout(_Desc(4, 4, 48, k_mixed=1))
+    raw = mixed.raw(rec, "k", spec)
+    assert np.array_equal(mixed.records(raw, "k", spec), rec)
+    stored = CacheLayout(_Desc(4, 4, 48)).records(raw, "k")                 # the nibbles as stored
+    nib = np.stack([stored & 15, stored >> 4], axis=2).reshape(48, 128).astype(np.int64)
+    lo_b = np.where(width < 4, 1 << width, 0)
+    hi_b = np.where(width < 4, 2 << width, 16)
+    assert np.all((nib >= lo_b) & (nib < hi_b))
+    assert np.array_equal(nib - lo_b, codes.astype(np.int64))
+    # values are not offset; a never-written (zero) row reads back as zero
+    assert np.array_equal(mixed.records(mixed.raw(rec, "v", spec), "v", spec), rec)
+    assert not mixed.records(np.zeros(48 * 64, dtype=np.uint8), "k", spec).any()

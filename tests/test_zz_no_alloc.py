@@ -45,8 +45,8 @@ def _cache(tq, wl, B, T):
     for b in range(B):
         for h in range(wl.n_kv_heads):
             ek, ev = oracle_encode(st, "k", b, h), oracle_encode(st, "v", b, h)
-            put_pair(torch, cache, "k", b, h, ek.codes, ek.norms)
-            put_pair(torch, cache, "v", b, h, ev.codes, ev.norms)
+            put_pair(torch, cache, "k", b, h, ek.codes, ek.norms, st=st)
+            put_pair(torch, cache, "v", b, h, ev.codes, ev.norms, st=st)
             encs[(b, h)] = (ek, ev)
     cache.encs = encs
     return st, cache, q, sl
