@@ -551,6 +551,52 @@ def lse_merge(partials, v_spec: HeadSpec) -> np.ndarray:
     return (ot / l[:, None]) @ v_spec.R
 
 
+def part_state(q, K, V) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """(m, l, o) of one part of the keys in the original domain: s_j = <q, k_j> / sqrt(d),
+    m = max_j s_j, l = sum_j e^(s_j - m), o = sum_j e^(s_j - m) v_j (not normalised).
+    An empty part yields (-inf, 0, 0)."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if K.shape[0] == 0:
+        return np.full(q.shape[0], -np.inf), np.zeros(q.shape[0]), np.zeros_like(q)
+    s = q @ K.T / math.sqrt(q.shape[-1])
+    m = s.max(axis=1)
+    p = np.exp(s - m[:, None])
+    return m, p.sum(axis=1), p @ V
+
+
+def attend_prefix_packed(q, K_pre, V_pre, k_idx, k_norm, k_spec: HeadSpec, v_idx, v_norm, v_spec: HeadSpec,
+                         seq_len: int) -> np.ndarray:
+    """Attention of one (batch, KV head) over two parts of its keys: a block of
+    unquantised tokens (K_pre, V_pre [n][d]: the exact values of the stored
+    fp16 / bf16 / fp32 inputs) and the first seq_len tokens of the packed cache.
+    The unquantised block is the prefill kept in fp16 [RotaryQuant, deferred
+    prefill] or the recent-token buffer [Block-GTQ]; the set of keys is the
+    union of the two parts whatever their order in the sequence.
+
+    Each part is attended on its own: the unquantised part in the original
+    domain; the packed part in the rotated domain (q~ = R_K q, n C[idx]) and
+    brought back with its one inverse rotation, o_p = R_V^T o~_p (linear, so it
+    applies to the unnormalised sum).  The parts are merged by log-sum-exp
+    [Block-GTQ, key-axis split]: M = max_u m_u,
+      o = sum_u e^(m_u - M) o_u / sum_u e^(m_u - M) l_u."""
+    q = np.asarray(q, dtype=np.float64)
+    parts = [part_state(q, K_pre, V_pre)]
+    L = int(seq_len)
+    if L > 0:
+        m, l, ot = split_partials(q, k_idx, k_norm, k_spec, v_idx, v_norm, v_spec, [(0, L)])[0]
+        parts.append((m, l, ot @ v_spec.R))
+    ms = np.stack([p[0] for p in parts])
+    M = ms.max(axis=0)
+    if not np.all(np.isfinite(M)):
+        return np.zeros_like(q)
+    w = np.where(np.isfinite(ms), np.exp(ms - M[None]), 0.0)
+    l = sum(w[i] * parts[i][1] for i in range(len(parts)))
+    o = sum(w[i][:, None] * parts[i][2] for i in range(len(parts)))
+    return o / l[:, None]
+
+
 # ============================================================================
 # 6. Whole-cache helpers (loops over (batch, KV head); no reordering)
 # ============================================================================
