@@ -358,6 +358,46 @@ tq_status tq_decode_attention_noalloc(const tq_cache_desc* desc, const tq_cache_
 /* Size in bytes of the fixed scratch array behind tq_decode_attention_noalloc. */
 size_t tq_decode_noalloc_max_scratch_bytes(void);
 
+/* Decode attention over two parts of each sequence's keys: a block of
+ * unquantised tokens (the prompt's K and V kept in fp16/bf16: deferred prefill
+ * [RotaryQuant, IsoQuant decode flow]; or the recent-token buffer [Block-GTQ,
+ * limitations]) and the packed cache.  The set of keys attended is the union of
+ * the two parts: the first d_prefix_lens[b] unquantised tokens and the first
+ * d_seq_lens[b] packed tokens of batch b.  The packed part is attended as by
+ * tq_decode_attention (automatic plan), which also leaves each head's log2-sum-
+ * exp in the workspace; the unquantised part is attended in the original domain
+ * (scores q k / sqrt(d) in fp32 from the stored values) and the two are merged
+ * by log-sum-exp [Block-GTQ, key-axis split with log-sum-exp merge].
+ *   k_prefix, v_prefix  device [batch][prefix_capacity][n_kv_heads][128] of
+ *                prefix_dtype (TQ_F32, TQ_F16 or TQ_BF16), the layout of
+ *                tq_quantize_append's input; may be NULL when max_prefix_len = 0
+ *   d_prefix_lens  device int32 [batch]; values above prefix_capacity or
+ *                max_prefix_len are clamped (TQ_DEV_SEQ_OVER_CAPACITY /
+ *                TQ_DEV_SEQ_OVER_MAX); 0 = no unquantised token
+ *   max_seq_len  0 (no packed token: cache and d_seq_lens are not read) up to
+ *                t_capacity
+ *   max_prefix_len  0 .. prefix_capacity
+ *   workspace    device, 256-byte aligned, at least
+ *                tq_decode_prefix_workspace_bytes(desc, max_prefix_len) bytes,
+ *                zero-filled before its first use; every call leaves it so
+ *   out          device fp32 [batch][n_q_heads][128]; a head with no key at all
+ *                gets zeros
+ * Two kernels on `stream` (the second a programmatic dependent of the first).
+ * Errors: TQ_ERR_INVALID_ARG (NULL, misaligned, range), TQ_ERR_WORKSPACE, the
+ * errors of tq_decode_attention, TQ_ERR_CUDA. */
+tq_status tq_decode_attention_prefix(const tq_cache_desc* desc, const tq_cache_ptrs* cache,
+                                     const void* q, int32_t q_dtype,
+                                     const int32_t* d_seq_lens, int32_t max_seq_len,
+                                     const void* k_prefix, const void* v_prefix,
+                                     int32_t prefix_dtype, int32_t prefix_capacity,
+                                     const int32_t* d_prefix_lens, int32_t max_prefix_len,
+                                     float* out, void* workspace, size_t workspace_bytes,
+                                     int32_t* d_status, void* stream);
+
+/* Workspace bytes of tq_decode_attention_prefix for at most max_prefix_len
+ * unquantised tokens per sequence (0 on a bad descriptor). */
+size_t tq_decode_prefix_workspace_bytes(const tq_cache_desc* desc, int32_t max_prefix_len);
+
 /* The splits and V mode tq_decode_attention would use (host only).  For the
  * tensor-core kernel *splits_out is the number of CTAs (the 16-token tiles of
  * all (batch, KV head) pairs, in pair order, are divided evenly over them; the

@@ -67,6 +67,9 @@ _SIGS = {
     "tq_decode_attention_noalloc": (_I, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_ptrs), _P, _I,
                                          _P, _I, _P, _P, _P]),
     "tq_decode_noalloc_max_scratch_bytes": (ctypes.c_size_t, []),
+    "tq_decode_attention_prefix": (_I, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_ptrs), _P, _I, _P,
+                                        _I, _P, _P, _I, _I, _P, _I, _P, _P, ctypes.c_size_t, _P, _P]),
+    "tq_decode_prefix_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(tq_cache_desc), _I]),
 }
 
 
@@ -241,6 +244,30 @@ def tq_decode_attention_noalloc(desc: tq_cache_desc, cache: tq_cache_ptrs, q, se
                                              _stream(stream)), "tq_decode_attention_noalloc")
 
 
+def tq_decode_prefix_workspace_bytes(desc: tq_cache_desc, max_prefix_len: int) -> int:
+    return int(lib().tq_decode_prefix_workspace_bytes(ctypes.byref(desc), int(max_prefix_len)))
+
+
+def tq_decode_attention_prefix(desc: tq_cache_desc, cache: tq_cache_ptrs, q, seq_lens, max_seq_len: int,
+                               k_prefix, v_prefix, prefix_lens, max_prefix_len: int, out, workspace, status=None,
+                               stream=None):
+    """Attention over the unquantised tokens k_prefix / v_prefix (CUDA
+    [batch][capacity][n_kv][128] fp32/fp16/bf16, the first prefix_lens[b] of
+    batch b) plus the packed cache (the first seq_lens[b] tokens); out CUDA fp32
+    [batch][n_q][128]; workspace zero-filled before its first use."""
+    _require_cuda(q, seq_lens, k_prefix, v_prefix, prefix_lens, out, workspace, status)
+    if k_prefix is not None and (v_prefix is None or k_prefix.dtype != v_prefix.dtype or
+                                 k_prefix.shape != v_prefix.shape):
+        raise TypeError("k_prefix and v_prefix must share a dtype and a shape")
+    cap = 0 if k_prefix is None else int(k_prefix.shape[1])
+    pdt = TQ_F16 if k_prefix is None else _dtype_code(k_prefix)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().tq_decode_attention_prefix(ctypes.byref(desc), ctypes.byref(cache), _ptr(q), _dtype_code(q),
+                                            _ptr(seq_lens), int(max_seq_len), _ptr(k_prefix), _ptr(v_prefix), pdt,
+                                            cap, _ptr(prefix_lens), int(max_prefix_len), _ptr(out), _ptr(workspace),
+                                            nbytes, _ptr(status), _stream(stream)), "tq_decode_attention_prefix")
+
+
 # ---------------------------------------------------------------- allocation helper
 class PackedKVCache:
     """Device buffers of one packed cache, allocated through PyTorch (the
@@ -275,6 +302,20 @@ class PackedKVCache:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         tq_decode_attention_ex(self.desc, self.ptrs, q, seq_lens, max_seq_len, out, self.workspace, self.status,
                                stream, v_mode, n_splits)
+        return out
+
+    def decode_prefix(self, q, seq_lens, max_seq_len, k_prefix, v_prefix, prefix_lens, max_prefix_len, out=None,
+                      stream=None):
+        """Attention over the unquantised tokens k_prefix / v_prefix plus the
+        packed cache (tq_decode_attention_prefix); the workspace grows as needed."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        need = tq_decode_prefix_workspace_bytes(self.desc, max_prefix_len)
+        if getattr(self, "prefix_workspace", None) is None or self.prefix_workspace.numel() < need:
+            self.prefix_workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=self.device)
+        tq_decode_attention_prefix(self.desc, self.ptrs, q, seq_lens, max_seq_len, k_prefix, v_prefix, prefix_lens,
+                                   max_prefix_len, out, self.prefix_workspace, self.status, stream)
         return out
 
     def norms_view(self, which: str):

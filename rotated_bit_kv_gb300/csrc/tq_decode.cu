@@ -381,10 +381,14 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
     return TQ_OK;
 }
 
-tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,
-                                 const int32_t* d_seq_lens, int32_t max_seq_len, float* out, void* workspace,
-                                 size_t workspace_bytes, int32_t* d_status, void* stream, int32_t v_mode,
-                                 int32_t n_splits) {
+}  // extern "C"
+
+// Decode attention with an optional per-head log2-sum-exp output (lse, [batch][n_q]
+// fp32 device or null), shared by tq_decode_attention_ex and the prefix entry.
+tq_status tq_decode_run(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,
+                        const int32_t* d_seq_lens, int32_t max_seq_len, float* out, void* workspace,
+                        size_t workspace_bytes, int32_t* d_status, void* stream, int32_t v_mode, int32_t n_splits,
+                        float* lse) {
     if (!d || !c || d->head_dim != TQ_HEAD_DIM) return TQ_ERR_INVALID_ARG;
     if (!q || !d_seq_lens || !out || !c->k_codes || !c->k_norms || !c->v_codes || !c->v_norms || !c->params)
         return TQ_ERR_INVALID_ARG;
@@ -416,6 +420,7 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     a.q = q;
     a.seq_lens = d_seq_lens;
     a.out = out;
+    a.lse = lse;
     a.status = d_status;
     a.tickets = nullptr;
     a.ws_part = nullptr;
@@ -446,6 +451,16 @@ tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c,
     dim3 grid(splits, d->n_kv_heads, d->batch);
     fn<<<grid, kThreads, 0, (cudaStream_t)stream>>>(a);
     return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" {
+
+tq_status tq_decode_attention_ex(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,
+                                 const int32_t* d_seq_lens, int32_t max_seq_len, float* out, void* workspace,
+                                 size_t workspace_bytes, int32_t* d_status, void* stream, int32_t v_mode,
+                                 int32_t n_splits) {
+    return tq_decode_run(d, c, q, q_dtype, d_seq_lens, max_seq_len, out, workspace, workspace_bytes, d_status,
+                         stream, v_mode, n_splits, nullptr);
 }
 
 tq_status tq_decode_attention(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,

@@ -18,6 +18,7 @@ struct DecodeArgs {
     const void* q;
     const int32_t* seq_lens;
     float* out;
+    float* lse;         // optional [B][Hq]: log2-sum-exp of each head's scores (log2 units), or null
     float* ws_part;
     int32_t* tickets;
     int32_t* status;
@@ -204,10 +205,10 @@ __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b) {
 // A warp per head finds M_g = max_t m_t and L_g = sum_t 2^(m_t - M_g) l_t; then each
 // thread accumulates four coordinates of one head over the parts, its loads
 // independent of each other so that their latencies overlap.  Empty parts
-// (m = -inf) weigh 0; a pair with no tokens gives 0.  NTHR threads.
+// (m = -inf) weigh 0; a pair with no tokens gives 0.  NTHR threads; M_g and L_g
+// stay in sM, sL (shared).
 template <int GP, int NTHR>
-__device__ __forceinline__ void merge_parts(const float* base, int parts, float (*ot)[128]) {
-    __shared__ float sM[GP], sL[GP];
+__device__ __forceinline__ void merge_parts(const float* base, int parts, float (*ot)[128], float* sM, float* sL) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int g = warp; g < GP; g += NTHR / 32) {
         float M = -INFINITY;
@@ -254,10 +255,12 @@ __device__ __forceinline__ void merge_parts(const float* base, int parts, float 
 
 // Epilogue: `ot[g][c]` holds this CTA's unnormalised o~, (m[g], l[g]) its
 // softmax state (identical in every thread).  Either finalise directly (one
-// split) or publish the partial and let the last CTA merge.
+// split) or publish the partial and let the last CTA merge; the finalising CTA
+// also writes each head's log2-sum-exp when asked (a.lse).
 template <int GP>
 __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const float* m,
                          const float* l, int* is_last, int b, int h, int s) {
+    __shared__ float sM[GP], sL[GP];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (a.n_splits > 1) {
         float* part = a.ws_part + ((((size_t)b * a.Hkv + h) * a.n_splits + s) * GP) * kPartStride;
@@ -277,7 +280,7 @@ __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*o
         __threadfence();
         // log-sum-exp merge over the splits  [Block-GTQ]
         merge_parts<GP, kThreads>(a.ws_part + (((size_t)b * a.Hkv + h) * a.n_splits * GP) * kPartStride,
-                                  a.n_splits, ot);
+                                  a.n_splits, ot, sM, sL);
         if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
         __syncthreads();
     } else {
@@ -285,8 +288,14 @@ __device__ void epilogue(const DecodeArgs& a, const tq_head_params& P, float (*o
             const int g = i >> 7;
             ot[g][i & 127] = l[g] > 0.f ? ot[g][i & 127] / l[g] : 0.f;
         }
+        if (tid < GP) {
+            sM[tid] = m[tid];
+            sL[tid] = l[tid];
+        }
         __syncthreads();
     }
+    if (a.lse && tid < a.G)   // the softmax mass, for a later merge with other keys
+        a.lse[(size_t)b * a.Hq + (size_t)h * a.G + tid] = sL[tid] > 0.f ? sM[tid] + log2f(sL[tid]) : -INFINITY;
     // o = R_V^T o~, once per query head  [RotaryQuant Key design 3, Kernel D]
     for (int g = warp; g < a.G; g += 4) {
         float v[4];

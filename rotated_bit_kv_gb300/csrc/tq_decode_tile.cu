@@ -769,9 +769,10 @@ __device__ __forceinline__ void merge_warps(const float (*wo)[GPE][128], const f
 // issues all of the batch's loads (m_t, l_t and its o~ quadruple) at once, then
 // moves its running maximum M to the batch's and folds the batch in:
 //   acc = 2^(M_old - M) acc + sum_t 2^(m_t - M) o~_t,  L likewise with l_t.
-// Empty parts (m = -inf) weigh 0; a pair with no tokens gives 0.
+// Empty parts (m = -inf) weigh 0; a pair with no tokens gives 0.  The merged
+// (M, L) of head g go to mo[g], lo[g] (shared).
 template <int GP>
-__device__ __forceinline__ void merge_pieces(const float* base, int parts, float (*ot)[128]) {
+__device__ __forceinline__ void merge_pieces(const float* base, int parts, float (*ot)[128], float* mo, float* lo) {
     static_assert(GP * 32 <= kNThr, "one coordinate quadruple per thread");
     constexpr int MB = GP <= 4 ? 8 : 16;   // parts in flight (the 4-head kernels' register budget)
     const int tid = threadIdx.x, g = tid >> 5, d4 = tid & 31;
@@ -808,6 +809,10 @@ __device__ __forceinline__ void merge_pieces(const float* base, int parts, float
         M = Mb;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (d4 == 0) {
+        mo[g] = M;
+        lo[g] = L;
+    }
     ot[g][4 * d4] = acc.x * inv;
     ot[g][4 * d4 + 1] = acc.y * inv;
     ot[g][4 * d4 + 2] = acc.z * inv;
@@ -815,9 +820,14 @@ __device__ __forceinline__ void merge_pieces(const float* base, int parts, float
 }
 
 // o = R_V^T o~ for the pair's query heads from ot (normalised), into out
-// [RotaryQuant Key design 3, Kernel D]
-__device__ __forceinline__ void store_out(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const Seg& sg) {
+// [RotaryQuant Key design 3, Kernel D]; with a.lse, each head's log2-sum-exp
+// m + log2 l from its softmax state (mm, ll)
+__device__ __forceinline__ void store_out(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128],
+                                          const float* mm, const float* ll, const Seg& sg) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (a.lse && threadIdx.x < a.G)
+        a.lse[(size_t)sg.b * a.Hq + (size_t)sg.h * a.G + threadIdx.x] =
+            ll[threadIdx.x] > 0.f ? mm[threadIdx.x] + log2f(ll[threadIdx.x]) : -INFINITY;
     for (int g = warp; g < a.G; g += kNW) {
         float v[4];
 #pragma unroll
@@ -855,7 +865,7 @@ __device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float
             ot[g][i & 127] = ll[g] > 0.f ? ot[g][i & 127] / ll[g] : 0.f;
         }
         __syncthreads();
-        store_out(a, P, ot, sg);
+        store_out(a, P, ot, mm, ll, sg);
         if (tid == 0) *last = 0;
     }
 }
@@ -863,12 +873,13 @@ __device__ void finish_piece(const DecodeArgs& a, const tq_head_params& P, float
 // The merge of a pair whose last partial this CTA published: all partials by
 // log-sum-exp, the ticket reset for the next call, then R_V^T and the write.
 template <int GP>
-__device__ void merge_pair(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], const Seg& sg) {
+__device__ void merge_pair(const DecodeArgs& a, const tq_head_params& P, float (*ot)[128], float* mm, float* ll,
+                           const Seg& sg) {
     __threadfence();
-    merge_pieces<GP>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot);
+    merge_pieces<GP>(a.ws_part + (size_t)sg.first * GP * kPartStride, sg.parts, ot, mm, ll);
     if (threadIdx.x == 0) a.tickets[sg.b * a.Hkv + sg.h] = 0;   // ready for the next call
     __syncthreads();
-    store_out(a, P, ot, sg);
+    store_out(a, P, ot, mm, ll, sg);
 }
 
 // q~ = R_K q of head g of pair (b, h) into dst[128] (log2 units); one warp
@@ -1054,6 +1065,8 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
         if (seq_len_of(a, bb, false) == 0) {
             float* ob = a.out + (size_t)bb * a.Hq * 128;
             for (int i = tid; i < a.Hq * 128; i += kNThr) ob[i] = 0.f;
+            if (a.lse)
+                for (int i = tid; i < a.Hq; i += kNThr) a.lse[(size_t)bb * a.Hq + i] = -INFINITY;
         }
     }
     __syncthreads();
@@ -1245,7 +1258,7 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
         for (int k = 0; k < nseg; ++k) {
             if (!S.last[k]) continue;
             const Seg sg = S.seg[k];
-            merge_pair<GPE>(a, a.params[sg.h], S.ot, sg);
+            merge_pair<GPE>(a, a.params[sg.h], S.ot, S.mm, S.ll, sg);
             __syncthreads();
         }
     }

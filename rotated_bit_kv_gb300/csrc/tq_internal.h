@@ -67,3 +67,11 @@ int tq_v_crossover(void);   // V-mode crossover length (TQ_V_CROSSOVER env, defa
 #ifdef __cplusplus
 }
 #endif
+
+// Decode attention with an optional per-head log2-sum-exp output (lse: device fp32
+// [batch][n_q_heads], log2 units of q log2(e) / sqrt(d), or NULL); implemented in
+// tq_decode.cu, used by tq_decode_attention_ex and the prefix entry point.
+tq_status tq_decode_run(const tq_cache_desc* d, const tq_cache_ptrs* c, const void* q, int32_t q_dtype,
+                        const int32_t* d_seq_lens, int32_t max_seq_len, float* out, void* workspace,
+                        size_t workspace_bytes, int32_t* d_status, void* stream, int32_t v_mode, int32_t n_splits,
+                        float* lse);

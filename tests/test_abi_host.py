@@ -173,3 +173,33 @@ def test_decode_plan_host_only(tqlib):
         tq.tq_decode_plan(d, 0)
     with pytest.raises(tq.TQError):
         tq.tq_decode_plan(d, 9000)
+
+
+def test_prefix_workspace_and_argument_checks(tqlib):
+    """Host-side behaviour of the prefix entry point: workspace sizes grow with the
+    unquantised length and hold the packed decode's; bad arguments are refused
+    before any device work (every call below fails its checks)."""
+    d = tqlib.tq_cache_desc_init(128, 32, 8, 4, 1000, 0, 3, 3, 1)
+    w0 = tqlib.tq_decode_prefix_workspace_bytes(d, 0)
+    w1 = tqlib.tq_decode_prefix_workspace_bytes(d, 4096)
+    assert w0 >= tqlib.tq_decode_workspace_bytes(d, 1) and w1 > w0
+    assert tqlib.tq_decode_prefix_workspace_bytes(d, -1) == 0
+    h = tqlib.lib()
+    c = tqlib.tq_cache_ptrs(16, 16, 16, 16, 16)
+    w50 = tqlib.tq_decode_prefix_workspace_bytes(d, 50)
+    args = dict(q=256, qdt=tqlib.TQ_F16, sl=256, msl=10, kp=256, vp=256, pdt=tqlib.TQ_F16, cap=100, pl=256, mpl=50,
+                out=256, ws=256, wsb=w50)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return h.tq_decode_attention_prefix(ctypes.byref(d), ctypes.byref(c), a["q"], a["qdt"], a["sl"], a["msl"],
+                                            a["kp"], a["vp"], a["pdt"], a["cap"], a["pl"], a["mpl"], a["out"], a["ws"],
+                                            a["wsb"], None, None)
+    assert call(out=0) == tqlib.TQ_ERR_INVALID_ARG
+    assert call(pl=0) == tqlib.TQ_ERR_INVALID_ARG
+    assert call(pdt=7) == tqlib.TQ_ERR_INVALID_ARG
+    assert call(mpl=101) == tqlib.TQ_ERR_INVALID_ARG          # above the capacity
+    assert call(kp=0) == tqlib.TQ_ERR_INVALID_ARG             # unquantised tokens without K
+    assert call(kp=258) == tqlib.TQ_ERR_INVALID_ARG           # misaligned
+    assert call(wsb=w50 - 1) == tqlib.TQ_ERR_WORKSPACE
+    assert call(ws=0) == tqlib.TQ_ERR_WORKSPACE
