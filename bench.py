@@ -638,6 +638,57 @@ def run_crossover(args):
         torch.cuda.empty_cache()
 
 
+def run_prefix(args):
+    """Decode over unquantised (fp16) tokens plus the packed cache: time of the
+    packed decode alone and of the whole call (packed decode, then the fp16
+    kernel with the log-sum-exp merge), cold L2 as in the sweep; bytes = the
+    packed part's decode bytes + the unquantised K and V read."""
+    import torch
+
+    import rotated_bit_kv_gb300 as tq
+
+    tq.build()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cases = [(W.llama8b_decode(seq_len=6144), 6144, 2048, "fp16 prefix 2048 + packed 6144"),
+             (W.llama8b_decode(seq_len=512), 512, 8192, "deferred prefill: fp16 prompt 8192 + packed 512"),
+             (W.mixed_rate_long(131072), 131072, 128, "recent-token buffer: fp16 128 + packed 131072"),
+             (W.so4_wht(seq_len=128), 128, 32768, "fp16 prompt 32768 + packed 128")]
+    print("| workload | B | packed T | fp16 P | packed decode us | whole call us | fp16 part us | "
+          "whole-call GB/s | of measured peak |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for wl, T, P, what in cases:
+        if args.only and args.only not in wl.name:
+            continue
+        inp = W.make_inputs(wl, seq_len=T)
+        desc, blob = library_setup(tq, wl, inp, T)
+        cache = tq.PackedKVCache(desc, blob, device=dev)
+        K = _to_torch(torch, inp.K, wl.in_dtype, dev)
+        V = _to_torch(torch, inp.V, wl.in_dtype, dev)
+        cache.append(K, V, torch.zeros(wl.batch, dtype=torch.int32, device=dev))
+        del K, V
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        kp = torch.randn((wl.batch, P, wl.n_kv_heads, 128), generator=g, device=dev).to(torch.float16)
+        vp = torch.randn((wl.batch, P, wl.n_kv_heads, 128), generator=g, device=dev).to(torch.float16)
+        q = _to_torch(torch, inp.q, wl.in_dtype, dev)
+        seq = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
+        pl = torch.full((wl.batch,), P, dtype=torch.int32, device=dev)
+        out = torch.empty((wl.batch, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+        us_p = _cold_launch_us(torch, flush, lambda: cache.decode(q, seq, T, out=out), args.steps)
+        us_w = _cold_launch_us(torch, flush, lambda: cache.decode_prefix(q, seq, T, kp, vp, pl, P, out=out),
+                               args.steps)
+        if int(cache.status.item()) != 0:
+            raise RuntimeError(f"device status {int(cache.status.item())}")
+        nbytes = step_bytes(wl, T, desc)["decode"] + 2 * kp.numel() * kp.element_size()
+        gbs = nbytes / (us_w * 1e-6) / 1e9
+        print(f"| {wl.name} ({what}) | {wl.batch} | {T} | {P} | {us_p:.1f} | {us_w:.1f} | {us_w - us_p:.1f} | "
+              f"{gbs:.0f} | {100 * gbs / peak:.1f} % |", flush=True)
+        del cache, q, out, kp, vp
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -654,7 +705,12 @@ def main():
     ap.add_argument("--only", default="", help="sweep: workloads whose name contains this")
     ap.add_argument("--crossover", action="store_true",
                     help="token- against dimension-parallel decode on natural-layout caches (a table)")
+    ap.add_argument("--prefix", action="store_true",
+                    help="decode over fp16 tokens plus the packed cache (a table)")
     args = ap.parse_args()
+    if args.prefix:
+        run_prefix(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -316,8 +316,11 @@ tq_status tq_decode_attention(const tq_cache_desc* desc, const tq_cache_ptrs* ca
 /* tq_decode_attention with explicit choices, for tests and tuning:
  *   v_mode    TQ_VMODE_*.  TQ_LAYOUT_TILE16 caches run the tensor-core kernel
  *             (AUTO, TENSOR or TENSOR_STREAMK); TQ_LAYOUT_NATURAL caches run
- *             the CUDA-core kernels (AUTO: token parallel below the crossover
- *             length, dimension parallel above; or either one explicitly).
+ *             the CUDA-core kernels (AUTO: token parallel below the format's
+ *             crossover length, dimension parallel from it on; the crossover
+ *             measured on GB300 is 0 for every natural-layout format, so AUTO
+ *             is dimension parallel; the environment variable TQ_V_CROSSOVER
+ *             overrides it; or either kernel explicitly).
  *   n_splits  0 for the automatic choice; else, CUDA-core kernels: key-axis
  *             splits per (batch, KV head), 1..TQ_MAX_SPLITS; tensor-core
  *             kernel: the number of CTAs the tiles of all pairs are divided

@@ -356,9 +356,10 @@ tq_status tq_decode_plan(const tq_cache_desc* d, int32_t max_seq_len, int32_t v_
         if (v_mode_out) *v_mode_out = mode;
         return TQ_OK;
     }
-    // natural layout: token-parallel below the crossover, dimension-parallel above
+    // natural layout: token-parallel below the format's measured crossover,
+    // dimension-parallel from it on
     if (mode == TQ_VMODE_TENSOR) return TQ_ERR_UNSUPPORTED;
-    if (mode == TQ_VMODE_AUTO) mode = max_seq_len < tq_v_crossover() ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
+    if (mode == TQ_VMODE_AUTO) mode = max_seq_len < tq_v_crossover(d) ? TQ_VMODE_TOKEN_PARALLEL : TQ_VMODE_DIM_PARALLEL;
     int splits = n_splits;
     const long long pairs = (long long)d->batch * d->n_kv_heads;
     if (splits == 0) {

@@ -1121,14 +1121,15 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
         const int nseg = S.nseg;
         if (nseg == 0) break;
 
-        // first keys of the round, in flight while the queries are rotated
+        // the round's first tile, in flight while the queries are rotated
         KRegs<KB, KN> kA, kB;
         VRegs<BITS, NSEG> vA, vB;
         PairPtr pp = pair_ptr<KB, KN, BITS, NSEG>(a, S.seg[0].b, S.seg[0].h);
-        bool k_loaded = false;
+        bool first_loaded = false;
         if (S.seg[0].t_lo + warp < S.seg[0].t_hi) {
             load_k(kA, pp, S.seg[0].t_lo + warp, ln, f16n);
-            k_loaded = true;
+            load_v(vA, pp, S.seg[0].t_lo + warp, ln, f16n);
+            first_loaded = true;
         }
         if constexpr (!KMIX) {
             for (int i = warp; i < nseg * GPE; i += kNW) {
@@ -1219,8 +1220,8 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
                 else qk_phase<NT, BITS, NSEG>(kd, ln, bq, f16n, s0, s8);
                 pv_phase<NT, BITS, NSEG>(vd, s0, s8, nv, ln, f16n, ws);
             };
-            if (n > 0) {
-                if (!k_loaded) load_k(kA, pp, tile_at(0), ln, f16n);
+            if (n > 0 && !first_loaded) {
+                load_k(kA, pp, tile_at(0), ln, f16n);
                 load_v(vA, pp, tile_at(0), ln, f16n);
             }
             for (int i = 0; i < n; i += 2) {
@@ -1236,14 +1237,15 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
                 }
                 step(kB, vB, nval_at(i + 1));
             }
-            // the next piece's first keys, in flight during the merge
-            k_loaded = false;
+            // the next piece's first tile, in flight during the merge
+            first_loaded = false;
             if (k + 1 < nseg) {
                 const Seg& sn = S.seg[k + 1];
                 pp = pair_ptr<KB, KN, BITS, NSEG>(a, sn.b, sn.h);
                 if (sn.t_lo + warp < sn.t_hi) {
                     load_k(kA, pp, sn.t_lo + warp, ln, f16n);
-                    k_loaded = true;
+                    load_v(vA, pp, sn.t_lo + warp, ln, f16n);
+                    first_loaded = true;
                 }
             }
             warp_state_out<NT>(ws, ln, S.wo[warp], S.wm[warp], S.wl[warp]);

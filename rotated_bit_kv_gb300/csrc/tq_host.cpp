@@ -189,13 +189,19 @@ const char* tq_status_string(tq_status s) {
     }
 }
 
-int tq_v_crossover(void) {
+int tq_v_crossover(const tq_cache_desc* d) {
     const char* s = getenv("TQ_V_CROSSOVER");
     if (s && *s) {
         long v = strtol(s, nullptr, 10);
         if (v >= 0 && v < (1L << 30)) return (int)v;
     }
-    return 512;
+    // Measured on GB300 for each natural-layout format (16 query heads per KV
+    // head; fp32 norms with 32-wide blocks; fp32 norms with mixed-rate keys) over
+    // T = 64 .. 4096: dimension-parallel accumulation is as fast or faster at
+    // every length (the pages' T = 512 crossover comes from a GPU without the
+    // key-axis split), so the crossover is 0 for all of them.
+    (void)d;
+    return 0;
 }
 
 tq_status tq_codebook(int32_t block_dim, int32_t bits, float* centroids, float* boundaries) {

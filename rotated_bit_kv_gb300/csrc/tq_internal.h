@@ -63,7 +63,8 @@ static inline int tq_v_fmt(const tq_cache_desc* d) {
 #ifdef __cplusplus
 extern "C" {
 #endif
-int tq_v_crossover(void);   // V-mode crossover length (TQ_V_CROSSOVER env, default 512)
+int tq_v_crossover(const tq_cache_desc* d);   // V-mode crossover length of a natural-layout
+                                              // format (TQ_V_CROSSOVER env overrides)
 #ifdef __cplusplus
 }
 #endif

@@ -159,11 +159,13 @@ def test_decode_plan_host_only(tqlib):
     sp, vm = tq.tq_decode_plan(d, 100)
     assert vm == tq.TQ_VMODE_TENSOR and sp == 224                       # 1792 tiles, 8 per CTA (one a warp)
     assert tq.tq_decode_plan(d, 100, tq.TQ_VMODE_TENSOR, 7) == (7, tq.TQ_VMODE_TENSOR)
-    # natural layout (16 query heads per KV head): token-parallel when short
+    # natural layout (16 query heads per KV head): dimension-parallel at every
+    # length (the measured crossover is 0)
     d3 = tq.tq_cache_desc_init(128, 32, 2, 32, 8190, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
     assert d3.layout == tq.TQ_LAYOUT_NATURAL and d3.t_alloc == 8190
     sp, vm = tq.tq_decode_plan(d3, 100)
-    assert vm == tq.TQ_VMODE_TOKEN_PARALLEL and sp <= 2
+    assert vm == tq.TQ_VMODE_DIM_PARALLEL and sp <= 2
+    assert tq.tq_decode_plan(d3, 1)[1] == tq.TQ_VMODE_DIM_PARALLEL
     sp, vm = tq.tq_decode_plan(d3, 8190)
     assert vm == tq.TQ_VMODE_DIM_PARALLEL and 1 <= sp <= tq.TQ_MAX_SPLITS
     with pytest.raises(tq.TQError) as e:
@@ -203,3 +205,24 @@ def test_prefix_workspace_and_argument_checks(tqlib):
     assert call(kp=258) == tqlib.TQ_ERR_INVALID_ARG           # misaligned
     assert call(wsb=w50 - 1) == tqlib.TQ_ERR_WORKSPACE
     assert call(ws=0) == tqlib.TQ_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("fmt", ["g16", "wht32_f32", "mixed_f32"])
+def test_crossover_per_format(tqlib, fmt, monkeypatch):
+    tq = tqlib
+    """Natural-layout formats: dimension-parallel from length 1 (measured crossover
+    0); TQ_V_CROSSOVER = X moves the switch to X (token-parallel at X - 1,
+    dimension-parallel at X)."""
+    if fmt == "g16":
+        d = tq.tq_cache_desc_init(128, 32, 2, 4, 4096, tq.TQ_ROT_WHT128, 3, 3, tq.TQ_F16)
+    elif fmt == "wht32_f32":
+        d = tq.tq_cache_desc_init(128, 32, 8, 4, 4096, tq.TQ_ROT_WHT32, 3, 3, tq.TQ_F32)
+    else:
+        d = tq.tq_cache_desc_init(128, 16, 2, 1, 4096, tq.TQ_ROT_WHT128, 0, 3, tq.TQ_F32, 1)
+    assert d.layout == tq.TQ_LAYOUT_NATURAL
+    monkeypatch.delenv("TQ_V_CROSSOVER", raising=False)
+    for T in (1, 511, 512, 4096):
+        assert tq.tq_decode_plan(d, T)[1] == tq.TQ_VMODE_DIM_PARALLEL
+    monkeypatch.setenv("TQ_V_CROSSOVER", "512")
+    assert tq.tq_decode_plan(d, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
+    assert tq.tq_decode_plan(d, 512)[1] == tq.TQ_VMODE_DIM_PARALLEL

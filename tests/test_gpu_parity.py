@@ -329,8 +329,8 @@ def test_decode_short_and_tile_edges(tq, name, T):
 
 def test_v_mode_plan(tq):
     """Tile-layout caches take the tensor-core kernel at every length (and no
-    CUDA-core kernel); natural-layout caches switch from token- to
-    dimension-parallel V accumulation at the crossover length."""
+    CUDA-core kernel); natural-layout caches take dimension-parallel V
+    accumulation at every length (their measured crossover is 0)."""
     for name in ("so4", "block32_tq3", "block32_tq4", "tiny"):
         st, _ = _encode_on_gpu(tq, name, 1, 8, cap_extra=601)     # any capacity (tiles are padded)
         for T in (8, 511, 512, 600):
@@ -339,11 +339,10 @@ def test_v_mode_plan(tq):
             with pytest.raises(tq.TQError) as e:
                 tq.tq_decode_plan(st.desc, 512, vm)
             assert e.value.status == tq.TQ_ERR_UNSUPPORTED
-    for name in ("llama8b_g16", "block32_f32"):
+    for name in ("llama8b_g16", "block32_f32", "mixed_f32"):
         st, _ = _encode_on_gpu(tq, name, 1, 8, cap_extra=600)
-        X = 512   # the crossover length (TQ_V_CROSSOVER unset)
-        assert tq.tq_decode_plan(st.desc, X - 1)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
-        assert tq.tq_decode_plan(st.desc, X)[1] == tq.TQ_VMODE_DIM_PARALLEL
+        for T in (1, 511, 512):   # measured crossover 0: dimension-parallel at every length
+            assert tq.tq_decode_plan(st.desc, T)[1] == tq.TQ_VMODE_DIM_PARALLEL
         with pytest.raises(tq.TQError) as e:
             tq.tq_decode_plan(st.desc, 512, tq.TQ_VMODE_TENSOR)
         assert e.value.status == tq.TQ_ERR_UNSUPPORTED
