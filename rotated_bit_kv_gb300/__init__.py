@@ -111,6 +111,8 @@ def tq_block_energy(q_cal: np.ndarray, k_cal: np.ndarray) -> np.ndarray:
     q = np.ascontiguousarray(q_cal, dtype=np.float32)
     k = np.ascontiguousarray(k_cal, dtype=np.float32)
     T, G, d = q.shape
+    if k.shape != (T, d):
+        raise ValueError(f"k_cal must be [T][d] = [{T}][{d}] like q_cal's tokens, got {list(k.shape)}")
     s = np.zeros(d // 2, dtype=np.float64)
     _check(lib().tq_block_energy(q.ctypes.data, k.ctypes.data, T, G, d, s.ctypes.data), "tq_block_energy")
     return s

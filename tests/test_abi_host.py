@@ -226,3 +226,11 @@ def test_crossover_per_format(tqlib, fmt, monkeypatch):
     monkeypatch.setenv("TQ_V_CROSSOVER", "512")
     assert tq.tq_decode_plan(d, 511)[1] == tq.TQ_VMODE_TOKEN_PARALLEL
     assert tq.tq_decode_plan(d, 512)[1] == tq.TQ_VMODE_DIM_PARALLEL
+
+
+def test_block_energy_shape_check(tqlib):
+    """The binding refuses calibration keys whose token count differs from the
+    queries' (the C function reads T rows of both)."""
+    q = np.zeros((16, 4, 128), dtype=np.float32)
+    with pytest.raises(ValueError):
+        tqlib.tq_block_energy(q, np.zeros((8, 128), dtype=np.float32))

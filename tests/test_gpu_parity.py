@@ -340,7 +340,8 @@ def test_v_mode_plan(tq):
                 tq.tq_decode_plan(st.desc, 512, vm)
             assert e.value.status == tq.TQ_ERR_UNSUPPORTED
     for name in ("llama8b_g16", "block32_f32", "mixed_f32"):
-        st, _ = _encode_on_gpu(tq, name, 1, 8, cap_extra=600)
+        T0 = 600 if name == "mixed_f32" else 8   # mixed-rate keys calibrate on 512 tokens
+        st, _ = _encode_on_gpu(tq, name, 1, T0, cap_extra=600)
         for T in (1, 511, 512):   # measured crossover 0: dimension-parallel at every length
             assert tq.tq_decode_plan(st.desc, T)[1] == tq.TQ_VMODE_DIM_PARALLEL
         with pytest.raises(tq.TQError) as e:
