@@ -128,8 +128,8 @@ class ClockSampler:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("tq_decode.cu", "tq_decode_tile.cu", "tq_tile.cuh", "tq_decode_common.cuh", "tq_device.cuh",
-              "tq_internal.h"):
+    for f in ("tq_decode.cu", "tq_decode_tile.cu", "tq_tile.cuh", "tq_mma.cuh", "tq_decode_common.cuh",
+              "tq_device.cuh", "tq_internal.h"):
         with open(os.path.join(ROOT, "rotated_bit_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -371,9 +371,13 @@ size_t tq_decode_noalloc_max_scratch_bytes(void);
  * exp in the workspace; the unquantised part is attended in the original domain
  * (scores q k / sqrt(d) in fp32 from the stored values) and the two are merged
  * by log-sum-exp [Block-GTQ, key-axis split with log-sum-exp merge].
- *   k_prefix, v_prefix  device [batch][prefix_capacity][n_kv_heads][128] of
- *                prefix_dtype (TQ_F32, TQ_F16 or TQ_BF16), the layout of
- *                tq_quantize_append's input; may be NULL when max_prefix_len = 0
+ *   k_prefix, v_prefix  device, 16-byte aligned, [batch][prefix_capacity]
+ *                [n_kv_heads][128] of prefix_dtype (TQ_F32, TQ_F16 or TQ_BF16),
+ *                the layout of tq_quantize_append's input; may be NULL when
+ *                max_prefix_len = 0.  Up to 8 query heads per KV head the
+ *                scores and the value sum run on tensor cores with fp16
+ *                operands (bf16 / fp32 values are rounded to fp16: they must
+ *                lie in fp16 range) and fp32 accumulation; above 8, in fp32
  *   d_prefix_lens  device int32 [batch]; values above prefix_capacity or
  *                max_prefix_len are clamped (TQ_DEV_SEQ_OVER_CAPACITY /
  *                TQ_DEV_SEQ_OVER_MAX); 0 = no unquantised token

@@ -39,6 +39,7 @@
 #include <utility>
 
 #include "tq_decode_common.cuh"
+#include "tq_mma.cuh"
 #include "tq_tile.cuh"
 
 namespace {
@@ -56,9 +57,6 @@ constexpr int kMaxGrid = 152 * 8;        // bound on CTAs (sizes the partial slo
 // is this constant, folded into every lookup's immediate offset (the kernel
 // checks it at entry).
 constexpr uint32_t kTabShared = 1024;
-#ifndef TQ_TILE_LAZYMAX
-#define TQ_TILE_LAZYMAX 1
-#endif
 #ifndef TQ_TILE_QKCH
 #define TQ_TILE_QKCH 2   // QK accumulator chains of the one-norm formats (2 or 4)
 #endif
@@ -104,79 +102,6 @@ static_assert(offsetof(SmemMix1, ktab) == 65536 && offsetof(SmemMix2, ktab) == 6
               "key tables must follow the value tables");
 static_assert(offsetof(SmemUni1, wo) % 16 == 0 && offsetof(SmemMix2, wo) % 16 == 0,
               "warp state rows must be 16-byte aligned");
-
-__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-    return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ float ex2(float x) {   // hardware 2^x (ftz); 2^-inf = 0
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint4 ldg_stream4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ldg_stream2(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ldg_u64(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint4 ldg_u128(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-template <class Fn, int... I>
-__device__ __forceinline__ void unroll_seq(Fn&& f, std::integer_sequence<int, I...>) {
-    (f(std::integral_constant<int, I>{}), ...);
-}
-template <int N, class Fn>
-__device__ __forceinline__ void unroll(Fn&& f) {
-    unroll_seq(f, std::make_integer_sequence<int, N>{});
-}
 
 // ---- code-pair table and lookups
 
@@ -420,42 +345,12 @@ __device__ __forceinline__ void load_v(VRegs<BITS, NSEG>& td, const PairPtr& pp,
     }
 }
 
-// Online-softmax state of one warp for NT groups of four heads; lane (r, c) holds
-// head 4j + c: o~ at coordinates 32 mt + 2r + {0, 1, 16, 17} (unnormalised), the
-// running base m (log2 units) and its part of the running sum l.
-template <int NT>
-struct WState {
-    float o[NT][4][4];
-    float m[NT], l[NT];
-    __device__ __forceinline__ void reset() {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            m[j] = -INFINITY;
-            l[j] = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) o[j][mt][0] = o[j][mt][1] = o[j][mt][2] = o[j][mt][3] = 0.f;
-        }
-    }
-};
-
-__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
-__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
-
 // The QK operand B of a lane (uniform-rate keys), in registers.
 template <int NT>
 struct BqT {
     uint32_t r[NT][8][2];
     __device__ __forceinline__ uint2 get(int j, int st) const { return make_uint2(r[j][st][0], r[j][st][1]); }
 };
-
-// fp16 pair of (x, y) (hi = false) or of what the fp16 rounding of (x, y) leaves
-// (hi = true gives the rounded pair itself)
-__device__ __forceinline__ uint32_t pack_part(float x, float y, bool lo) {
-    const uint32_t h = pack_h2(x, y);
-    if (!lo) return h;
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-    return pack_h2(x - f.x, y - f.y);
-}
 
 // QK operand B from q~ ([GPE][128] floats, log2 units) times kinv: lane (r, c), head
 // 4j + r/2; k step st holds coordinates 16 st + 2c, +1 (b0) and 16 st + 2c + 8, +9
@@ -618,47 +513,8 @@ __device__ __forceinline__ void pv_phase(const VRegs<BITS, NSEG>& td, float (&s0
         s8[j] = in8 ? s8[j] : -INFINITY;
     }
 
-    // ---- online softmax: the base moves only when the tile maximum exceeds it by
-    // more than 4 (log2 units), so p <= 16 and rescales are rare
-    bool move = false;
-#if TQ_TILE_LAZYMAX
-    // a tile needs the maximum only when one of its scores passes the base + 4
-#pragma unroll
-    for (int j = 0; j < NT; ++j) move = move || s0[j] > ws.m[j] + 4.f || s8[j] > ws.m[j] + 4.f;
-    if (__any_sync(TQ_FULL_MASK, move)) {
-        float mn[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            float mt = fmaxf(s0[j], s8[j]);
-            mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 4));
-            mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 8));
-            mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 16));
-            mn[j] = mt > ws.m[j] + 4.f ? mt : ws.m[j];
-        }
-#else
-    float mn[NT];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        float mt = fmaxf(s0[j], s8[j]);
-        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 4));
-        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 8));
-        mt = fmaxf(mt, __shfl_xor_sync(TQ_FULL_MASK, mt, 16));
-        mn[j] = mt > ws.m[j] + 4.f ? mt : ws.m[j];
-        move = move || mn[j] != ws.m[j];
-    }
-    if (__any_sync(TQ_FULL_MASK, move)) {
-#endif
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const float cf = ex2(ws.m[j] - mn[j]);   // 0 on the first tile (m = -inf)
-            ws.l[j] *= cf;
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                ws.o[j][mt][0] *= cf; ws.o[j][mt][1] *= cf; ws.o[j][mt][2] *= cf; ws.o[j][mt][3] *= cf;
-            }
-            ws.m[j] = mn[j];
-        }
-    }
+    // ---- online softmax (lazy base: p <= 16, rare rescales)
+    tile_softmax<NT>(s0, s8, ws);
 
     // ---- P operand (k = token-parity pairs, columns = head-parity pairs)
     // After the transposes lane (r, c) holds, for head r/2 (+4j), tokens 2c, 2c+1
@@ -677,11 +533,7 @@ __device__ __forceinline__ void pv_phase(const VRegs<BITS, NSEG>& td, float (&s0
             p0 *= vn0;
             p8 *= vn8;
         }
-        const uint32_t t0 = movtrans(pack_h2(p0, p0)), t1 = movtrans(pack_h2(p8, p8));
-        bp[j][0][0] = prmt(t0, 0u, ln.sel_lo);
-        bp[j][0][1] = prmt(t0, 0u, ln.sel_hi);
-        bp[j][1][0] = prmt(t1, 0u, ln.sel_lo);
-        bp[j][1][1] = prmt(t1, 0u, ln.sel_hi);
+        p_operand(p0, p8, ln.sel_lo, ln.sel_hi, bp[j]);
     }
 
     // ---- PV: group u of the values holds tokens 2c + 8u (A) and 2c + 1 + 8u (B)
@@ -1000,7 +852,11 @@ __device__ __forceinline__ int seq_len_of(const DecodeArgs& a, int b, bool repor
 #ifdef TQ_TILE_MAXNREG
 #define TQ_TILE_BOUNDS __maxnreg__(TQ_TILE_MAXNREG)
 #else
-#define TQ_TILE_BOUNDS __launch_bounds__(kNThr, (NT == 1 && !KMIX) ? TQ_TILE_MINB : 1)
+// two CTAs per SM for four heads and one norm per vector (128 registers); one for
+// eight heads, for four 32-wide blocks (their four block norms and chains spill
+// at 128 registers: one CTA with all registers measured 8 % faster) and for
+// mixed-rate keys (shared memory)
+#define TQ_TILE_BOUNDS __launch_bounds__(kNThr, (NT == 1 && !KMIX && NSEG == 1) ? TQ_TILE_MINB : 1)
 #endif
 // NT: groups of four query heads; BITS, NSEG: code width and norm segments of the
 // values (and of the keys unless KMIX: mixed-rate keys in nibble containers with
@@ -1319,9 +1175,9 @@ int tq_decode_tc_max_grid() { return kMaxGrid; }
 
 int tq_decode_tc_sk_grid(const tq_cache_desc* d, int max_seq_len) {
     // resident CTAs on this device; without one, the design's: 2 (4 query heads
-    // per KV head) or 1 (8) CTAs per SM on 152 SMs
+    // per KV head, one norm per vector) or 1 CTAs per SM on 152 SMs
     int cap = grid_cap(d);
-    if (cap <= 0) cap = (d->group <= 4 && !d->k_mixed ? TQ_TILE_MINB : 1) * 152;
+    if (cap <= 0) cap = (d->group <= 4 && !d->k_mixed && d->rot != TQ_ROT_WHT32 ? TQ_TILE_MINB : 1) * 152;
     // one wave of resident CTAs, each warp with at least one tile
     const long long tiles = (long long)d->batch * d->n_kv_heads * ((max_seq_len + kTok - 1) / kTok);
     long long g = (tiles + kNW - 1) / kNW;

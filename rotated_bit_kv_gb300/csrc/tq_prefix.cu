@@ -24,6 +24,7 @@
 #include <stddef.h>
 
 #include "tq_decode_common.cuh"
+#include "tq_mma.cuh"
 
 namespace {
 
@@ -87,6 +88,56 @@ __device__ __forceinline__ int prefix_len(const PrefixArgs& a, int b, bool repor
     if (L < 0) L = 0;
     if (report && flags && a.status) atomicOr(a.status, flags);
     return L;
+}
+
+// The end of a prefix CTA: ot[g][0..127] (flat, unnormalised) and (sM, sL) hold
+// its section's state.  Sections: publish, the last CTA of the (batch, KV head)
+// merges them all (normalised into ot, (M, L) in sM, sL); one section:
+// normalise.  Then the merge with the packed part:
+//   o = (w_p o_p + w_f L_f o_f) / (w_p + w_f L_f).
+template <int GP, int NTHR>
+__device__ __forceinline__ void prefix_finish(const PrefixArgs& a, float* ot, float* sM, float* sL, int* is_last,
+                                              int b, int h, int s) {
+    const int tid = threadIdx.x;
+    if (a.splits > 1) {
+        float* part = a.ws_part + ((((size_t)b * a.Hkv + h) * a.splits + s) * GP) * kPartStride;
+        for (int i = tid; i < GP * 128; i += NTHR) part[(i >> 7) * kPartStride + (i & 127)] = ot[i];
+        if (tid < GP) {
+            part[tid * kPartStride + 128] = sM[tid];
+            part[tid * kPartStride + 129] = sL[tid];
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const int ticket = atomicAdd(a.tickets + (size_t)b * a.Hkv + h, 1);
+            *is_last = ticket == a.splits - 1;
+        }
+        __syncthreads();
+        if (!*is_last) return;
+        __threadfence();
+        merge_parts<GP, NTHR>(a.ws_part + (((size_t)b * a.Hkv + h) * a.splits * GP) * kPartStride, a.splits,
+                              reinterpret_cast<float(*)[128]>(ot), sM, sL);
+        if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
+        __syncthreads();
+    } else {
+        for (int i = tid; i < GP * 128; i += NTHR) {
+            const int g = i >> 7;
+            ot[i] = sL[g] > 0.f ? ot[i] / sL[g] : 0.f;
+        }
+        __syncthreads();
+    }
+    for (int i = tid; i < a.G * 128; i += NTHR) {
+        const int g = i >> 7;
+        float* dst = a.out + ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128 + (i & 127);
+        const float lp = a.lse_p ? a.lse_p[(size_t)b * a.Hq + (size_t)h * a.G + g] : -INFINITY;
+        const float Mf = sM[g], Lf = sL[g];
+        const float M = fmaxf(lp, Mf);
+        const float wp = lp == -INFINITY ? 0.f : ex2f(lp - M);
+        const float wf = (Mf == -INFINITY || !(Lf > 0.f)) ? 0.f : ex2f(Mf - M) * Lf;
+        const float den = wp + wf;
+        const float op = wp > 0.f ? *dst : 0.f;   // the packed output is read only when it weighs
+        *dst = den > 0.f ? (wp * op + wf * ot[i]) / den : 0.f;
+    }
 }
 
 template <int GP>
@@ -181,67 +232,225 @@ __global__ void __launch_bounds__(kPThr) prefix_attend(PrefixArgs a) {
     }
     __syncthreads();
 
-    // ---- sections: publish, the last CTA merges (normalised into ot, (M, L) in sM, sL)
-    if (a.splits > 1) {
-        float* part = a.ws_part + ((((size_t)b * a.Hkv + h) * a.splits + s) * GP) * kPartStride;
-        for (int i = tid; i < GP * 128; i += kPThr) part[(i >> 7) * kPartStride + (i & 127)] = ot[i];
-        if (tid < GP) {
-            part[tid * kPartStride + 128] = sM[tid];
-            part[tid * kPartStride + 129] = sL[tid];
+    prefix_finish<GP, kPThr>(a, ot, sM, sL, &is_last, b, h, s);
+}
+
+// ---- tensor-core kernel for up to 8 query heads per KV head
+//
+// Each warp takes whole 16-token tiles of its CTA's section, on the legacy
+// warp-level MMA with fp16 operands and fp32 accumulation, in the coordinate-pair
+// form of the packed-cache kernel with the operands read straight from the
+// unquantised rows:
+//   QK: S[16 tok x 8] = K[16 x 128] . B_q[128 x 8], lane (r, c) holding pairs
+//       16c .. 16c+15 of tokens r and r + 8 (64 contiguous bytes each) and B_q the
+//       query (rounded to fp16, and its rounding remainder, in the two columns of
+//       a head) at the same pairs;
+//   PV: O[64 pairs x 8] += V[pairs x (token, parity)] . B_p, m tile mt holding
+//       pairs 8r + 2mt (rows r) and 8r + 2mt + 1 (rows r + 8), so that lane (r, c)
+//       reads pairs 8r .. 8r+7 (32 contiguous bytes) of tokens 2c, 2c+1, 2c+8,
+//       2c+9 and ends with coordinates 16r .. 16r+15 of its head.
+// bf16 and fp32 inputs are rounded to fp16 on load (values must lie in fp16 range).
+constexpr int kTW = 8;
+constexpr int kTThr = kTW * 32;
+
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
+    return pack_h2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+// N fp16 words (2N elements) of the input from element `elem` (16-byte aligned)
+template <int DT, int N>
+__device__ __forceinline__ void load_words(const void* base, size_t elem, uint32_t (&w)[N]) {
+    if constexpr (DT == TQ_F32) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float4 x = __ldg(p + i);
+            w[2 * i] = pack_h2(x.x, x.y);
+            w[2 * i + 1] = pack_h2(x.z, x.w);
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const int ticket = atomicAdd(a.tickets + (size_t)b * a.Hkv + h, 1);
-            is_last = ticket == a.splits - 1;
-        }
-        __syncthreads();
-        if (!is_last) return;
-        __threadfence();
-        merge_parts<GP, kPThr>(a.ws_part + (((size_t)b * a.Hkv + h) * a.splits * GP) * kPartStride, a.splits,
-                               reinterpret_cast<float(*)[128]>(ot), sM, sL);
-        if (tid == 0) a.tickets[(size_t)b * a.Hkv + h] = 0;   // ready for the next call
-        __syncthreads();
     } else {
-        for (int i = tid; i < GP * 128; i += kPThr) {
-            const int g = i >> 7;
-            ot[i] = sL[g] > 0.f ? ot[i] / sL[g] : 0.f;
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            const uint4 x = __ldg(p + i);
+            w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
         }
-        __syncthreads();
+        if constexpr (DT == TQ_BF16) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) w[i] = bf2_to_h2(w[i]);
+        }
+    }
+}
+
+template <int NT, int DT>
+__global__ void __launch_bounds__(kTThr, (NT == 1 && DT == TQ_F16) ? 2 : 1) prefix_tile(PrefixArgs a) {
+    constexpr int GPE = 4 * NT;
+    __shared__ __align__(16) float qf[GPE][128];
+    __shared__ __align__(16) float wo[kTW][GPE][128];
+    __shared__ float wm[kTW][GPE], wl[kTW][GPE];
+    __shared__ float sM[GPE], sL[GPE];
+    __shared__ int is_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int L = prefix_len(a, b, s == 0 && h == 0);
+    const int t0 = s * a.split_len, t1 = min(L, t0 + a.split_len);
+    for (int g = warp; g < GPE; g += kTW) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (g < a.G) tq::load4(a.q, ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128 + 4 * lane, a.q_dtype, v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qf[g][4 * lane + i] = v[i] * (kLog2e * kInvSqrtD);
+    }
+    __syncthreads();
+    const int r = lane >> 2, c = lane & 3;
+    const bool odd = r & 1;
+    uint32_t bq[NT][8][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const float* qh = qf[4 * j + (r >> 1)];
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            const int d0 = 2 * (16 * c + 2 * st);
+            bq[j][st][0] = pack_part(qh[d0], qh[d0 + 1], odd);
+            bq[j][st][1] = pack_part(qh[d0 + 2], qh[d0 + 3], odd);
+        }
+    }
+    const uint32_t sel_lo = odd ? 0x1044u : 0x4410u, sel_hi = odd ? 0x3244u : 0x4432u;
+    WState<NT> ws;
+    ws.reset();
+
+    const int ntile = t1 > t0 ? (t1 - t0 + 15) / 16 : 0;
+    const size_t row = (size_t)a.Hkv * 128;
+    const size_t base = ((size_t)b * a.cap * a.Hkv + h) * 128;
+    auto tok = [&](int tb, int i) { return (size_t)min(tb + i, t1 - 1); };   // past the end: a valid row, weight 0
+    uint32_t kr[16], k8[16], va0[8], vb0[8], va1[8], vb1[8];
+    auto load_k = [&](int tb) {
+        load_words<DT>(a.k, base + tok(tb, r) * row + 32 * c, kr);
+        load_words<DT>(a.k, base + tok(tb, r + 8) * row + 32 * c, k8);
+    };
+    auto load_v = [&](int tb) {
+        load_words<DT>(a.v, base + tok(tb, 2 * c) * row + 16 * r, va0);
+        load_words<DT>(a.v, base + tok(tb, 2 * c + 1) * row + 16 * r, vb0);
+        load_words<DT>(a.v, base + tok(tb, 2 * c + 8) * row + 16 * r, va1);
+        load_words<DT>(a.v, base + tok(tb, 2 * c + 9) * row + 16 * r, vb1);
+    };
+    if (warp < ntile) {
+        load_k(t0 + 16 * warp);
+        load_v(t0 + 16 * warp);
+    }
+    for (int i = warp; i < ntile; i += kTW) {
+        const int tb = t0 + 16 * i, nval = min(16, t1 - tb);
+        float acc[NT][2][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) acc[j][q][0] = acc[j][q][1] = acc[j][q][2] = acc[j][q][3] = 0.f;
+#pragma unroll
+        for (int st = 0; st < 8; ++st)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+                mma16816(acc[j][st & 1], kr[2 * st], k8[2 * st], kr[2 * st + 1], k8[2 * st + 1], bq[j][st][0],
+                         bq[j][st][1]);
+        float s0[NT], s8[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {   // both columns (rounded q and its remainder), both chains
+            s0[j] = r < nval ? (acc[j][0][0] + acc[j][0][1]) + (acc[j][1][0] + acc[j][1][1]) : -INFINITY;
+            s8[j] = r + 8 < nval ? (acc[j][0][2] + acc[j][0][3]) + (acc[j][1][2] + acc[j][1][3]) : -INFINITY;
+        }
+        if (i + kTW < ntile) load_k(tb + 16 * kTW);   // the key registers are free
+        tile_softmax<NT>(s0, s8, ws);
+        uint32_t bp[NT][2][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const float p0 = ex2(s0[j] - ws.m[j]), p8 = ex2(s8[j] - ws.m[j]);
+            ws.l[j] += p0 + p8;
+            p_operand(p0, p8, sel_lo, sel_hi, bp[j]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                mma16816(ws.o[j][mt], va0[2 * mt], va0[2 * mt + 1], vb0[2 * mt], vb0[2 * mt + 1], bp[j][0][0],
+                         bp[j][0][1]);
+                mma16816(ws.o[j][mt], va1[2 * mt], va1[2 * mt + 1], vb1[2 * mt], vb1[2 * mt + 1], bp[j][1][0],
+                         bp[j][1][1]);
+            }
+        if (i + kTW < ntile) load_v(tb + 16 * kTW);
     }
 
-    // ---- merge with the packed part: o = (w_p o_p + w_f L_f o_f) / (w_p + w_f L_f)
-    for (int i = tid; i < a.G * 128; i += kPThr) {
-        const int g = i >> 7;
-        float* dst = a.out + ((size_t)b * a.Hq + (size_t)h * a.G + g) * 128 + (i & 127);
-        const float lp = a.lse_p ? a.lse_p[(size_t)b * a.Hq + (size_t)h * a.G + g] : -INFINITY;
-        const float Mf = sM[g], Lf = sL[g];
-        const float M = fmaxf(lp, Mf);
-        const float wp = lp == -INFINITY ? 0.f : ex2f(lp - M);
-        const float wf = (Mf == -INFINITY || !(Lf > 0.f)) ? 0.f : ex2f(Mf - M) * Lf;
-        const float den = wp + wf;
-        const float op = wp > 0.f ? *dst : 0.f;   // the packed output is read only when it weighs
-        *dst = den > 0.f ? (wp * op + wf * ot[i]) / den : 0.f;
+    // ---- the warps' states into one (m, l, o~) per head (flat in wo[0])
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) ws.l[j] += __shfl_xor_sync(TQ_FULL_MASK, ws.l[j], msk);
+        if (r == 0) {
+            wm[warp][4 * j + c] = ws.m[j];
+            wl[warp][4 * j + c] = ws.l[j];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+            *reinterpret_cast<float4*>(&wo[warp][4 * j + c][16 * r + 4 * mt]) =
+                make_float4(ws.o[j][mt][0], ws.o[j][mt][1], ws.o[j][mt][2], ws.o[j][mt][3]);
     }
+    __syncthreads();
+    float* ot = &wo[0][0][0];
+    for (int i = tid; i < GPE * 128; i += kTThr) {
+        const int g = i >> 7, d = i & 127;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kTW; ++w) M = fmaxf(M, wm[w][g]);
+        float Lt = 0.f, ov = 0.f;
+#pragma unroll
+        for (int w = 0; w < kTW; ++w) {
+            const float wt = (M == -INFINITY || wm[w][g] == -INFINITY) ? 0.f : ex2f(wm[w][g] - M);
+            Lt = fmaf(wt, wl[w][g], Lt);
+            ov = fmaf(wt, wo[w][g][d], ov);
+        }
+        ot[i] = ov;   // wo[0][g][d]: this thread alone reads and writes column (g, d)
+        if (d == 0) {
+            sM[g] = M;
+            sL[g] = Lt;
+        }
+    }
+    __syncthreads();
+    prefix_finish<GPE, kTThr>(a, ot, sM, sL, &is_last, b, h, s);
 }
 
 using PrefixFn = void (*)(PrefixArgs);
 
-PrefixFn pick_prefix(int G) {
-    if (G <= 1) return prefix_attend<1>;
-    if (G <= 4) return prefix_attend<4>;
-    if (G <= 8) return prefix_attend<8>;
+// Up to 8 query heads per KV head: the tensor-core kernel (*tc set); more: the
+// CUDA-core kernel.
+PrefixFn pick_prefix(int G, int dtype, bool* tc) {
+    *tc = G <= 8;
+    if (G <= 4) return dtype == TQ_F16 ? prefix_tile<1, TQ_F16> : dtype == TQ_BF16 ? prefix_tile<1, TQ_BF16>
+                                                                                     : prefix_tile<1, TQ_F32>;
+    if (G <= 8) return dtype == TQ_F16 ? prefix_tile<2, TQ_F16> : dtype == TQ_BF16 ? prefix_tile<2, TQ_BF16>
+                                                                                     : prefix_tile<2, TQ_F32>;
     return prefix_attend<16>;
 }
 
-int gp_of(int G) { return G <= 1 ? 1 : G <= 4 ? 4 : G <= 8 ? 8 : 16; }
+// heads per partial row group: the tensor-core kernel's 4 or 8, the CUDA-core kernel's 16
+int gp_of(int G) { return G <= 4 ? 4 : G <= 8 ? 8 : 16; }
 
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// Sections of the unquantised tokens: enough CTAs to fill the GPU about eight
-// times over (4-warp CTAs), sections of at least 64 tokens.
+// Sections of the tensor-core kernel: 304 CTAs of 8 warps (one wave at two per
+// SM, the fp16 four-head kernel; two waves of the others), sections of at least
+// 128 tokens (a tile per warp), whole tiles.
+int tile_splits(const tq_cache_desc* d, int max_prefix_len) {
+    const long long pairs = (long long)d->batch * d->n_kv_heads;
+    const long long want = (152LL * 2 + pairs - 1) / pairs;
+    long long sp = (max_prefix_len + 127) / 128;
+    if (sp > want) sp = want;
+    if (sp > TQ_MAX_SPLITS) sp = TQ_MAX_SPLITS;
+    return sp < 1 ? 1 : (int)sp;
+}
+
+// Sections of the CUDA-core kernel: enough CTAs to fill the GPU about eight
+// times over (4-warp CTAs), sections of at least 64 tokens.  Never fewer than
+// the tensor-core kernel's, so the workspace sized by these fits both.
 int prefix_splits(const tq_cache_desc* d, int max_prefix_len) {
     const long long pairs = (long long)d->batch * d->n_kv_heads;
     const long long want = (152LL * 8 + pairs - 1) / pairs;
@@ -277,8 +486,8 @@ tq_status tq_decode_attention_prefix(const tq_cache_desc* d, const tq_cache_ptrs
     if (max_seq_len < 0 || max_prefix_len < 0 || prefix_capacity < 0 || max_prefix_len > prefix_capacity)
         return TQ_ERR_INVALID_ARG;
     if (max_prefix_len > 0 && (!k_prefix || !v_prefix)) return TQ_ERR_INVALID_ARG;
-    const size_t pa = prefix_dtype == TQ_F32 ? 16 : 8, qa = q_dtype == TQ_F32 ? 16 : 8;
-    if (!aligned_to(k_prefix, pa) || !aligned_to(v_prefix, pa) || !aligned_to(q, qa) || !aligned_to(out, 16))
+    const size_t qa = q_dtype == TQ_F32 ? 16 : 8;   // the unquantised rows are read in 16-byte pieces
+    if (!aligned_to(k_prefix, 16) || !aligned_to(v_prefix, 16) || !aligned_to(q, qa) || !aligned_to(out, 16))
         return TQ_ERR_INVALID_ARG;
     const size_t need = tq_decode_prefix_workspace_bytes(d, max_prefix_len);
     if (!workspace || workspace_bytes < need || !aligned_to(workspace, 256)) return TQ_ERR_WORKSPACE;
@@ -313,13 +522,16 @@ tq_status tq_decode_attention_prefix(const tq_cache_desc* d, const tq_cache_ptrs
     a.G = d->group;
     a.cap = prefix_capacity;
     a.max_len = max_prefix_len;
-    a.splits = prefix_splits(d, max_prefix_len);
+    bool tc = false;
+    PrefixFn fn = pick_prefix(d->group, prefix_dtype, &tc);
+    a.splits = tc ? tile_splits(d, max_prefix_len) : prefix_splits(d, max_prefix_len);
     a.split_len = (max_prefix_len + a.splits - 1) / a.splits;
+    if (tc) a.split_len = (a.split_len + 15) / 16 * 16;   // whole tiles per section
     a.dtype = prefix_dtype;
     a.q_dtype = q_dtype;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.splits, d->n_kv_heads, d->batch);
-    cfg.blockDim = dim3(kPThr);
+    cfg.blockDim = dim3(tc ? kTThr : kPThr);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr[1];
@@ -327,7 +539,7 @@ tq_status tq_decode_attention_prefix(const tq_cache_desc* d, const tq_cache_ptrs
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pick_prefix(d->group), a) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, fn, a) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 }  // extern "C"
