@@ -672,8 +672,11 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
                                          uint8_t (*ring)[16][kTcRow]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const uint32_t nwarps = gridDim.x * kTcWarps;
-    const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;   // (b, t, h) triples
-    const uint32_t tiles = (total + 7) / 8;
+    // a tile = 8 consecutive tokens of one (batch, KV head): tile = (b Hkv + h) ntt + tt
+    // holds tokens 8 tt .. 8 tt + 7 (those past n_new are loaded clamped, not stored),
+    // so its records fill one half of a 16-token cache tile (consecutive positions)
+    const uint32_t ntt = ((uint32_t)a.n_new + 7) / 8;
+    const uint32_t tiles = (uint32_t)a.B * (uint32_t)a.Hkv * ntt;
     uint32_t tile = blockIdx.x * kTcWarps + (threadIdx.x >> 5);
     if (tile >= tiles) return;
     const int Hkv = a.Hkv, n_new = a.n_new, Tcap = a.Tcap;
@@ -689,20 +692,16 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
         hb[e][1] = pm1_pair<DT>(popc4((4 * c + 2) & j) & 1, popc4((4 * c + 3) & j) & 1);
     }
 
-    // this lane's triple p = 8 tile + g, carried forward by 8 nwarps per pass
-    uint32_t p = tile * 8 + (uint32_t)g;
-    int h, t, b;
-    {
-        const uint32_t q = p / (uint32_t)Hkv;
-        h = (int)(p - q * (uint32_t)Hkv);
-        b = (int)(q / (uint32_t)n_new);
-        t = (int)(q - (uint32_t)b * (uint32_t)n_new);
-    }
-    const uint32_t step = 8u * nwarps;
-    const uint32_t sq = step / (uint32_t)Hkv;
-    const int sh = (int)(step - sq * (uint32_t)Hkv);
-    const int sb = (int)(sq / (uint32_t)n_new);
-    const int st = (int)(sq - (uint32_t)sb * (uint32_t)n_new);
+    // this lane's (batch, token, KV head): token 8 tt + g of the tile
+    int h, t, b, t8;
+    auto locate = [&](uint32_t tl_) {
+        const uint32_t bh = tl_ / ntt;
+        t8 = 8 * (int)(tl_ - bh * ntt);
+        b = (int)(bh / (uint32_t)Hkv);
+        h = (int)(bh - (uint32_t)b * (uint32_t)Hkv);
+        t = t8 + g;
+    };
+    locate(tile);
 
     // the head's sign masks (coordinates 16s + 4c .. +3) and K / V boundaries
     uint32_t msk[8][2];
@@ -726,16 +725,18 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
     };
 
     // The warp's tiles stream through a two-stage ring in shared memory (cp.async,
-    // 16 bytes a lane): rows 0-7 = K, 8-15 = V of triples 8 tl .. 8 tl + 7 (rows past
-    // the last triple repeat it)
-    auto issue = [&](uint32_t tl, int stg) {
-        const uint32_t p0 = tl * 8;
+    // 16 bytes a lane): rows 0-7 = K, 8-15 = V of the tile's 8 tokens (rows past the
+    // last token repeat it)
+    auto issue = [&](uint32_t tl_, int stg) {
+        const uint32_t bh = tl_ / ntt;
+        const int tt8 = 8 * (int)(tl_ - bh * ntt);
+        const uint32_t bb = bh / (uint32_t)Hkv, hh = bh - bb * (uint32_t)Hkv;
+        const size_t row0 = (size_t)bb * n_new * Hkv + hh;   // input row of (bb, token 0, hh)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = lane + 32 * k, row = i >> 4, col = i & 15;
-            uint32_t pp = p0 + (uint32_t)(row & 7);
-            pp = pp < total ? pp : total - 1;
-            const uint16_t* src = (k < 4 ? Ksrc : Vsrc) + (size_t)pp * 128 + col * 8;
+            const int tk = min(tt8 + (row & 7), n_new - 1);
+            const uint16_t* src = (k < 4 ? Ksrc : Vsrc) + (row0 + (size_t)tk * Hkv) * 128 + col * 8;
             const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&ring[stg][row][col * 16]);
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
         }
@@ -749,7 +750,7 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
     asm volatile("cp.async.commit_group;");
 
     for (;;) {
-        const bool valid = p < total;
+        const bool valid = t < n_new;
         if (h != h_loaded) {
             load_head(h);
             h_loaded = h;
@@ -793,8 +794,7 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
         uint32_t pc[8];   // codes of coordinates 16u + 4c .. +3: K at bits 0-11, V at 12-23
 #pragma unroll
         for (int u = 0; u < 8; ++u) pc[u] = 0;
-        uint32_t pn = p + step;
-        const bool more = pn < (tiles * 8u) && pn > p;
+        const bool more = tl + nwarps < tiles && tl + nwarps > tl;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             float acc[8][4];
@@ -938,16 +938,9 @@ __device__ __forceinline__ void qtc_loop(const QuantArgs& a, const float2* tab, 
                 __float2half_rn(c ? vn : kn);
 
         if (!more) break;
-        p = pn;
         tl += nwarps;
         stg ^= 1;
-        h += sh;
-        const int cq = h >= Hkv ? 1 : 0;
-        h -= cq ? Hkv : 0;
-        t += st + cq;
-        const int cb = t >= n_new ? 1 : 0;
-        t -= cb ? n_new : 0;
-        b += sb + cb;
+        locate(tl);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
@@ -964,8 +957,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, 4) tq_quantize_tc(QuantArgs a) 
     __shared__ __align__(16) uint8_t ring[kTcWarps][2][16][kTcRow];
     __shared__ __align__(16) float2 tab[kCells];
     __shared__ int use_tab;
-    const uint32_t total = (uint32_t)a.B * (uint32_t)a.n_new * (uint32_t)a.Hkv;
-    if ((uint32_t)blockIdx.x * kTcWarps * 8 >= total) return;   // no tile for this CTA (uniform)
+    const uint32_t tiles = (uint32_t)a.B * (uint32_t)a.Hkv * (((uint32_t)a.n_new + 7) / 8);
+    if ((uint32_t)blockIdx.x * kTcWarps >= tiles) return;   // no tile for this CTA (uniform)
     if (threadIdx.x == 0) use_tab = 1;
     __syncthreads();
     // one table serves all heads when every head's K and V boundaries equal head 0's K boundaries
@@ -1052,16 +1045,12 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     if (!d->k_mixed && d->rot == TQ_ROT_WHT128 && d->k_bits == 3 && d->v_bits == 3 && d->norm_dtype == TQ_F16 &&
         d->k_norm_slots == 1 && d->v_norm_slots == 1 && (in_dtype == TQ_BF16 || in_dtype == TQ_F16) &&
         aligned(K, 16) && aligned(V, 16) && aligned(c->k_codes, 16) && aligned(c->v_codes, 16) &&
-        triples >= kTcMinTriples) {
-        // whole prompts: 16 vectors per warp through the tensor cores
-        long long tb = ((triples + 7) / 8 + kTcWarps - 1) / kTcWarps;
-        if (tb > kTcMaxBlocks) {
-            // warps loop over the rest; 8 x (warp count) a multiple of the head count
-            // keeps each lane on one KV head
-            tb = kTcMaxBlocks;
-            const int m = d->n_kv_heads / std::gcd(d->n_kv_heads, 8 * kTcWarps);
-            if (tb >= m) tb -= tb % m;
-        }
+        triples >= kTcMinTriples && n_new >= 8) {
+        // whole prompts: 16 vectors (K and V of 8 consecutive tokens of one head) per
+        // warp through the tensor cores; warps loop over the tiles past one grid
+        const long long ttiles = (long long)d->batch * d->n_kv_heads * ((n_new + 7) / 8);
+        long long tb = (ttiles + kTcWarps - 1) / kTcWarps;
+        if (tb > kTcMaxBlocks) tb = kTcMaxBlocks;
         if (in_dtype == TQ_BF16) tq_quantize_tc<TQ_BF16><<<(unsigned)tb, kTcWarps * 32, 0, st>>>(a);
         else tq_quantize_tc<TQ_F16><<<(unsigned)tb, kTcWarps * 32, 0, st>>>(a);
         return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
