@@ -867,6 +867,12 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
     using Smem = TileSmem<GPE, KMIX>;
     constexpr int NP = Smem::NP;
     constexpr int KB = KMIX ? 4 : BITS, KN = KMIX ? 4 : NSEG;
+#ifndef TQ_TILE_DEPTH2
+#define TQ_TILE_DEPTH2 1
+#endif
+    // tiles in flight ahead of the one processed: two where one CTA runs per SM and
+    // registers are left (8 heads, or four 32-wide blocks), else one
+    constexpr int DEPTH = (TQ_TILE_DEPTH2 && !KMIX && (NT == 2 || NSEG == 4)) ? 2 : 1;
     extern __shared__ __align__(128) unsigned char tile_smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>(tile_smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1069,7 +1075,6 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
             const int n = sg.t_hi - sg.t_lo > warp ? (sg.t_hi - sg.t_lo - warp + kNW - 1) / kNW : 0;
             auto tile_at = [&](int i) { return sg.t_lo + warp + kNW * i; };
             auto nval_at = [&](int i) { return min(kTok, sg.L - tile_at(i) * kTok); };
-            // tile i + 1 loads while tile i is processed
             auto step = [&](const KRegs<KB, KN>& kd, const VRegs<BITS, NSEG>& vd, int nv) {
                 float s0[NT], s8[NT];
                 if constexpr (KMIX) qk_phase_mix<NT>(kd, colpack, bmp, kmask, s0, s8);
@@ -1080,18 +1085,48 @@ __global__ void TQ_TILE_BOUNDS decode_tile(DecodeArgs a) {
                 load_k(kA, pp, tile_at(0), ln, f16n);
                 load_v(vA, pp, tile_at(0), ln, f16n);
             }
-            for (int i = 0; i < n; i += 2) {
-                if (i + 1 < n) {
-                    load_k(kB, pp, tile_at(i + 1), ln, f16n);
-                    load_v(vB, pp, tile_at(i + 1), ln, f16n);
+            if constexpr (DEPTH == 2) {
+                // tiles i + 1 and i + 2 in flight while tile i is processed
+                KRegs<KB, KN> kC;
+                VRegs<BITS, NSEG> vC;
+                if (n > 1) {
+                    load_k(kB, pp, tile_at(1), ln, f16n);
+                    load_v(vB, pp, tile_at(1), ln, f16n);
                 }
-                step(kA, vA, nval_at(i));
-                if (i + 1 >= n) break;
-                if (i + 2 < n) {
-                    load_k(kA, pp, tile_at(i + 2), ln, f16n);
-                    load_v(vA, pp, tile_at(i + 2), ln, f16n);
+                for (int i = 0; i < n; i += 3) {
+                    if (i + 2 < n) {
+                        load_k(kC, pp, tile_at(i + 2), ln, f16n);
+                        load_v(vC, pp, tile_at(i + 2), ln, f16n);
+                    }
+                    step(kA, vA, nval_at(i));
+                    if (i + 1 >= n) break;
+                    if (i + 3 < n) {
+                        load_k(kA, pp, tile_at(i + 3), ln, f16n);
+                        load_v(vA, pp, tile_at(i + 3), ln, f16n);
+                    }
+                    step(kB, vB, nval_at(i + 1));
+                    if (i + 2 >= n) break;
+                    if (i + 4 < n) {
+                        load_k(kB, pp, tile_at(i + 4), ln, f16n);
+                        load_v(vB, pp, tile_at(i + 4), ln, f16n);
+                    }
+                    step(kC, vC, nval_at(i + 2));
                 }
-                step(kB, vB, nval_at(i + 1));
+            } else {
+                // tile i + 1 in flight while tile i is processed
+                for (int i = 0; i < n; i += 2) {
+                    if (i + 1 < n) {
+                        load_k(kB, pp, tile_at(i + 1), ln, f16n);
+                        load_v(vB, pp, tile_at(i + 1), ln, f16n);
+                    }
+                    step(kA, vA, nval_at(i));
+                    if (i + 1 >= n) break;
+                    if (i + 2 < n) {
+                        load_k(kA, pp, tile_at(i + 2), ln, f16n);
+                        load_v(vA, pp, tile_at(i + 2), ln, f16n);
+                    }
+                    step(kB, vB, nval_at(i + 1));
+                }
             }
             // the next piece's first tile, in flight during the merge
             first_loaded = false;
