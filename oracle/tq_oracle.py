@@ -27,6 +27,9 @@ the method, in the order the pages give them.  Sources, by page title:
   block energy s_i, objective J(b) = sum_i s_i 4^(-b_i), greedy allocation by
   Delta_i = (3/4) s_i 4^(-b_i), same-width grouping, key-axis split with
   log-sum-exp merge.
+* [ZipFusion] "ZipFusion: Fusing Lossless KV Decompression with Attention for
+  Efficient LLM Decoding" (paper-daily.com): the lossless bf16 block codec
+  (compression format; register restore) and attention on the restored values.
 
 Readings where the pages are silent or ambiguous:
 * density exponent (d-3)/2 (the §2.2 formula; the intuition paragraph's
@@ -627,3 +630,91 @@ def head_specs(wl, inputs, block_bits=None, mats=None):
 def norm_dtype_name(wl) -> str:
     from workloads import F16
     return "f16" if wl.norm_dtype == F16 else "f32"
+
+
+# ============================================================================
+# 8. ZipFusion lossless bf16 block codec  [ZipFusion, compression format and
+#    register restore]
+# ============================================================================
+#
+# A block is 512 bf16 values (their 16-bit patterns).  Its base b is the smallest
+# exponent field rounded down to even; the block compresses iff every exponent
+# lies in [b, b + 15].  A compressed value keeps its low byte (7 mantissa bits
+# and the exponent's lowest bit) and a 4-bit code: the sign and d = (e - b) >> 1.
+# Restore: high byte = 128 sign + b/2 + d.  Codes of a group of 8 consecutive
+# values go two per byte: byte k (k = 0..3) holds value k's sign in bit 7 and d
+# in bits 0-2, value k + 4's sign in bit 6 and d in bits 3-5.
+ZF_BLOCK = 512
+
+
+def zf_exponent(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.int64) >> 7) & 0xFF
+
+
+def zf_base(bits: np.ndarray) -> int:
+    """b: the smallest exponent field of the block, rounded down to even."""
+    return int(zf_exponent(bits).min()) // 2 * 2
+
+
+def zf_compressible(bits: np.ndarray) -> bool:
+    e = zf_exponent(bits)
+    return int(e.max()) <= zf_base(bits) + 15
+
+
+def zf_encode_block(bits: np.ndarray):
+    """(half_base, low[512] uint8, codes[256] uint8) of a compressible block."""
+    bits = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    assert bits.size == ZF_BLOCK and zf_compressible(bits)
+    b = zf_base(bits)
+    e = (bits >> 7) & 0xFF
+    sign = bits >> 15
+    d = (e - b) >> 1
+    low = (bits & 0xFF).astype(np.uint8)
+    codes = np.zeros(ZF_BLOCK // 2, dtype=np.uint8)
+    for g in range(ZF_BLOCK // 8):
+        for k in range(4):
+            i, j = 8 * g + k, 8 * g + k + 4
+            codes[4 * g + k] = (sign[i] << 7) | d[i] | (sign[j] << 6) | (d[j] << 3)
+    return b // 2, low, codes
+
+
+def zf_decode_block(half_base: int, low: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    """The 512 bf16 bit patterns of a compressed block."""
+    out = np.zeros(ZF_BLOCK, dtype=np.uint16)
+    for i in range(ZF_BLOCK):
+        g, k = divmod(i, 8)
+        byte = int(codes[4 * g + (k % 4)])
+        if k < 4:
+            sign, d = byte >> 7, byte & 7
+        else:
+            sign, d = (byte >> 6) & 1, (byte >> 3) & 7
+        hi = 128 * sign + half_base + d
+        out[i] = (hi << 8) | int(low[i])
+    return out
+
+
+def zf_high_bytes(code_byte: int, half_base: int):
+    """High bytes of the two values whose codes share one code byte (the first
+    value of the pair and the one four places later)."""
+    hi1 = 128 * (code_byte >> 7) + half_base + (code_byte & 7)
+    hi5 = 128 * ((code_byte >> 6) & 1) + half_base + ((code_byte >> 3) & 7)
+    return hi1, hi5
+
+
+def zf_page_blocks(page: np.ndarray) -> np.ndarray:
+    """The four 512-value blocks of one 16-token page of one (batch, KV head):
+    page [16][128] bf16 bits -> [4][512]; block j holds tokens 4j .. 4j+3 in
+    (token, coordinate) order."""
+    page = np.asarray(page, dtype=np.uint16)
+    return page.reshape(4, 4 * page.shape[1])
+
+
+def zf_page_roundtrip(page: np.ndarray) -> np.ndarray:
+    """Encode and restore every block of a page (raw blocks as they are)."""
+    out = []
+    for blk in zf_page_blocks(page):
+        if zf_compressible(blk):
+            out.append(zf_decode_block(*zf_encode_block(blk)))
+        else:
+            out.append(blk.copy())
+    return np.concatenate(out).reshape(np.asarray(page).shape)
