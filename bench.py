@@ -689,6 +689,58 @@ def run_prefix(args):
         torch.cuda.empty_cache()
 
 
+def run_zip(args):
+    """ZipFusion store and attention (a table): the llama8b shape at the pages'
+    measured setting (batch 32, 2048 tokens, bf16 K/V with the llama8b channel
+    recipe), and longer contexts.  Time of the attention on the compressed pages
+    and of the same tensor-core attention on the raw bf16 rows (the unquantised-
+    token path with no packed token), cold L2; bytes = what each one reads."""
+    import torch
+
+    import rotated_bit_kv_gb300 as tq
+
+    tq.build()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    print("| workload | B | T | stored / raw bytes | zip attention us | raw bf16 attention us | zip GB/s read | "
+          "of measured peak | raw-equivalent GB/s |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for wl, T in ((W.llama8b_decode(seq_len=2048), 2048), (W.llama8b_decode(seq_len=8192), 8192)):
+        inp = W.make_inputs(wl, seq_len=T)
+        K = _to_torch(torch, inp.K, W.BF16, dev)
+        V = _to_torch(torch, inp.V, W.BF16, dev)
+        q = _to_torch(torch, inp.q, W.BF16, dev)
+        lens = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
+        z = tq.ZipKVCache(wl.batch, wl.n_q_heads, wl.n_kv_heads, T, device=dev)
+        z.store(K, V, lens)
+        torch.cuda.synchronize()
+        if int(z.status.item()) != 0:
+            raise RuntimeError(f"device status {int(z.status.item())}")
+        # bytes the attention reads: every block at its stored size (+ metadata, q, out)
+        stored = 0
+        for meta in (z.k_meta, z.v_meta):
+            m = meta.cpu().numpy().view(np.uint32).reshape(-1, 2)[:, 1]
+            marks = np.stack([(m >> (8 * j)) & 0xFF for j in range(4)])
+            stored += int(np.where(marks == 0xFF, 1024, 768).sum()) + m.size * 8
+        raw = 2 * K.numel() * 2
+        qo = q.numel() * 2 + q.numel() * 4
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        us_z = _cold_launch_us(torch, flush, lambda: z.decode(q, lens, T, out=out), args.steps)
+        # the raw rows through the prefix entry (no packed token)
+        desc = tq.tq_cache_desc_init(128, wl.n_q_heads, wl.n_kv_heads, wl.batch, 16, W.ROT_WHT128, 3, 3, W.F16)
+        blob = tq.tq_params_build(desc, signs=inp.signs[:, :])
+        cache = tq.PackedKVCache(desc, blob, device=dev)
+        zero = torch.zeros(wl.batch, dtype=torch.int32, device=dev)
+        us_r = _cold_launch_us(torch, flush, lambda: cache.decode_prefix(q, zero, 0, K, V, lens, T, out=out), args.steps)
+        gbs = (stored + qo) / (us_z * 1e-6) / 1e9
+        eq = (raw + qo) / (us_z * 1e-6) / 1e9
+        print(f"| {wl.name} (bf16, ZipFusion pages) | {wl.batch} | {T} | {stored / raw:.3f} | {us_z:.1f} | {us_r:.1f} | "
+              f"{gbs:.0f} | {100 * gbs / peak:.1f} % | {eq:.0f} |", flush=True)
+        del z, K, V, cache
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -707,7 +759,11 @@ def main():
                     help="token- against dimension-parallel decode on natural-layout caches (a table)")
     ap.add_argument("--prefix", action="store_true",
                     help="decode over fp16 tokens plus the packed cache (a table)")
+    ap.add_argument("--zip", action="store_true", help="ZipFusion store and attention (a table)")
     args = ap.parse_args()
+    if args.zip:
+        run_zip(args)
+        return
     if args.prefix:
         run_prefix(args)
         return

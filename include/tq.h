@@ -63,6 +63,7 @@ typedef int32_t tq_status;
 #define TQ_DEV_SEQ_OVER_MAX       2  /* seq_len > max_seq_len: clamped         */
 #define TQ_DEV_BAD_POSITION       4  /* append position outside [0, capacity): skipped */
 #define TQ_DEV_INTERNAL           8  /* a kernel's own layout check failed: output not written */
+#define TQ_DEV_BAD_METADATA      16  /* a ZipFusion page offset outside its pool: page 0 read instead */
 
 /* ---------------------------------------------------------------- enums */
 #define TQ_F32   0
@@ -400,6 +401,65 @@ tq_status tq_decode_attention_prefix(const tq_cache_desc* desc, const tq_cache_p
                                      const int32_t* d_prefix_lens, int32_t max_prefix_len,
                                      float* out, void* workspace, size_t workspace_bytes,
                                      int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------- ZipFusion
+ * A lossless store of bf16 K/V and decode attention on it [ZipFusion:
+ * compression format; register restore; attention kernel].
+ *
+ * Pages of 16 tokens of one (batch, KV head), for K and V separately; a page's
+ * 2048 values are four 512-value blocks (block j = tokens 4j .. 4j+3, values in
+ * (token, coordinate) order).  A block whose exponent fields all lie in
+ * [b, b + 15], b = their minimum rounded down to even, is compressed to 768 B:
+ * its 512 low bytes (7 mantissa bits and the exponent's lowest bit), then 256
+ * code bytes, one byte per pair of values of a group of 8 (values g8+k and g8+k+4,
+ * k = 0..3): sign of the first in bit 7 and d = (e - b) >> 1 in bits 0-2, sign of
+ * the second in bit 6 and its d in bits 3-5; restore: high byte = 128 sign + b/2
+ * + d.  Other blocks, and every block of a page that is not full, stay raw (1024 B
+ * of bf16).  Blocks follow one another from the page's offset.  Metadata, 8 bytes
+ * per page: uint32 offset of block 0 from the pool base in 256-byte units, then
+ * one byte per block: b/2, or 0xFF for raw.
+ * Pools hold one 4096-byte slot per page (page (b, h, p) at slot
+ * (b * n_kv_heads + h) * (t_capacity / 16) + p); the metadata offset lets a
+ * memory manager place pages elsewhere (not part of this library). */
+
+/* Bytes of one pool (K or V) and of one metadata array for a store of
+ * t_capacity tokens (a multiple of 16) per (batch, KV head); 0 on bad sizes. */
+size_t tq_zip_pool_bytes(int32_t batch, int32_t n_kv_heads, int32_t t_capacity);
+size_t tq_zip_meta_bytes(int32_t batch, int32_t n_kv_heads, int32_t t_capacity);
+
+/* Store the first d_lens[b] tokens of K and V of every sequence as pages.
+ *   K, V        device bf16 [batch][n_tokens][n_kv_heads][128], 16-byte aligned
+ *   d_lens      device int32 [batch]; values above t_capacity or n_tokens are
+ *               clamped (TQ_DEV_SEQ_OVER_CAPACITY)
+ *   k_pool, v_pool  device, 256-byte aligned, tq_zip_pool_bytes each
+ *   k_meta, v_meta  device, 8-byte aligned, tq_zip_meta_bytes each; pages past
+ *               a sequence's length are not written
+ * Errors: TQ_ERR_INVALID_ARG (NULL, misaligned, sizes), TQ_ERR_CUDA. */
+tq_status tq_zip_store(const void* K, const void* V, int32_t batch, int32_t n_kv_heads, int32_t n_tokens,
+                       int32_t t_capacity, const int32_t* d_lens, void* k_pool, void* v_pool, void* k_meta,
+                       void* v_meta, int32_t* d_status, void* stream);
+
+/* Workspace of tq_zip_decode_attention (0: unsupported shape). */
+size_t tq_zip_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t max_seq_len);
+
+/* Decode attention over stored pages: softmax(q K^T / sqrt(128)) V over the first
+ * d_seq_lens[b] tokens, the blocks restored in registers and fed to the tensor
+ * cores (fp16 operands, fp32 accumulation; bf16 values must lie in fp16 range).
+ *   q           device [batch][n_q_heads][128] of q_dtype; at most 8 query heads
+ *               per KV head (else TQ_ERR_UNSUPPORTED)
+ *   d_seq_lens  device int32 [batch] (clamped to max_seq_len and t_capacity; the
+ *               pages read must have been stored); max_seq_len 1 .. t_capacity
+ *   workspace   tq_zip_workspace_bytes, 256-byte aligned, zero-filled before its
+ *               first use (every call leaves it so)
+ *   out         device fp32 [batch][n_q_heads][128]
+ * A page offset outside its pool reads page 0 and ORs TQ_DEV_BAD_METADATA.
+ * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_zip_decode_attention(const void* q, int32_t q_dtype, int32_t batch, int32_t n_q_heads,
+                                  int32_t n_kv_heads, int32_t t_capacity, const void* k_pool,
+                                  const void* v_pool, const void* k_meta, const void* v_meta,
+                                  const int32_t* d_seq_lens, int32_t max_seq_len, float* out,
+                                  void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                  void* stream);
 
 /* Workspace bytes of tq_decode_attention_prefix for at most max_prefix_len
  * unquantised tokens per sequence (0 on a bad descriptor). */

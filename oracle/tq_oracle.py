@@ -701,20 +701,54 @@ def zf_high_bytes(code_byte: int, half_base: int):
     return hi1, hi5
 
 
-def zf_page_blocks(page: np.ndarray) -> np.ndarray:
+def zf_block_groups(which: str):
+    """The page's four blocks as lists of 64 groups of 8 values, in the order a
+    block stores them: [4][64] of (token, first coordinate).  The pages keep each
+    MMA thread's 8 values together and lay K and V out for their own products
+    ([ZipFusion], register restore); here the groups a lane (r, c) reads at one
+    step of the attention form one block, so that a block's mode is the same for
+    the whole warp:
+      K block q (q = 0..3): group 2L + u, L = 4r + c, is token r + 8u, coordinates
+        32c + 8q .. +7 (the lane's keys of tokens r and r + 8);
+      V block 2e + q (e, q = 0, 1): group 2L + u is token 8e + 2c + u, coordinates
+        16r + 8q .. +7 (the lane's values of tokens 2c + 8e and 2c + 8e + 1)."""
+    out = []
+    for j in range(4):
+        grp = []
+        for L in range(32):
+            r, c = L >> 2, L & 3
+            for u in range(2):
+                if which == "k":
+                    grp.append((r + 8 * u, 32 * c + 8 * j))
+                else:
+                    e, q = j >> 1, j & 1
+                    grp.append((8 * e + 2 * c + u, 16 * r + 8 * q))
+        out.append(grp)
+    return out
+
+
+def zf_page_blocks(page: np.ndarray, which: str) -> np.ndarray:
     """The four 512-value blocks of one 16-token page of one (batch, KV head):
-    page [16][128] bf16 bits -> [4][512]; block j holds tokens 4j .. 4j+3 in
-    (token, coordinate) order."""
+    page [16][128] bf16 bits -> [4][512] in block order (zf_block_groups)."""
     page = np.asarray(page, dtype=np.uint16)
-    return page.reshape(4, 4 * page.shape[1])
+    return np.stack([np.concatenate([page[t, d0:d0 + 8] for t, d0 in grp]) for grp in zf_block_groups(which)])
 
 
-def zf_page_roundtrip(page: np.ndarray) -> np.ndarray:
+def zf_page_unblocks(blocks: np.ndarray, which: str) -> np.ndarray:
+    """Inverse of zf_page_blocks."""
+    page = np.zeros((16, 128), dtype=np.uint16)
+    for j, grp in enumerate(zf_block_groups(which)):
+        for g, (t, d0) in enumerate(grp):
+            page[t, d0:d0 + 8] = blocks[j][8 * g:8 * g + 8]
+    return page
+
+
+def zf_page_roundtrip(page: np.ndarray, which: str) -> np.ndarray:
     """Encode and restore every block of a page (raw blocks as they are)."""
     out = []
-    for blk in zf_page_blocks(page):
+    for blk in zf_page_blocks(page, which):
         if zf_compressible(blk):
             out.append(zf_decode_block(*zf_encode_block(blk)))
         else:
             out.append(blk.copy())
-    return np.concatenate(out).reshape(np.asarray(page).shape)
+    return zf_page_unblocks(np.stack(out), which)

@@ -19,6 +19,7 @@ from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_NO_CONVERGENCE, TQ_ERR_WORKSPACE = range(6)
 TQ_DEV_SEQ_OVER_CAPACITY, TQ_DEV_SEQ_OVER_MAX, TQ_DEV_BAD_POSITION, TQ_DEV_INTERNAL = 1, 2, 4, 8
+TQ_DEV_BAD_METADATA = 16
 TQ_F32, TQ_F16, TQ_BF16 = 0, 1, 2
 TQ_ROT_WHT128, TQ_ROT_WHT32, TQ_ROT_SO4_WHT128 = 0, 1, 2
 TQ_PART_K_CODES, TQ_PART_K_NORMS, TQ_PART_V_CODES, TQ_PART_V_NORMS, TQ_PART_PARAMS = range(5)
@@ -70,6 +71,12 @@ _SIGS = {
     "tq_decode_attention_prefix": (_I, [ctypes.POINTER(tq_cache_desc), ctypes.POINTER(tq_cache_ptrs), _P, _I, _P,
                                         _I, _P, _P, _I, _I, _P, _I, _P, _P, ctypes.c_size_t, _P, _P]),
     "tq_decode_prefix_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(tq_cache_desc), _I]),
+    "tq_zip_pool_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "tq_zip_meta_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "tq_zip_store": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "tq_zip_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "tq_zip_decode_attention": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, ctypes.c_size_t, _P,
+                                     _P]),
 }
 
 
@@ -268,6 +275,72 @@ def tq_decode_attention_prefix(desc: tq_cache_desc, cache: tq_cache_ptrs, q, seq
                                             _ptr(seq_lens), int(max_seq_len), _ptr(k_prefix), _ptr(v_prefix), pdt,
                                             cap, _ptr(prefix_lens), int(max_prefix_len), _ptr(out), _ptr(workspace),
                                             nbytes, _ptr(status), _stream(stream)), "tq_decode_attention_prefix")
+
+
+def tq_zip_pool_bytes(batch: int, n_kv_heads: int, t_capacity: int) -> int:
+    return int(lib().tq_zip_pool_bytes(int(batch), int(n_kv_heads), int(t_capacity)))
+
+
+def tq_zip_meta_bytes(batch: int, n_kv_heads: int, t_capacity: int) -> int:
+    return int(lib().tq_zip_meta_bytes(int(batch), int(n_kv_heads), int(t_capacity)))
+
+
+def tq_zip_workspace_bytes(batch: int, n_q_heads: int, n_kv_heads: int, max_seq_len: int) -> int:
+    return int(lib().tq_zip_workspace_bytes(int(batch), int(n_q_heads), int(n_kv_heads), int(max_seq_len)))
+
+
+def tq_zip_store(K, V, lens, t_capacity: int, k_pool, v_pool, k_meta, v_meta, status=None, stream=None):
+    """K, V: CUDA bf16 [batch][n_tokens][n_kv][128]; lens CUDA int32 [batch]."""
+    _require_cuda(K, V, lens, k_pool, v_pool, k_meta, v_meta, status)
+    torch = _torch()
+    if K.dtype != torch.bfloat16 or V.dtype != torch.bfloat16 or K.shape != V.shape:
+        raise TypeError("K and V must be bf16 tensors of one shape")
+    B, T, Hkv, d = K.shape
+    _check(lib().tq_zip_store(_ptr(K), _ptr(V), B, Hkv, T, int(t_capacity), _ptr(lens), _ptr(k_pool), _ptr(v_pool),
+                              _ptr(k_meta), _ptr(v_meta), _ptr(status), _stream(stream)), "tq_zip_store")
+
+
+def tq_zip_decode_attention(q, n_kv_heads: int, t_capacity: int, k_pool, v_pool, k_meta, v_meta, seq_lens,
+                            max_seq_len: int, out, workspace, status=None, stream=None):
+    _require_cuda(q, k_pool, v_pool, k_meta, v_meta, seq_lens, out, workspace, status)
+    B, Hq, d = q.shape
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().tq_zip_decode_attention(_ptr(q), _dtype_code(q), B, Hq, int(n_kv_heads), int(t_capacity),
+                                         _ptr(k_pool), _ptr(v_pool), _ptr(k_meta), _ptr(v_meta), _ptr(seq_lens),
+                                         int(max_seq_len), _ptr(out), _ptr(workspace), nbytes, _ptr(status),
+                                         _stream(stream)), "tq_zip_decode_attention")
+
+
+class ZipKVCache:
+    """Device buffers of a ZipFusion store (pools, metadata, workspace, status),
+    allocated through PyTorch."""
+
+    def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, t_capacity: int, device="cuda"):
+        torch = _torch()
+        self.batch, self.n_q_heads, self.n_kv_heads, self.t_capacity = batch, n_q_heads, n_kv_heads, t_capacity
+        self.device = torch.device(device)
+
+        def buf(n):
+            return torch.zeros(max(int(n), 16), dtype=torch.uint8, device=self.device)
+
+        self.k_pool = buf(tq_zip_pool_bytes(batch, n_kv_heads, t_capacity))
+        self.v_pool = buf(tq_zip_pool_bytes(batch, n_kv_heads, t_capacity))
+        self.k_meta = buf(tq_zip_meta_bytes(batch, n_kv_heads, t_capacity))
+        self.v_meta = buf(tq_zip_meta_bytes(batch, n_kv_heads, t_capacity))
+        self.workspace = buf(tq_zip_workspace_bytes(batch, n_q_heads, n_kv_heads, t_capacity))
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def store(self, K, V, lens, stream=None):
+        tq_zip_store(K, V, lens, self.t_capacity, self.k_pool, self.v_pool, self.k_meta, self.v_meta, self.status,
+                     stream)
+
+    def decode(self, q, seq_lens, max_seq_len, out=None, stream=None):
+        torch = _torch()
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        tq_zip_decode_attention(q, self.n_kv_heads, self.t_capacity, self.k_pool, self.v_pool, self.k_meta,
+                                self.v_meta, seq_lens, max_seq_len, out, self.workspace, self.status, stream)
+        return out
 
 
 # ---------------------------------------------------------------- allocation helper

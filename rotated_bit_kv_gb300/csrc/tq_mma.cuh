@@ -4,6 +4,7 @@
 // streaming loads, compile-time unrolling.  Internal linkage: included by one
 // translation unit per kernel family.
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -29,6 +30,20 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
+}
+
+// the same MMA with bf16 operands (A and B both bf16)
+__device__ __forceinline__ void mma16816_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -82,6 +97,13 @@ __device__ __forceinline__ void unroll_seq(Fn&& f, std::integer_sequence<int, I.
 template <int N, class Fn>
 __device__ __forceinline__ void unroll(Fn&& f) {
     unroll_seq(f, std::make_integer_sequence<int, N>{});
+}
+
+// bf16 pair of (x, y) (lo = false) or of what its bf16 rounding leaves (lo = true)
+__device__ __forceinline__ uint32_t pack_part_bf(float x, float y, bool lo) {
+    const uint32_t h = pack_bf2(x, y);
+    if (!lo) return h;
+    return pack_bf2(x - __uint_as_float(h << 16), y - __uint_as_float(h & 0xffff0000u));
 }
 
 // fp16 pair of (x, y) (lo = false) or of what the fp16 rounding of (x, y)
@@ -151,6 +173,15 @@ __device__ __forceinline__ void tile_softmax(const float (&s0)[NT], const float 
 // r + 8 (lane (r, c), head 4j + c): after the 8x8 transposes lane (r, c) holds, for
 // head r/2, tokens 2c, 2c+1 (k step 0: b0, b1) and 2c+8, 2c+9 (k step 1), each
 // weight in the column of its parity (selectors sel_lo / sel_hi of the lane).
+__device__ __forceinline__ void p_operand_words(uint32_t w0, uint32_t w8, uint32_t sel_lo, uint32_t sel_hi,
+                                                uint32_t (&bp)[2][2]) {
+    const uint32_t t0 = movtrans(w0), t1 = movtrans(w8);
+    bp[0][0] = prmt(t0, 0u, sel_lo);
+    bp[0][1] = prmt(t0, 0u, sel_hi);
+    bp[1][0] = prmt(t1, 0u, sel_lo);
+    bp[1][1] = prmt(t1, 0u, sel_hi);
+}
+
 __device__ __forceinline__ void p_operand(float p0, float p8, uint32_t sel_lo, uint32_t sel_hi, uint32_t (&bp)[2][2]) {
     const uint32_t t0 = movtrans(pack_h2(p0, p0)), t1 = movtrans(pack_h2(p8, p8));
     bp[0][0] = prmt(t0, 0u, sel_lo);

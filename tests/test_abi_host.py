@@ -234,3 +234,28 @@ def test_block_energy_shape_check(tqlib):
     q = np.zeros((16, 4, 128), dtype=np.float32)
     with pytest.raises(ValueError):
         tqlib.tq_block_energy(q, np.zeros((8, 128), dtype=np.float32))
+
+
+def test_zip_sizes_and_argument_checks(tqlib):
+    """ZipFusion host side: a 4096-byte slot and 8 metadata bytes per 16-token page;
+    capacities not a multiple of 16 and more than 8 query heads per KV head are
+    refused before any device work."""
+    assert tqlib.tq_zip_pool_bytes(2, 8, 64) == 2 * 8 * 4 * 4096
+    assert tqlib.tq_zip_meta_bytes(2, 8, 64) == 2 * 8 * 4 * 8
+    assert tqlib.tq_zip_pool_bytes(2, 8, 65) == 0
+    assert tqlib.tq_zip_workspace_bytes(2, 32, 8, 64) > 0
+    assert tqlib.tq_zip_workspace_bytes(2, 32, 2, 64) == 0          # 16 heads per KV head
+    h = tqlib.lib()
+    ws = tqlib.tq_zip_workspace_bytes(2, 32, 8, 64)
+    args = [256, tqlib.TQ_BF16, 2, 32, 8, 64, 256, 256, 256, 256, 256, 64, 256, 256, ws, None, None]
+
+    def call(i, v):
+        a = list(args)
+        a[i] = v
+        return h.tq_zip_decode_attention(*a)
+    assert call(5, 65) == tqlib.TQ_ERR_INVALID_ARG                   # capacity not whole pages
+    assert call(11, 65) == tqlib.TQ_ERR_INVALID_ARG                  # max_seq_len above capacity
+    assert call(4, 2) == tqlib.TQ_ERR_UNSUPPORTED                    # 16 query heads per KV head
+    assert call(14, ws - 1) == tqlib.TQ_ERR_WORKSPACE
+    assert call(6, 128) == tqlib.TQ_ERR_INVALID_ARG                  # pool not 256-byte aligned
+    assert h.tq_zip_store(256, 256, 2, 8, 0, 64, 256, 256, 256, 256, 256, None, None) == tqlib.TQ_ERR_INVALID_ARG

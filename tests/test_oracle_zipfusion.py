@@ -93,14 +93,31 @@ def test_high_byte_identity():
         assert half + d == e[i] >> 1 <= 127
 
 
-def test_page_is_four_blocks_and_round_trips():
+@pytest.mark.parametrize("which", ["k", "v"])
+def test_page_is_four_blocks_and_round_trips(which):
     """A 16-token page of one head (128 coordinates) is four 512-value blocks (the
-    pages: four key blocks per head and page); incompressible blocks stay raw."""
+    pages: four key blocks per head and page) that partition it; incompressible
+    blocks stay raw and the page restores exactly."""
     rng = np.random.default_rng(6)
     page = (rng.standard_normal((16, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
-    page[12, 3] = bf16(0, 3, 1)                     # block 3 spans exponents far apart
-    blocks = O.zf_page_blocks(page)
+    page[12, 3] = bf16(0, 3, 1)                     # one block spans exponents far apart
+    blocks = O.zf_page_blocks(page, which)
     assert blocks.shape == (4, 512)
-    np.testing.assert_array_equal(blocks[1], page[4:8].reshape(-1))
-    assert not O.zf_compressible(blocks[3])
-    np.testing.assert_array_equal(O.zf_page_roundtrip(page), page)
+    seen = np.zeros((16, 128), dtype=int)
+    for grp in O.zf_block_groups(which):
+        for t, d0 in grp:
+            seen[t, d0:d0 + 8] += 1
+    assert np.all(seen == 1)
+    np.testing.assert_array_equal(O.zf_page_unblocks(blocks, which), page)
+    assert sum(not O.zf_compressible(b) for b in blocks) == 1
+    np.testing.assert_array_equal(O.zf_page_roundtrip(page, which), page)
+
+
+def test_block_groups_follow_the_lanes():
+    """Block q of K holds lane (r, c)'s keys of tokens r and r + 8 at coordinates
+    32c + 8q .. +7, next to each other; V block 2e + q lane (r, c)'s values of
+    tokens 2c + 8e and 2c + 8e + 1 at coordinates 16r + 8q .. +7."""
+    gk, gv = O.zf_block_groups("k"), O.zf_block_groups("v")
+    L = 4 * 5 + 3   # lane r = 5, c = 3
+    assert gk[2][2 * L] == (5, 32 * 3 + 16) and gk[2][2 * L + 1] == (13, 32 * 3 + 16)
+    assert gv[3][2 * L] == (8 + 6, 16 * 5 + 8) and gv[3][2 * L + 1] == (8 + 7, 16 * 5 + 8)
