@@ -14,6 +14,9 @@ the method, in the order the pages give them.  Sources, by page title:
   §2.2 the coordinate density after a random rotation, f(t) ~ (1-t^2)^((d-3)/2);
   §2.3 the Lloyd-Max codebook (centroid / midpoint conditions) and the
        MSE <= 2.7/4^b bound;
+  §2.4 the two-stage key code for 1-2 bits: a (b-1)-bit MSE code plus a 1-bit
+       QJL code (signs of a random projection) of its residual, for an
+       unbiased inner product;
   §3.1 Hadamard with a +-1 sign flip in place of a random orthogonal matrix,
        32-wide blocks with their own norm;
   §3.3 8 three-bit indices in 3 bytes, two four-bit indices per byte,
@@ -47,7 +50,11 @@ Readings where the pages are silent or ambiguous:
   is encoded by one TQ-MSE encoder with its own random orthogonal matrix, its
   own norm and the codebook for its own width; groups are laid out in ascending
   bit width, one index per nibble;
-* attention scale 1/sqrt(head_dim); greedy ties go to the lowest block index.
+* attention scale 1/sqrt(head_dim); greedy ties go to the lowest block index;
+* two-stage keys: the residual is taken in the rotated, normalised domain of the
+  MSE stage (r = y - C[idx]); the projection S (d x d, i.i.d. N(0, 1)) is an
+  input; sign(0) counts as +1; the stored norms are n and n * ||r||; the
+  estimator is the sign projection's unbiased one, ||r|| sqrt(pi/2)/d <S q~, sign>.
 """
 from __future__ import annotations
 
@@ -752,3 +759,134 @@ def zf_page_roundtrip(page: np.ndarray, which: str) -> np.ndarray:
         else:
             out.append(blk.copy())
     return zf_page_unblocks(np.stack(out), which)
+
+
+# ============================================================================
+# 9. Two-stage key code: a (b-1)-bit MSE code and a 1-bit QJL code of its
+#    residual  [TQ-MNN §2.4]
+# ============================================================================
+#
+# An MSE-optimal code shrinks inner products.  For keys at 1-2 bits the page
+# spends b - 1 bits on the MSE code and the last bit on a quantised
+# Johnson-Lindenstrauss code of what the MSE code leaves over: the signs of a
+# random Gaussian projection, which give an unbiased estimate of <q, k>.
+# The estimator written out here is the standard one for a sign projection:
+# for s ~ N(0, I_d), E[<s, a> sign(<s, r>)] = sqrt(2/pi) <a, r> / ||r||, so with
+# the d rows of S and rho = ||r||,
+#   <a, r>  ~=  rho * sqrt(pi/2) / d * <S a, sign(S r)>    (unbiased).
+# Everything stays in the rotated, normalised domain of the MSE stage: y = R x /
+# ||x||, r = y - C[idx], and q~ = R q as in the one-stage path.
+
+
+@dataclass
+class QjlSpec:
+    """One KV head's two-stage key code: rotation R (as the one-stage spec),
+    MSE bits b - 1 (0: no MSE code, the whole normalised vector goes to the QJL
+    stage) and the d x d projection S with i.i.d. N(0, 1) entries."""
+    R: np.ndarray
+    mse_bits: int
+    S: np.ndarray
+
+
+def qjl_scale(d: int) -> float:
+    """sqrt(pi/2) / d, the factor that makes the sign estimate unbiased."""
+    return math.sqrt(math.pi / 2.0) / d
+
+
+def qjl_quantize(x: np.ndarray, qs: QjlSpec, norm_dtype: str):
+    """Encode keys x [N][d]: n = ||x||; y = R x / n; idx = #{k : y > beta_k} on
+    the (b-1)-bit codebook (all 0 and no reconstruction when b = 1); r = y -
+    C[idx]; rho = ||r||; z = S r; sign bit = 1 where z >= 0 (the reading of
+    sign(0) is +1).  Stored norms: slot 0 n, slot 1 n * rho (rounded to the norm
+    dtype).  Returns (idx [N][d], sign bits [N][d] 0/1, norms [N][2], y, z)."""
+    x = np.asarray(x, dtype=np.float64)
+    N, d = x.shape
+    n = np.sqrt(np.sum(x * x, axis=1))
+    with np.errstate(invalid="ignore", divide="ignore"):
+        y = np.where(n[:, None] > 0, (x @ qs.R.T) / n[:, None], 0.0)
+    if qs.mse_bits > 0:
+        cb = codebook(d, qs.mse_bits)
+        idx = codebook_search(y, cb)
+        yhat = cb.centroids[idx]
+    else:
+        idx = np.zeros((N, d), dtype=np.int64)
+        yhat = np.zeros((N, d))
+    r = y - yhat
+    rho = np.sqrt(np.sum(r * r, axis=1))
+    z = r @ np.asarray(qs.S, dtype=np.float64).T
+    sbits = (z >= 0).astype(np.int64)
+    norms = np.stack([n, n * rho], axis=1)
+    return idx, sbits, round_norm(norms, norm_dtype), y, z
+
+
+def qjl_record_bytes(mse_bits: int, d: int = 128) -> int:
+    """(b - 1) * d / 8 bytes of MSE codes, then d / 8 bytes of signs."""
+    return (mse_bits + 1) * d // 8
+
+
+def pack_bits(v: np.ndarray, width: int) -> np.ndarray:
+    """Fields of `width` bits, LSB first: field i at bits [width i, width (i+1))
+    of the little-endian byte stream."""
+    v = np.asarray(v, dtype=np.int64)
+    N, d = v.shape
+    bits = np.zeros((N, d * width), dtype=np.uint8)
+    for k in range(width):
+        bits[:, k::width] = (v >> k) & 1
+    return np.packbits(bits, axis=1, bitorder="little")
+
+
+def unpack_bits(b: np.ndarray, width: int, d: int) -> np.ndarray:
+    bits = np.unpackbits(np.asarray(b, dtype=np.uint8), axis=1, bitorder="little").astype(np.int64)
+    v = np.zeros((bits.shape[0], d), dtype=np.int64)
+    for k in range(width):
+        v |= bits[:, k:d * width:width] << k
+    return v
+
+
+def qjl_pack(idx: np.ndarray, sbits: np.ndarray, mse_bits: int) -> np.ndarray:
+    """One record per key: the MSE codes (mse_bits each, LSB first), then the d
+    sign bits (bit j of the sign bytes = sign of z_j)."""
+    parts = [pack_bits(idx, mse_bits)] if mse_bits > 0 else []
+    parts.append(pack_bits(sbits, 1))
+    return np.concatenate(parts, axis=1)
+
+
+def qjl_unpack(codes: np.ndarray, mse_bits: int, d: int = 128):
+    codes = np.asarray(codes, dtype=np.uint8)
+    nb = mse_bits * d // 8
+    idx = unpack_bits(codes[:, :nb], mse_bits, d) if mse_bits > 0 else np.zeros((codes.shape[0], d), np.int64)
+    return idx, unpack_bits(codes[:, nb:nb + d // 8], 1, d)
+
+
+def qjl_scores(q: np.ndarray, idx, sbits, norms, qs: QjlSpec) -> np.ndarray:
+    """Estimated <q_g, k_j> [G][N]:
+      n_j <q~, C[idx_j]> + (n_j rho_j) sqrt(pi/2)/d <S q~, 2 sbits_j - 1>,
+    q~ = R q; the first term is absent when b = 1."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    nrm = np.asarray(norms, dtype=np.float64)
+    qt = q @ qs.R.T
+    if qs.mse_bits > 0:
+        C = codebook(d, qs.mse_bits).centroids
+        mse = (qt @ C[idx].T) * nrm[:, 0][None, :]
+    else:
+        mse = np.zeros((q.shape[0], idx.shape[0]))
+    u = qt @ np.asarray(qs.S, dtype=np.float64).T               # S q~
+    sg = 2.0 * np.asarray(sbits, dtype=np.float64) - 1.0
+    return mse + qjl_scale(d) * (u @ sg.T) * nrm[:, 1][None, :]
+
+
+def attend_qjl(q, k_idx, k_sbits, k_norm, qs: QjlSpec, v_idx, v_norm, v_spec: HeadSpec, seq_len: int):
+    """Decode attention of one (batch, KV head) with two-stage keys: scores are
+    the estimates of qjl_scores over sqrt(d); values as in attend_rotated
+    (rotated domain, one inverse rotation)."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    L = int(seq_len)
+    if L <= 0:
+        return np.zeros_like(q)
+    s = qjl_scores(q, k_idx[:L], k_sbits[:L], k_norm[:L], qs) / math.sqrt(d)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    a = p / p.sum(axis=1, keepdims=True)
+    Vt = dequantize_rotated(v_idx[:L], v_norm[:L], v_spec)
+    return (a @ Vt) @ v_spec.R
