@@ -741,6 +741,51 @@ def run_zip(args):
         torch.cuda.empty_cache()
 
 
+def run_two_stage(args):
+    """Two-stage keys (a (k_bits - 1)-bit MSE code plus a 1-bit QJL code of the
+    residual) on the llama8b head shape (a table): the whole-prompt append and the
+    decode (CUDA-core kernels on the natural layout, the library's plan), cold L2;
+    bytes = K and V records and norms read + q + out."""
+    import torch
+
+    import rotated_bit_kv_gb300 as tq
+
+    tq.build()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    print("| workload | B | T | K bytes / token-head | plan (splits, V mode) | append us | decode us | GB/s | "
+          "of measured peak |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for k_bits in (1, 2):
+        wl = W.two_stage_keys(k_bits, seq_len=args.seq_len, batch=8)
+        T = wl.seq_len
+        inp = W.make_inputs(wl, seq_len=T)
+        desc = tq.tq_cache_desc_init(128, wl.n_q_heads, wl.n_kv_heads, wl.batch, T, wl.rot, wl.k_bits, wl.v_bits,
+                                     wl.norm_dtype)
+        S = np.stack([W.two_stage_projection(128, wl.seed, h) for h in range(wl.n_kv_heads)])
+        cache = tq.PackedKVCache(desc, tq.tq_params_build(desc, signs=inp.signs, k_group_mats=S), device=dev)
+        K = _to_torch(torch, inp.K, W.BF16, dev)
+        V = _to_torch(torch, inp.V, W.BF16, dev)
+        q = _to_torch(torch, inp.q, W.BF16, dev)
+        start = torch.zeros(wl.batch, dtype=torch.int32, device=dev)
+        us_a = _cold_launch_us(torch, flush, lambda: cache.append(K, V, start), max(3, args.steps // 4))
+        if int(cache.status.item()) != 0:
+            raise RuntimeError(f"device status {int(cache.status.item())}")
+        lens = torch.full((wl.batch,), T, dtype=torch.int32, device=dev)
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        us = _cold_launch_us(torch, flush, lambda: cache.decode(q, lens, T, out=out), args.steps)
+        pairs = wl.batch * wl.n_kv_heads
+        per = desc.k_code_bytes + desc.k_norm_slots * desc.norm_bytes + desc.v_code_bytes + desc.norm_bytes
+        nbytes = pairs * T * per + q.numel() * 2 + q.numel() * 4
+        gbs = nbytes / (us * 1e-6) / 1e9
+        sp, vm = tq.tq_decode_plan(desc, T)
+        print(f"| {wl.name} | {wl.batch} | {T} | {desc.k_code_bytes + 2 * desc.norm_bytes} | {sp}, {vm} | "
+              f"{us_a:.1f} | {us:.1f} | {gbs:.0f} | {100 * gbs / peak:.1f} % |", flush=True)
+        del cache, K, V
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -760,7 +805,12 @@ def main():
     ap.add_argument("--prefix", action="store_true",
                     help="decode over fp16 tokens plus the packed cache (a table)")
     ap.add_argument("--zip", action="store_true", help="ZipFusion store and attention (a table)")
+    ap.add_argument("--two-stage", action="store_true",
+                    help="keys at 1-2 bits with the QJL residual stage: append and decode (a table)")
     args = ap.parse_args()
+    if args.two_stage:
+        run_two_stage(args)
+        return
     if args.zip:
         run_zip(args)
         return

@@ -78,7 +78,12 @@ typedef int32_t tq_status;
  *                                                      [RotaryQuant, Key design 2]
  * Mixed-rate keys (k_mixed = 1) replace K's rotation by one random orthogonal
  * matrix per same-width group of RoPE blocks [Block-GTQ, physical encoding and
- * grouping]; V keeps `rot`. */
+ * grouping]; V keeps `rot`.
+ * Two-stage keys (k_bits 1 or 2) [TQ-MNN §2.4]: K keeps `rot` for a
+ * (k_bits - 1)-bit MSE code of y = R x / ||x|| and adds a 1-bit QJL code of its
+ * residual r = y - C[idx]: the signs of S r for a caller-drawn Gaussian
+ * projection S, from which <q~, r> is estimated without bias as
+ * ||r|| sqrt(pi/2) / 128 <S q~, sign(S r)>. */
 #define TQ_ROT_WHT128      0
 #define TQ_ROT_WHT32       1
 #define TQ_ROT_SO4_WHT128  2
@@ -120,15 +125,20 @@ typedef int32_t tq_status;
  * 32-dim block) or 4 (mixed-rate keys: slot b-1 holds the norm of the b-bit
  * group, 0 if empty).
  *
+ * Two-stage keys (k_bits 1 or 2): (k_bits - 1) * 16 bytes of 1-bit MSE codes
+ * (index i at bit i, LSB first; none for k_bits = 1), then 16 bytes of signs
+ * (bit j = 1 iff (S r)_j >= 0): 16 or 32 B.  Two norm slots: ||x|| and
+ * ||x|| * ||r||.
+ *
  * Positions per (batch, KV head): t_alloc = t_capacity rounded up to a multiple
  * of 16 (TQ_LAYOUT_TILE16) or t_capacity (TQ_LAYOUT_NATURAL).  Every array is
  * [batch][n_kv_heads][t_alloc positions] of per-position data:
  *   k_codes, v_codes  k_code_bytes / v_code_bytes per position, uint8
  *   k_norms, v_norms  k_norm_slots / v_norm_slots per position, norm_dtype
  *
- * TQ_LAYOUT_NATURAL (more than 8 query heads per KV head, or fp32 norms with
- * four slots: WHT32 or mixed-rate keys): position t holds the record and norms
- * of token t.
+ * TQ_LAYOUT_NATURAL (more than 8 query heads per KV head, fp32 norms with four
+ * slots: WHT32 or mixed-rate keys, or two-stage keys): position t holds the
+ * record and norms of token t.
  *
  * TQ_LAYOUT_TILE16 (every other cache): positions come in tiles of 16; tile j of
  * a (batch, KV head) holds tokens 16j .. 16j+15 in 16 * code_bytes bytes of codes
@@ -168,7 +178,7 @@ typedef struct tq_cache_desc {
     int32_t batch;
     int32_t t_capacity;
     int32_t rot;            /* TQ_ROT_* */
-    int32_t k_bits;         /* 3 or 4 (ignored when k_mixed) */
+    int32_t k_bits;         /* 3 or 4; 1 or 2: two-stage keys (ignored when k_mixed) */
     int32_t v_bits;         /* 3 or 4 */
     int32_t norm_dtype;     /* TQ_F16 or TQ_F32 */
     int32_t k_mixed;        /* 0 or 1 */
@@ -234,9 +244,13 @@ tq_status tq_block_bit_alloc(const double* s, int32_t L, int32_t b_min, int32_t 
                              int32_t B_total, int32_t* b_out);
 
 /* Fill a cache descriptor and validate the shape.
+ *   k_bits  3 or 4 (the same as v_bits), or 1 or 2 for two-stage keys
+ *           (WHT128 or SO4_WHT128, any v_bits); ignored when k_mixed
+ *   v_bits  3 or 4
  * Errors: TQ_ERR_INVALID_ARG (non-positive sizes, n_q_heads not a multiple of
  * n_kv_heads, bad enum), TQ_ERR_UNSUPPORTED (head_dim != 128, group >
- * TQ_MAX_GROUP, bits outside {3, 4}, WHT32 or SO4 combined with k_mixed). */
+ * TQ_MAX_GROUP, bits outside the sets above, k_bits 3/4 different from v_bits,
+ * WHT32 combined with k_mixed or with two-stage keys). */
 tq_status tq_cache_desc_init(tq_cache_desc* desc, int32_t head_dim, int32_t n_q_heads,
                              int32_t n_kv_heads, int32_t batch, int32_t t_capacity,
                              int32_t rot, int32_t k_bits, int32_t v_bits,
@@ -258,7 +272,9 @@ size_t tq_cache_bytes(const tq_cache_desc* desc, int32_t part);
  *   k_group_mats host fp32: for each KV head, for each width b = 1..4 whose
  *                group is non-empty (n_b = 2 * #blocks), the n_b x n_b
  *                row-major orthogonal matrix Pi_b, concatenated; required iff
- *                k_mixed
+ *                k_mixed.  For two-stage keys (k_bits 1 or 2): the QJL
+ *                projections S, [n_kv][128][128] row-major (row j gives sign
+ *                bit j), entries i.i.d. N(0, 1) drawn by the caller; required
  * Codebooks are solved here (tq_codebook) for every (width, bits) in use.
  * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_NO_CONVERGENCE. */
 tq_status tq_params_build(const tq_cache_desc* desc, const float* signs, const float* quats,
@@ -272,6 +288,9 @@ tq_status tq_params_build(const tq_cache_desc* desc, const float* signs, const f
  * call].  For every (b, t, h) and both K and V: n = ||x|| per norm segment,
  * y = R x / n, idx = #{k : y > boundary_k} (fp32 compares, ties to the lower
  * cell) [TQ-MNN §3.4], pack, store the norm rounded to norm_dtype.
+ * Two-stage keys [TQ-MNN §2.4]: the same on the (k_bits - 1)-bit codebook (no
+ * search for k_bits = 1), then r = y - C[idx], z = S r in fp32, sign bits
+ * z_j >= 0, norms ||x|| and ||x|| * ||r||.
  *   K, V         device [batch][n_new][n_kv_heads][128] of in_dtype
  *   in_dtype     TQ_F32, TQ_F16 or TQ_BF16
  *   d_start_pos  device int32 [batch]: token t goes to slot d_start_pos[b] + t;
@@ -298,6 +317,9 @@ size_t tq_decode_workspace_bytes(const tq_cache_desc* desc, int32_t max_splits);
  * merge].  For each batch b and q head g of KV head h:
  *   q~ = R_K q;  s_j = sum_seg n_{j,seg} <q~_seg, C_seg[idx_{j,seg}]> / sqrt(128)
  *   a = softmax(s) over j < seq_len_b;  o~ = sum_j a_j v~_j;  o = R_V^T o~.
+ * Two-stage keys [TQ-MNN §2.4]: s_j = (n_j <q~, C[idx_j]> + n_j rho_j
+ * sqrt(pi/2) / 128 <S q~, 2 sign_j - 1>) / sqrt(128), with S q~ formed once per
+ * query head.
  *   q            device [batch][n_q_heads][128] of q_dtype (TQ_F32/F16/BF16)
  *   d_seq_lens   device int32 [batch]; clamped to [0, min(t_capacity,
  *                max_seq_len)] with TQ_DEV_* flags; seq_len 0 gives o = 0

@@ -145,8 +145,38 @@ def tq_cache_bytes(desc: tq_cache_desc, part: int) -> int:
     return int(lib().tq_cache_bytes(ctypes.byref(desc), part))
 
 
+def _params_sizes(desc: tq_cache_desc, signs, quats, k_block_bits, k_group_mats):
+    """Check the host arrays against what tq_params_build reads (include/tq.h), so
+    that a short array is an error here rather than a read past its end."""
+    nkv = int(desc.n_kv_heads)
+
+    def size(x):
+        return None if x is None else int(np.asarray(x).size)
+
+    if signs is not None and size(signs) != nkv * 128:
+        raise ValueError(f"signs: {size(signs)} values, want n_kv * 128 = {nkv * 128}")
+    if quats is not None and size(quats) != nkv * 32 * 8:
+        raise ValueError(f"quats: {size(quats)} values, want n_kv * 256 = {nkv * 256}")
+    if int(desc.k_mixed):
+        if k_block_bits is None or k_group_mats is None:
+            raise ValueError("mixed-rate keys need k_block_bits and k_group_mats")
+        bb = np.asarray(k_block_bits)
+        if bb.size != nkv * 64:
+            raise ValueError(f"k_block_bits: {bb.size} values, want n_kv * 64 = {nkv * 64}")
+        bb = bb.reshape(nkv, 64)
+        need = int(sum((2 * int(np.sum(bb[h] == b))) ** 2 for h in range(nkv) for b in range(1, 5)))
+        if size(k_group_mats) != need:
+            raise ValueError(f"k_group_mats: {size(k_group_mats)} values, the allocation needs {need}")
+    elif int(desc.k_bits) in (1, 2):
+        if size(k_group_mats) != nkv * 128 * 128:
+            raise ValueError(f"two-stage keys need k_group_mats = the projections, n_kv * 128 * 128 values")
+
+
 def tq_params_build(desc: tq_cache_desc, signs=None, quats=None, k_block_bits=None, k_group_mats=None) -> np.ndarray:
-    """Host parameter blob (uint8); copy it to a 16-byte aligned device buffer."""
+    """Host parameter blob (uint8); copy it to a 16-byte aligned device buffer.
+    k_group_mats: the group matrices of mixed-rate keys, or the projections S
+    [n_kv][128][128] of two-stage keys (k_bits 1 or 2)."""
+    _params_sizes(desc, signs, quats, k_block_bits, k_group_mats)
     blob = np.zeros(int(desc.params_bytes), dtype=np.uint8)
     keep = []
 

@@ -35,14 +35,18 @@ constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kInvSqrtD = 0.08838834764831845f;   // 1/sqrt(128)
 constexpr int kPartStride = 132;                      // 128 (o~) + m + l, 16-byte rows
+constexpr float kQjlScale = 0.009791516697777346f;    // sqrt(pi/2) / 128 (two-stage keys)
 
 using DecodeArgs = tq::DecodeArgs;
 
 template <int F> struct Fmt {
     static constexpr bool three = (F == TQ_FMT_ONE3 || F == TQ_FMT_BLK3);
-    static constexpr int bytes = three ? 48 : 64;
+    // two-stage keys: `mse_words` words of 1-bit codes, then 4 words of signs
+    static constexpr bool qjl = (F == TQ_FMT_QJ1 || F == TQ_FMT_QJ2);
+    static constexpr int mse_words = F == TQ_FMT_QJ2 ? 4 : 0;
+    static constexpr int bytes = qjl ? 4 * (mse_words + 4) : three ? 48 : 64;
     static constexpr int words = bytes / 4;
-    static constexpr int nslots = (F == TQ_FMT_ONE3 || F == TQ_FMT_ONE4) ? 1 : 4;
+    static constexpr int nslots = qjl ? 2 : (F == TQ_FMT_ONE3 || F == TQ_FMT_ONE4) ? 1 : 4;
     static constexpr bool blk = (F == TQ_FMT_BLK3 || F == TQ_FMT_BLK4);
     static constexpr bool mix = (F == TQ_FMT_MIX4);
 };
@@ -72,6 +76,15 @@ template <int F>
 __device__ __forceinline__ void load_norms(const void* base, size_t tok, int norm_f16, float* n) {
     if (Fmt<F>::nslots == 1) {
         n[0] = tq::load_norm(base, tok, norm_f16);
+    } else if (Fmt<F>::nslots == 2) {
+        if (norm_f16) {
+            const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const __half*>(base) + tok * 2));
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
+            n[0] = a.x; n[1] = a.y;
+        } else {
+            const float2 f = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(base) + tok * 2));
+            n[0] = f.x; n[1] = f.y;
+        }
     } else if (norm_f16) {
         uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __half*>(base) + tok * 4));
         float2 a = __half22float2(*reinterpret_cast<__half2*>(&u.x));
@@ -98,14 +111,42 @@ __device__ __forceinline__ void load_row(const float* row, float* q) {
 }
 
 // s_g = sum over segments of n_seg * sum_c q~_g[c] C_seg[idx_c]   (log2 units:
-// q~ already carries log2(e) / sqrt(d))
+// q~ already carries log2(e) / sqrt(d)).  Two-stage keys [TQ-MNN §2.4]:
+// s_g = n <q~_g, C[idx]> + n rho <u_g, 2 sign - 1> with u_g = S q~_g sqrt(pi/2) / d
+// (in ut, same units); nrm = (n, n rho).
 template <int GP, int KF>
 __device__ __forceinline__ void qk_token(const uint32_t* rec, const float* nrm, const float (*qt)[GP],
-                                         const float (*kcb)[16], const uint8_t* kseg_of, float* sc) {
+                                         const float (*ut)[GP], const float (*kcb)[16], const uint8_t* kseg_of,
+                                         float* sc) {
     using K = Fmt<KF>;
 #pragma unroll
     for (int g = 0; g < GP; ++g) sc[g] = 0.f;
-    if (K::mix) {
+    if constexpr (K::qjl) {
+        float ms[GP], sg[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) { ms[g] = 0.f; sg[g] = 0.f; }
+        if constexpr (K::mse_words > 0) {
+            const float c0 = kcb[0][0], c1 = kcb[0][1];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float v = ((rec[c >> 5] >> (c & 31)) & 1u) ? c1 : c0;
+                float q[GP];
+                load_row<GP>(qt[c], q);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) ms[g] = fmaf(v, q[g], ms[g]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+            const float sgn = ((rec[K::mse_words + (j >> 5)] >> (j & 31)) & 1u) ? 1.f : -1.f;
+            float u[GP];
+            load_row<GP>(ut[j], u);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) sg[g] = fmaf(sgn, u[g], sg[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < GP; ++g) sc[g] = fmaf(nrm[0], ms[g], nrm[1] * sg[g]);
+    } else if (K::mix) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
             const int s = kseg_of[c];
@@ -151,6 +192,7 @@ struct Smem {
     alignas(16) float red[4][GP];
     alignas(16) float red2[4][GP];
     alignas(16) uint8_t kseg_of[128];
+    alignas(16) float ut[Fmt<KF>::qjl ? 128 : 1][GP];   // two-stage keys: S q~ sqrt(pi/2) / d
     int is_last;
 };
 
@@ -186,6 +228,19 @@ __device__ __forceinline__ void prologue(const DecodeArgs& a, const tq_head_para
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) S.qt[4 * lane + i][g] = v[i] * (kLog2e * kInvSqrtD);
+        if constexpr (Fmt<KF>::qjl) {
+            // u = S q~, once per query head [TQ-MNN §2.4]; the projection sits
+            // where mixed-rate keys keep their matrices
+            float* xs = S.xs[warp];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xs[4 * lane + i] = v[i];
+            __syncwarp();
+            float u[4];
+            tq::dense_rows_t(a.kmat + (size_t)h * 128 * 128, xs, u);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) S.ut[4 * lane + i][g] = u[i] * (kLog2e * kInvSqrtD * kQjlScale);
+        }
     }
 }
 

@@ -138,6 +138,26 @@ __device__ __forceinline__ void rotate_forward_dense(const tq_head_params& P, co
     }
 }
 
+// v = rows 4l .. 4l+3 of M xs for a 128 x 128 matrix stored transposed (MT,
+// row-major: MT[c][j] = M[j][c], 16-byte aligned) and the warp's staged vector
+// xs (128 floats, shared memory): per column one coalesced 16-byte load per lane
+// and a broadcast of x_c.
+__device__ __forceinline__ void dense_rows_t(const float* MT, const float* xs, float v[4]) {
+    const int lane = threadIdx.x & 31;
+    const float4* col = reinterpret_cast<const float4*>(MT) + lane;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < 128; ++c) {
+        const float4 m = __ldg(col + 32 * c);
+        const float x = xs[c];
+        a0 = fmaf(m.x, x, a0);
+        a1 = fmaf(m.y, x, a1);
+        a2 = fmaf(m.z, x, a2);
+        a3 = fmaf(m.w, x, a3);
+    }
+    v[0] = a0; v[1] = a1; v[2] = a2; v[3] = a3;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int m = 16; m; m >>= 1) x += __shfl_xor_sync(TQ_FULL_MASK, x, m);

@@ -278,9 +278,11 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     if (head_dim != TQ_HEAD_DIM) return TQ_ERR_UNSUPPORTED;
     if (n_q_heads / n_kv_heads > TQ_MAX_GROUP) return TQ_ERR_UNSUPPORTED;
     if (v_bits != 3 && v_bits != 4) return TQ_ERR_UNSUPPORTED;
-    if (!k_mixed && k_bits != 3 && k_bits != 4) return TQ_ERR_UNSUPPORTED;
-    if (!k_mixed && k_bits != v_bits) return TQ_ERR_UNSUPPORTED;   // one kernel per shared width
-    if (k_mixed && rot == TQ_ROT_WHT32) return TQ_ERR_UNSUPPORTED;
+    // two-stage keys [TQ-MNN §2.4]: (k_bits - 1)-bit MSE code + 1-bit QJL code
+    const bool two = !k_mixed && (k_bits == 1 || k_bits == 2);
+    if (!k_mixed && !two && k_bits != 3 && k_bits != 4) return TQ_ERR_UNSUPPORTED;
+    if (!k_mixed && !two && k_bits != v_bits) return TQ_ERR_UNSUPPORTED;   // one kernel per shared width
+    if ((k_mixed || two) && rot == TQ_ROT_WHT32) return TQ_ERR_UNSUPPORTED;
     if ((int64_t)batch * n_kv_heads * t_capacity > (int64_t)1 << 40) return TQ_ERR_INVALID_ARG;
     d->head_dim = head_dim;
     d->n_q_heads = n_q_heads;
@@ -293,20 +295,20 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     d->norm_dtype = norm_dtype;
     d->k_mixed = k_mixed;
     d->group = n_q_heads / n_kv_heads;
-    d->k_code_bytes = k_mixed ? 64 : (k_bits == 3 ? 48 : 64);
+    d->k_code_bytes = k_mixed ? 64 : two ? 16 * k_bits : (k_bits == 3 ? 48 : 64);
     d->v_code_bytes = v_bits == 3 ? 48 : 64;
-    d->k_norm_slots = (k_mixed || rot == TQ_ROT_WHT32) ? 4 : 1;
+    d->k_norm_slots = (k_mixed || rot == TQ_ROT_WHT32) ? 4 : two ? 2 : 1;
     d->v_norm_slots = rot == TQ_ROT_WHT32 ? 4 : 1;
     d->norm_bytes = norm_dtype == TQ_F16 ? 2 : 4;
     // the tile layout (read by the tensor-core decode kernel) for every format it
     // covers: at most 8 query heads per KV head, fp16 norms where a vector has
-    // four (the 32-wide blocks, mixed-rate keys)
-    const bool tile = d->group <= 8 && !((rot == TQ_ROT_WHT32 || k_mixed) && norm_dtype != TQ_F16);
+    // four (the 32-wide blocks, mixed-rate keys), not two-stage keys
+    const bool tile = d->group <= 8 && !two && !((rot == TQ_ROT_WHT32 || k_mixed) && norm_dtype != TQ_F16);
     d->layout = tile ? TQ_LAYOUT_TILE16 : TQ_LAYOUT_NATURAL;
     const int64_t alloc = tile ? ((int64_t)t_capacity + 15) / 16 * 16 : t_capacity;
     if (alloc > 0x7fffffff) return TQ_ERR_INVALID_ARG;
     d->t_alloc = (int32_t)alloc;
-    d->params_bytes = tq_params_blob_bytes(n_kv_heads, k_mixed);
+    d->params_bytes = tq_params_blob_bytes(n_kv_heads, k_mixed || two);
     return TQ_OK;
 }
 
@@ -330,6 +332,8 @@ tq_status tq_params_build(const tq_cache_desc* d, const float* signs, const floa
     if (need_signs && !signs) return TQ_ERR_INVALID_ARG;
     if (d->rot == TQ_ROT_SO4_WHT128 && !quats) return TQ_ERR_INVALID_ARG;
     if (d->k_mixed && (!k_block_bits || !k_group_mats)) return TQ_ERR_INVALID_ARG;
+    const bool two = tq_two_stage(d);
+    if (two && !k_group_mats) return TQ_ERR_INVALID_ARG;
     memset(host_blob, 0, (size_t)d->params_bytes);
     tq_head_params* hp = (tq_head_params*)host_blob;
     float* kmat_all = (float*)((char*)host_blob + (size_t)d->n_kv_heads * sizeof(tq_head_params));
@@ -354,7 +358,26 @@ tq_status tq_params_build(const tq_cache_desc* d, const float* signs, const floa
             memcpy(p.v_cent[s], c, sizeof(float) * 16);
             memcpy(p.v_bound[s], bd, sizeof(float) * 16);
         }
-        if (!d->k_mixed) {
+        if (two) {
+            // one 128-wide segment with the (k_bits - 1)-bit codebook (none for
+            // k_bits = 1); the projection S goes where mixed-rate keys keep k_mat
+            p.k_nseg = 1;
+            for (int s = 0; s <= 4; ++s) p.k_seg_start[s] = s < 1 ? 0 : 128;
+            p.k_seg_bits[0] = d->k_bits - 1;
+            if (d->k_bits == 2) {
+                const float *c, *bd;
+                tq_status st = memo.get(128, 1, &c, &bd, &p.k_h_scale[0]);
+                if (st != TQ_OK) return st;
+                memcpy(p.k_cent[0], c, sizeof(float) * 16);
+                memcpy(p.k_bound[0], bd, sizeof(float) * 16);
+            }
+            for (int i = 0; i < 128; ++i) p.k_gcoord[i] = i;
+            // stored transposed (column c of S contiguous) for coalesced reads
+            float* st = kmat_all + (size_t)h * 128 * 128;
+            const float* sm = k_group_mats + (size_t)h * 128 * 128;
+            for (int j = 0; j < 128; ++j)
+                for (int c = 0; c < 128; ++c) st[(size_t)c * 128 + j] = sm[(size_t)j * 128 + c];
+        } else if (!d->k_mixed) {
             const int kseg = d->rot == TQ_ROT_WHT32 ? 4 : 1;
             const int klen = 128 / kseg;
             p.k_nseg = kseg;

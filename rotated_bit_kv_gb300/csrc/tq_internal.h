@@ -11,6 +11,7 @@
 //   WHT32               : 4 segments of 32 (codebook for d = 32)
 //   mixed-rate keys     : segment s = bit width s + 1, length n_b (possibly 0),
 //                         codebook for d = n_b
+//   two-stage keys      : 1 segment of 128 with k_bits - 1 bits (0: no MSE code)
 struct alignas(16) tq_head_params {
     float signs[128];         // +-1 of the sign-flipped WHT
     float quat[32][8];        // per 4-dim block: q_L (w,x,y,z), q_R (w,x,y,z)
@@ -34,10 +35,17 @@ static_assert(sizeof(tq_head_params) % 16 == 0, "params record must stay 16-byte
 
 // For mixed-rate keys the blob continues with float k_mat[n_kv][128][128]:
 // rotated[r] = sum_c k_mat[r][c] * x[k_gcoord[c]], block diagonal (segment s
-// occupies rows and columns [k_seg_start[s], k_seg_start[s+1])).
-static inline int64_t tq_params_blob_bytes(int n_kv, int k_mixed) {
+// occupies rows and columns [k_seg_start[s], k_seg_start[s+1])).  For two-stage
+// keys the same place holds the QJL projections transposed: ST[n_kv][128][128]
+// with ST[c][j] = S[j][c] (S's row j gives sign bit j).
+static inline int64_t tq_params_blob_bytes(int n_kv, int has_kmat) {
     return (int64_t)n_kv * (int64_t)sizeof(tq_head_params) +
-           (k_mixed ? (int64_t)n_kv * 128 * 128 * 4 : 0);
+           (has_kmat ? (int64_t)n_kv * 128 * 128 * 4 : 0);
+}
+
+// Two-stage keys: a (k_bits - 1)-bit MSE code plus a 1-bit QJL code.
+static inline bool tq_two_stage(const tq_cache_desc* d) {
+    return !d->k_mixed && (d->k_bits == 1 || d->k_bits == 2);
 }
 
 // Key/value code formats used to select kernels.
@@ -47,10 +55,13 @@ enum tq_fmt : int {
     TQ_FMT_BLK3 = 2,   // four 32-wide segments, 3-bit codes (48 B)
     TQ_FMT_BLK4 = 3,   // four 32-wide segments, 4-bit codes (64 B)
     TQ_FMT_MIX4 = 4,   // runtime segments, one code per nibble (64 B)
+    TQ_FMT_QJ1 = 5,    // two-stage keys, k_bits 1: 128 sign bits (16 B)
+    TQ_FMT_QJ2 = 6,    // two-stage keys, k_bits 2: 128 one-bit codes + 128 sign bits (32 B)
 };
 
 static inline int tq_k_fmt(const tq_cache_desc* d) {
     if (d->k_mixed) return TQ_FMT_MIX4;
+    if (tq_two_stage(d)) return d->k_bits == 1 ? TQ_FMT_QJ1 : TQ_FMT_QJ2;
     if (d->rot == TQ_ROT_WHT32) return d->k_bits == 3 ? TQ_FMT_BLK3 : TQ_FMT_BLK4;
     return d->k_bits == 3 ? TQ_FMT_ONE3 : TQ_FMT_ONE4;
 }

@@ -29,6 +29,7 @@ struct QuantArgs {
     // head) in the arrays; tiled: TQ_LAYOUT_TILE16 (tq_tile.cuh) else one record
     // per position
     int B, n_new, Hkv, Tcap, t_alloc, tiled, in_dtype, norm_f16, rot, k_mixed;
+    int k_two;                   // two-stage keys: k_bits (1 or 2), else 0
     int code_bytes[2], norm_slots[2];
 };
 
@@ -236,6 +237,73 @@ __device__ __forceinline__ void encode_vector(const QuantArgs& a, const VecId& i
     }
 }
 
+// Two-stage key code [TQ-MNN §2.4]: y = R x / n on the (k_bits - 1)-bit codebook
+// (one boundary; no code for k_bits = 1), residual r = y - C[idx], z = S r (fp32,
+// the transposed projection in the blob's matrix slot), sign bits z_j >= 0;
+// norms n and n ||r||.  Natural layout: the record is (k_bits - 1) * 4 words of
+// codes then 4 words of signs, bit j of the stream for coordinate j.
+__device__ __forceinline__ void encode_two_stage(const QuantArgs& a, const VecId& id, const float* xin, float* xs) {
+    const int lane = threadIdx.x & 31;
+    const int h = id.h, t = id.t, b = id.b;
+    const int slot = a.start_pos[b] + t;
+    if (slot < 0 || slot >= a.Tcap) {
+        if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BAD_POSITION);
+        return;
+    }
+    const tq_head_params& P = a.params[h];
+    float y[4] = {xin[0], xin[1], xin[2], xin[3]};
+    const float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+    tq::rotate_forward(a.rot, P, y);
+    const float n = sqrtf(tq::warp_sum(ss));
+    const float inv = n > 0.f ? 1.f / n : 0.f;
+    uint32_t code4 = 0;
+    float r[4];
+    if (a.k_two == 2) {
+        const float bd = P.k_bound[0][0], c0 = P.k_cent[0][0], c1 = P.k_cent[0][1];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float yi = y[i] * inv;
+            const bool up = yi > bd;
+            code4 |= (up ? 1u : 0u) << i;
+            r[i] = yi - (up ? c1 : c0);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r[i] = y[i] * inv;
+    }
+    const float rho = sqrtf(tq::warp_sum(r[0] * r[0] + r[1] * r[1] + r[2] * r[2] + r[3] * r[3]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xs[4 * lane + i] = r[i];
+    __syncwarp();
+    float z[4];
+    tq::dense_rows_t(a.kmat + (size_t)h * 128 * 128, xs, z);
+    __syncwarp();   // xs is the next vector's staging buffer
+    uint32_t sgn4 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sgn4 |= (z[i] >= 0.f ? 1u : 0u) << i;
+    // word w of a 1-bit stream = the 4-bit groups of lanes 8w .. 8w+7
+    const int src = 8 * (lane & 3);
+    uint32_t wc = 0, wsg = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        wc |= __shfl_sync(TQ_FULL_MASK, code4, src + k) << (4 * k);
+        wsg |= __shfl_sync(TQ_FULL_MASK, sgn4, src + k) << (4 * k);
+    }
+    const size_t pos = (((size_t)b * a.Hkv + h) * a.t_alloc) + slot;
+    uint32_t* rec = reinterpret_cast<uint32_t*>(a.codes[0] + pos * a.code_bytes[0]);
+    const int mw = 4 * (a.k_two - 1);
+    if (lane < 4) {
+        if (mw) rec[lane] = wc;
+        rec[mw + lane] = wsg;
+    }
+    if (lane < 2) {
+        const float nv = lane == 0 ? n : n * rho;
+        const size_t ni = pos * 2 + lane;
+        if (a.norm_f16) static_cast<__half*>(a.norms[0])[ni] = __float2half_rn(nv);
+        else static_cast<float*>(a.norms[0])[ni] = nv;
+    }
+}
+
 // Encode one vector of a cache without mixed-rate keys: the rotation kind is a
 // template parameter, the boundaries of the lane's segment come in as float4s and
 // the count is unrolled.  Same steps and results as encode_vector.
@@ -350,8 +418,12 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
             idn = vec_id(a, vn);
             tq::load4((idn.which ? a.src[1] : a.src[0]), input_elem(vn), a.in_dtype, xn);
         }
-        if constexpr (ROT < 0) encode_vector(a, id, x, xs_all[wib]);
-        else encode_fast<ROT>(a, id, x, xs_all[wib]);
+        if constexpr (ROT < 0) {
+            if (id.which == 0 && a.k_two) encode_two_stage(a, id, x, xs_all[wib]);
+            else encode_vector(a, id, x, xs_all[wib]);
+        } else {
+            encode_fast<ROT>(a, id, x, xs_all[wib]);
+        }
         if (!more) break;
         __syncwarp();
         v = vn;
@@ -1032,6 +1104,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     a.norm_f16 = d->norm_dtype == TQ_F16;
     a.rot = d->rot;
     a.k_mixed = d->k_mixed;
+    a.k_two = tq_two_stage(d) ? d->k_bits : 0;
     a.code_bytes[0] = d->k_code_bytes;
     a.code_bytes[1] = d->v_code_bytes;
     a.norm_slots[0] = d->k_norm_slots;
@@ -1079,7 +1152,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
         }
         return cudaPeekAtLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
     }
-    if (d->k_mixed) tq_quantize_kernel<-1><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
+    if (d->k_mixed || a.k_two) tq_quantize_kernel<-1><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
     else if (d->rot == TQ_ROT_WHT128) tq_quantize_kernel<TQ_ROT_WHT128><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
     else if (d->rot == TQ_ROT_WHT32) tq_quantize_kernel<TQ_ROT_WHT32><<<(unsigned)blocks, kWarps * 32, 0, st>>>(a);
     else if (d->rot == TQ_ROT_SO4_WHT128)

@@ -102,7 +102,9 @@ def test_desc_sizes(tqlib):
     ((128, 30, 8, 1, 16, 0, 3, 3, 1), 1),     # n_q not a multiple of n_kv
     ((128, 32, 8, 0, 16, 0, 3, 3, 1), 1),     # batch 0
     ((128, 32, 8, 1, 16, 7, 3, 3, 1), 1),     # bad rotation
-    ((128, 32, 8, 1, 16, 0, 2, 2, 1), 2),     # 2-bit uniform codes not built
+    ((128, 32, 8, 1, 16, 0, 2, 2, 1), 2),     # 2-bit V codes not built
+    ((128, 32, 8, 1, 16, 1, 2, 3, 1), 2),     # two-stage keys with 32-wide blocks
+    ((128, 32, 8, 1, 16, 0, 5, 3, 1), 2),     # 5-bit keys
     ((128, 32, 8, 1, 16, 0, 3, 4, 1), 2),     # K and V widths differ
     ((128, 64, 2, 1, 16, 0, 3, 3, 1), 2),     # group 32 > 16
     ((128, 32, 8, 1, 16, 0, 3, 3, 2), 1),     # bf16 norms
@@ -135,9 +137,12 @@ def test_params_blob_contents(tqlib):
     for b in range(1, 5):
         want.append(want[-1] + sum(cs.size for bb_, cs in lay if bb_ == b))
     np.testing.assert_array_equal(starts, want)
-    # missing inputs are argument errors
-    with pytest.raises(tq.TQError):
+    # missing inputs are argument errors: in the binding, and in the library
+    with pytest.raises(ValueError):
         tq.tq_params_build(d, signs=signs)
+    out = np.zeros(int(d.params_bytes), np.uint8)
+    assert tq.lib().tq_params_build(ctypes.byref(d), signs.ctypes.data, None, None, None,
+                                    out.ctypes.data) == tq.TQ_ERR_INVALID_ARG
 
 
 def test_decode_plan_host_only(tqlib):

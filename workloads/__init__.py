@@ -10,7 +10,9 @@ here and handed to both the oracle and the CUDA library as inputs.
 
 Every array is produced from ``np.random.default_rng(seed)`` in a fixed draw
 order (outlier/scale channels -> K -> V -> calibration q -> decode q ->
-rotation parameters), so the oracle and the GPU see the same bytes.
+rotation parameters), so the oracle and the GPU see the same bytes.  The
+matrices drawn per head (mixed-rate key groups, two-stage key projections)
+come from streams of their own.
 
 bf16 tensors are represented as ``uint16`` bit patterns, obtained by
 round-to-nearest-even from the fp32 samples.
@@ -126,6 +128,23 @@ def mixed_rate_long(seq_len: int = 131072, seed: int = 0) -> Workload:
     the first 512 tokens; uniform 3-bit V with a sign-flipped 128-point WHT."""
     return Workload("mixed_rate_long", 16, 2, 1, seq_len, ROT_WHT128, 3, 3, BF16, F16,
                     "rope_decay", "normal", "rope_decay", mixed_k=True, seed=seed)
+
+
+def two_stage_keys(k_bits: int = 2, seq_len: int = 8192, batch: int = 8, seed: int = 0) -> Workload:
+    """Keys at 1 or 2 bits with the two-stage code ((k_bits - 1)-bit MSE code plus
+    a 1-bit QJL code of the residual, its projection drawn by two_stage_projection);
+    Llama-3.1-8B-shaped heads (32 query / 8 KV, d = 128), bf16 q/K/V, 3-bit V, one
+    128-wide sign-flipped WHT, fp16 norms; K channel scales lognormal(0, 0.5) with
+    2% of channels x15; V ~ N(0,1)."""
+    return Workload(f"two_stage_k{k_bits}", 32, 8, batch, seq_len, ROT_WHT128, k_bits, 3, BF16, F16,
+                    "lognormal_outlier", "normal", "normal", seed=seed)
+
+
+def two_stage_projection(d: int, seed: int, head: int) -> np.ndarray:
+    """The QJL projection S of one KV head: d x d, i.i.d. N(0, 1) entries, from
+    its own seeded stream (depends only on (seed, head))."""
+    rng = np.random.default_rng([seed, 0x514A, head])
+    return rng.standard_normal((d, d)).astype(np.float32)
 
 
 # T sweeps named by the workload descriptions.
