@@ -49,7 +49,9 @@ Readings where the pages are silent or ambiguous:
 * mixed-rate keys: RoPE block i is coordinates (2i, 2i+1); each same-width group
   is encoded by one TQ-MSE encoder with its own random orthogonal matrix, its
   own norm and the codebook for its own width; groups are laid out in ascending
-  bit width, one index per nibble;
+  bit width, one index per nibble, or (tight packing) each index at its
+  group's width, concatenated LSB first, the record rounded up to whole
+  16-byte units;
 * attention scale 1/sqrt(head_dim); greedy ties go to the lowest block index;
 * two-stage keys: the residual is taken in the rotated, normalised domain of the
   MSE stage (r = y - C[idx]); the projection S (d x d, i.i.d. N(0, 1)) is an
@@ -266,6 +268,7 @@ class HeadSpec:
     seg_coords: List[np.ndarray]
     n_norm_slots: int
     nibble_codes: bool        # codes stored one per nibble (4-bit or mixed)
+    tight: bool = False       # mixed-rate keys packed at their own widths (pack_tight)
 
 
 def spec_wht128(signs: np.ndarray, bits: int) -> HeadSpec:
@@ -308,10 +311,12 @@ def group_layout(block_bits: Sequence[int], b_min: int = 1, b_max: int = 4):
     return out
 
 
-def spec_group_dense(block_bits: Sequence[int], mats: dict) -> HeadSpec:
+def spec_group_dense(block_bits: Sequence[int], mats: dict, tight: bool = False) -> HeadSpec:
     """Mixed-rate keys: each same-width group is one TQ-MSE encoder with a
     random orthogonal matrix Pi_b of its own width, its own norm and the
-    codebook for (n_b, b)  [Block-GTQ; TQ-MNN §2.1].  `mats[b]` is Pi_b."""
+    codebook for (n_b, b)  [Block-GTQ; TQ-MNN §2.1].  `mats[b]` is Pi_b.
+    tight: the record packs each code at its group's width (pack_tight) instead
+    of one per nibble."""
     layout = group_layout(block_bits)
     d = 2 * len(block_bits)
     R = np.zeros((d, d))
@@ -325,7 +330,7 @@ def spec_group_dense(block_bits: Sequence[int], mats: dict) -> HeadSpec:
         segs.append(Segment(o, n, n, b, b - 1))
         coords.append(cs)
         o += n
-    return HeadSpec(R, segs, coords, 4, True)
+    return HeadSpec(R, segs, coords, 4, not tight, tight)
 
 
 # ============================================================================
@@ -406,11 +411,56 @@ def unpack_4bit(b: np.ndarray, d: int) -> np.ndarray:
     return out
 
 
+def code_widths(spec: HeadSpec) -> np.ndarray:
+    """[d] bits of the code at each record position (its segment's width)."""
+    w = np.zeros(sum(sg.length for sg in spec.segments), dtype=np.int64)
+    for sg in spec.segments:
+        w[sg.start:sg.start + sg.length] = sg.bits
+    return w
+
+
+def pack_tight(idx: np.ndarray, spec: HeadSpec) -> np.ndarray:
+    """Mixed-rate keys at their own widths  [Block-GTQ, packed cache: the groups'
+    codes concatenated]: the code at record position p takes w_p bits at bit
+    offset sum_{p' < p} w_p' of the little-endian byte stream, LSB first (the
+    positions are the groups in ascending width, as for the nibble record).
+    The record is the total width rounded up to whole 16-byte units."""
+    idx = np.asarray(idx, dtype=np.int64)
+    N, d = idx.shape
+    w = code_widths(spec)
+    assert w.size == d and np.all(idx < (1 << w)[None, :]) and idx.min() >= 0
+    total = int(w.sum())
+    nbits = -(-total // 128) * 128
+    bits = np.zeros((N, nbits), dtype=np.uint8)
+    off = 0
+    for p in range(d):
+        for k in range(int(w[p])):
+            bits[:, off + k] = (idx[:, p] >> k) & 1
+        off += int(w[p])
+    return np.packbits(bits, axis=1, bitorder="little")
+
+
+def unpack_tight(codes: np.ndarray, spec: HeadSpec, d: int) -> np.ndarray:
+    bits = np.unpackbits(np.asarray(codes, dtype=np.uint8), axis=1, bitorder="little").astype(np.int64)
+    w = code_widths(spec)
+    out = np.zeros((bits.shape[0], d), dtype=np.int64)
+    off = 0
+    for p in range(d):
+        for k in range(int(w[p])):
+            out[:, p] |= bits[:, off + k] << k
+        off += int(w[p])
+    return out
+
+
 def pack(idx: np.ndarray, spec: HeadSpec) -> np.ndarray:
+    if spec.tight:
+        return pack_tight(idx, spec)
     return pack_4bit(idx) if spec.nibble_codes else pack_3bit(idx)
 
 
 def unpack(codes: np.ndarray, spec: HeadSpec, d: int) -> np.ndarray:
+    if spec.tight:
+        return unpack_tight(codes, spec, d)
     return unpack_4bit(codes, d) if spec.nibble_codes else unpack_3bit(codes, d)
 
 
@@ -629,7 +679,7 @@ def head_specs(wl, inputs, block_bits=None, mats=None):
         else:
             raise ValueError(wl.rot)
         if wl.mixed_k:
-            k = spec_group_dense(block_bits[h], mats[h])
+            k = spec_group_dense(block_bits[h], mats[h], tight=getattr(wl, "tight_k", False))
         specs.append((k, v))
     return specs
 

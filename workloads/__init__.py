@@ -76,6 +76,7 @@ class Workload:
     v_recipe: str          # "outlier4x20", "normal"
     q_recipe: str          # "normal", "rope_decay"
     mixed_k: bool = False  # mixed-rate keys (greedy RoPE-block bit allocation)
+    tight_k: bool = False  # mixed-rate keys packed at their own widths (avg_bits * 16 B records)
     b_min: int = 1
     b_max: int = 4
     avg_bits: int = 3
