@@ -524,8 +524,10 @@ def library_setup(tq, wl, inp, t_capacity):
                     flat.append(W.haar_orthogonal(n, wl.seed, h, b).ravel())
         block_bits = np.stack(bbs).astype(np.int32)
         mats = np.concatenate(flat)
+    k_mixed = (2 if wl.tight_k else 1) if wl.mixed_k else 0
+    k_bits = (wl.avg_bits if wl.tight_k else 0) if wl.mixed_k else wl.k_bits
     desc = tq.tq_cache_desc_init(wl.head_dim, wl.n_q_heads, wl.n_kv_heads, wl.batch, t_capacity, wl.rot,
-                                 0 if wl.mixed_k else wl.k_bits, wl.v_bits, wl.norm_dtype, int(wl.mixed_k))
+                                 k_bits, wl.v_bits, wl.norm_dtype, k_mixed)
     blob = tq.tq_params_build(desc, signs=inp.signs, quats=inp.quats, k_block_bits=block_bits, k_group_mats=mats)
     return desc, blob
 
@@ -567,6 +569,8 @@ def run_sweep(args):
     cases += [(W.block32(3), 8192), (W.block32(4), 8192)]
     cases += [(W.so4_wht(seq_len=t), t) for t in (128, 256, 512, 2048, 8192, 32768)]
     cases += [(W.mixed_rate_long(seq_len=t), t) for t in (131072, 524288)]
+    # mixed-rate keys in tight records (natural layout, CUDA-core kernels)
+    cases += [(W.mixed_rate_long(seq_len=131072).with_(tight_k=True, name="mixed_rate_long_tight"), 131072)]
     print("| workload | B | T | plan (splits, V mode) | decode us | GB/s | of measured peak |")
     print("|---|---|---|---|---|---|---|")
     for wl, T in cases:

@@ -125,6 +125,11 @@ typedef int32_t tq_status;
  * 32-dim block) or 4 (mixed-rate keys: slot b-1 holds the norm of the b-bit
  * group, 0 if empty).
  *
+ * Tight mixed-rate keys (k_mixed = 2): each code at its group's width b, the
+ * groups in ascending width as above, concatenated LSB first (position p at bit
+ * offset sum_{p' < p} b_p'), k_bits * 16 bytes for an average of k_bits (2 or 3)
+ * bits per coordinate [Block-GTQ, packed cache]; four norm slots as above.
+ *
  * Two-stage keys (k_bits 1 or 2): (k_bits - 1) * 16 bytes of 1-bit MSE codes
  * (index i at bit i, LSB first; none for k_bits = 1), then 16 bytes of signs
  * (bit j = 1 iff (S r)_j >= 0): 16 or 32 B.  Two norm slots: ||x|| and
@@ -137,8 +142,8 @@ typedef int32_t tq_status;
  *   k_norms, v_norms  k_norm_slots / v_norm_slots per position, norm_dtype
  *
  * TQ_LAYOUT_NATURAL (more than 8 query heads per KV head, fp32 norms with four
- * slots: WHT32 or mixed-rate keys, or two-stage keys): position t holds the
- * record and norms of token t.
+ * slots: WHT32 or mixed-rate keys, tight mixed-rate keys, or two-stage keys):
+ * position t holds the record and norms of token t.
  *
  * TQ_LAYOUT_TILE16 (every other cache): positions come in tiles of 16; tile j of
  * a (batch, KV head) holds tokens 16j .. 16j+15 in 16 * code_bytes bytes of codes
@@ -181,7 +186,7 @@ typedef struct tq_cache_desc {
     int32_t k_bits;         /* 3 or 4; 1 or 2: two-stage keys (ignored when k_mixed) */
     int32_t v_bits;         /* 3 or 4 */
     int32_t norm_dtype;     /* TQ_F16 or TQ_F32 */
-    int32_t k_mixed;        /* 0 or 1 */
+    int32_t k_mixed;        /* 0; 1: nibble records; 2: tight records (k_bits = average bits) */
     /* derived */
     int32_t group;          /* n_q_heads / n_kv_heads */
     int32_t k_code_bytes;
@@ -245,8 +250,12 @@ tq_status tq_block_bit_alloc(const double* s, int32_t L, int32_t b_min, int32_t 
 
 /* Fill a cache descriptor and validate the shape.
  *   k_bits  3 or 4 (the same as v_bits), or 1 or 2 for two-stage keys
- *           (WHT128 or SO4_WHT128, any v_bits); ignored when k_mixed
+ *           (WHT128 or SO4_WHT128, any v_bits); ignored when k_mixed = 1; the
+ *           average bits per coordinate (2 or 3) when k_mixed = 2
  *   v_bits  3 or 4
+ *   k_mixed 0: uniform keys; 1: mixed-rate keys in nibble records; 2: mixed-rate
+ *           keys in tight records (the allocation must spend k_bits * 64 block
+ *           bits per KV head)
  * Errors: TQ_ERR_INVALID_ARG (non-positive sizes, n_q_heads not a multiple of
  * n_kv_heads, bad enum), TQ_ERR_UNSUPPORTED (head_dim != 128, group >
  * TQ_MAX_GROUP, bits outside the sets above, k_bits 3/4 different from v_bits,
@@ -272,7 +281,8 @@ size_t tq_cache_bytes(const tq_cache_desc* desc, int32_t part);
  *   k_group_mats host fp32: for each KV head, for each width b = 1..4 whose
  *                group is non-empty (n_b = 2 * #blocks), the n_b x n_b
  *                row-major orthogonal matrix Pi_b, concatenated; required iff
- *                k_mixed.  For two-stage keys (k_bits 1 or 2): the QJL
+ *                k_mixed.  With k_mixed = 2 every head's k_block_bits must sum to
+ *                k_bits * 64 (TQ_ERR_INVALID_ARG otherwise).  For two-stage keys (k_bits 1 or 2): the QJL
  *                projections S, [n_kv][128][128] row-major (row j gives sign
  *                bit j), entries i.i.d. N(0, 1) drawn by the caller; required
  * Codebooks are solved here (tq_codebook) for every (width, bits) in use.

@@ -19,9 +19,11 @@
 
 #include "tq_decode_cc.cuh"
 
-// Two-stage keys (tq_decode_two_stage.cu): the kernel for (padded group, key
-// format, value format, V mode), or null.
+// Two-stage keys (tq_decode_two_stage.cu) and tight mixed-rate key records
+// (tq_decode_tight.cu): the kernel for (padded group, key format, value format,
+// V mode), or null.
 KernelFn tq_two_stage_kernel(int GP, int kf, int vf, int mode);
+KernelFn tq_tight_kernel(int GP, int kf, int vf, int mode);
 
 namespace {
 template <int GP>
@@ -39,6 +41,10 @@ KernelFn pick_kernel(int G, int kf, int vf, int mode, int* GP) {
     if (kf == TQ_FMT_QJ1 || kf == TQ_FMT_QJ2) {
         *GP = G <= 1 ? 1 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
         return tq_two_stage_kernel(*GP, kf, vf, mode);
+    }
+    if (kf == TQ_FMT_MXT2 || kf == TQ_FMT_MXT3) {
+        *GP = G <= 1 ? 1 : G <= 4 ? 4 : G <= 8 ? 8 : 16;
+        return tq_tight_kernel(*GP, kf, vf, mode);
     }
     if (G <= 1) { *GP = 1; return pick_fmt<1>(kf, vf, mode); }
     if (G <= 4) { *GP = 4; return pick_fmt<4>(kf, vf, mode); }

@@ -32,6 +32,7 @@ template <int GP, int KF, int VF>
 __global__ void __launch_bounds__(kThreads) decode_dp(DecodeArgs a) {
     using KFm = Fmt<KF>;
     using VFm = Fmt<VF>;
+    static_assert(!KFm::tight || KFm::words <= VFm::words, "tight key records are staged in the V tile");
     __shared__ __align__(16) SmemDP<GP, KF, VF> S;
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -63,12 +64,16 @@ __global__ void __launch_bounds__(kThreads) decode_dp(DecodeArgs a) {
             float kn[4];
             load_record<KF>(a.k_codes, head_tok + j, rec);
             load_norms<KF>(a.k_norms, head_tok + j, a.norm_f16, kn);
-            qk_token<GP, KF>(rec, kn, S.s.qt, S.s.ut, S.s.kcb, S.s.kseg_of, sc);
+            // tight key records are staged in the V tile's words (column tid),
+            // which the V copy below overwrites after the barrier
+            qk_token<GP, KF>(rec, kn, S.s.qt, S.s.ut, S.s.kcb, S.s.kseg_of, sc, S.vtile + tid, kThreads,
+                             S.s.kseg_start);
             load_norms<VF>(a.v_norms, head_tok + j, a.norm_f16, vn);
         } else {
 #pragma unroll
             for (int g = 0; g < GP; ++g) sc[g] = -INFINITY;
         }
+        if constexpr (KFm::tight) __syncthreads();
         // stage the tile's V codes (contiguous records), 16-byte copies
         {
             const uint4* src = reinterpret_cast<const uint4*>(a.v_codes + (head_tok + tile) * VFm::bytes);
@@ -154,6 +159,7 @@ template <int GP, int KF, int VF>
 __global__ void __launch_bounds__(kThreads) decode_tp(DecodeArgs a) {
     using KFm = Fmt<KF>;
     using VFm = Fmt<VF>;
+    static_assert(!KFm::tight || KFm::words <= VRow<GP, VF>::stride, "tight key records are staged in the V rows");
     __shared__ __align__(16) SmemTP<GP, KF, VF> S;
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -181,7 +187,8 @@ __global__ void __launch_bounds__(kThreads) decode_tp(DecodeArgs a) {
             float kn[4];
             load_record<KF>(a.k_codes, head_tok + j, rec);
             load_norms<KF>(a.k_norms, head_tok + j, a.norm_f16, kn);
-            qk_token<GP, KF>(rec, kn, S.s.qt, S.s.ut, S.s.kcb, S.s.kseg_of, sc);
+            // tight key records are staged in this lane's V row before its V record
+            qk_token<GP, KF>(rec, kn, S.s.qt, S.s.ut, S.s.kcb, S.s.kseg_of, sc, myrow, 1, S.s.kseg_start);
             uint32_t vr[VFm::words];
             float vn[4] = {1.f, 1.f, 1.f, 1.f};
             load_record<VF>(a.v_codes, head_tok + j, vr);

@@ -44,11 +44,13 @@ template <int F> struct Fmt {
     // two-stage keys: `mse_words` words of 1-bit codes, then 4 words of signs
     static constexpr bool qjl = (F == TQ_FMT_QJ1 || F == TQ_FMT_QJ2);
     static constexpr int mse_words = F == TQ_FMT_QJ2 ? 4 : 0;
-    static constexpr int bytes = qjl ? 4 * (mse_words + 4) : three ? 48 : 64;
+    // mixed-rate keys in tight records (codes at their groups' widths)
+    static constexpr bool tight = (F == TQ_FMT_MXT2 || F == TQ_FMT_MXT3);
+    static constexpr int bytes = qjl ? 4 * (mse_words + 4) : tight ? (F == TQ_FMT_MXT2 ? 32 : 48) : three ? 48 : 64;
     static constexpr int words = bytes / 4;
     static constexpr int nslots = qjl ? 2 : (F == TQ_FMT_ONE3 || F == TQ_FMT_ONE4) ? 1 : 4;
     static constexpr bool blk = (F == TQ_FMT_BLK3 || F == TQ_FMT_BLK4);
-    static constexpr bool mix = (F == TQ_FMT_MIX4);
+    static constexpr bool mix = (F == TQ_FMT_MIX4 || tight);
 };
 
 // index of code c (compile-time in unrolled loops) from a record in registers
@@ -114,14 +116,45 @@ __device__ __forceinline__ void load_row(const float* row, float* q) {
 // q~ already carries log2(e) / sqrt(d)).  Two-stage keys [TQ-MNN §2.4]:
 // s_g = n <q~_g, C[idx]> + n rho <u_g, 2 sign - 1> with u_g = S q~_g sqrt(pi/2) / d
 // (in ut, same units); nrm = (n, n rho).
+//
+// Tight mixed-rate records: the record goes to this thread's staging words
+// (kst[i * kstride]) and the groups are walked in ascending width, the code at
+// position p read from bit offset sum_{p' < p} b_p' (funnel shift of two staged
+// words); kseg_start holds the groups' first positions.
 template <int GP, int KF>
 __device__ __forceinline__ void qk_token(const uint32_t* rec, const float* nrm, const float (*qt)[GP],
                                          const float (*ut)[GP], const float (*kcb)[16], const uint8_t* kseg_of,
-                                         float* sc) {
+                                         float* sc, uint32_t* kst = nullptr, int kstride = 0,
+                                         const int* kseg_start = nullptr) {
     using K = Fmt<KF>;
 #pragma unroll
     for (int g = 0; g < GP; ++g) sc[g] = 0.f;
-    if constexpr (K::qjl) {
+    if constexpr (K::tight) {
+#pragma unroll
+        for (int i = 0; i < K::words; ++i) kst[i * kstride] = rec[i];
+        int off = 0;
+#pragma unroll 1
+        for (int s = 0; s < 4; ++s) {
+            const int p1 = kseg_start[s + 1];
+            const uint32_t mask = (2u << s) - 1u;   // width s + 1
+            float part[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) part[g] = 0.f;
+#pragma unroll 2
+            for (int p = kseg_start[s]; p < p1; ++p, off += s + 1) {
+                const int wi = off >> 5;
+                const uint32_t lo = kst[wi * kstride];
+                const uint32_t hi = kst[min(wi + 1, K::words - 1) * kstride];
+                const float v = kcb[s][__funnelshift_r(lo, hi, off & 31) & mask];
+                float q[GP];
+                load_row<GP>(qt[p], q);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) part[g] = fmaf(v, q[g], part[g]);
+            }
+#pragma unroll
+            for (int g = 0; g < GP; ++g) sc[g] = fmaf(nrm[s], part[g], sc[g]);
+        }
+    } else if constexpr (K::qjl) {
         float ms[GP], sg[GP];
 #pragma unroll
         for (int g = 0; g < GP; ++g) { ms[g] = 0.f; sg[g] = 0.f; }
@@ -193,6 +226,7 @@ struct Smem {
     alignas(16) float red2[4][GP];
     alignas(16) uint8_t kseg_of[128];
     alignas(16) float ut[Fmt<KF>::qjl ? 128 : 1][GP];   // two-stage keys: S q~ sqrt(pi/2) / d
+    int kseg_start[5];                                  // mixed-rate keys: the groups' first positions
     int is_last;
 };
 
@@ -209,6 +243,7 @@ __device__ __forceinline__ void prologue(const DecodeArgs& a, const tq_head_para
         int s = 0;
         while (s < 3 && tid >= P.k_seg_start[s + 1]) ++s;
         S.kseg_of[tid] = (uint8_t)s;
+        if (tid < 5) S.kseg_start[tid] = P.k_seg_start[tid];
     }
     for (int g = warp; g < GP; g += 4) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};

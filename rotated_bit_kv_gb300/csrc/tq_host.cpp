@@ -274,7 +274,7 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     if (n_q_heads % n_kv_heads) return TQ_ERR_INVALID_ARG;
     if (rot != TQ_ROT_WHT128 && rot != TQ_ROT_WHT32 && rot != TQ_ROT_SO4_WHT128) return TQ_ERR_INVALID_ARG;
     if (norm_dtype != TQ_F16 && norm_dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
-    if (k_mixed != 0 && k_mixed != 1) return TQ_ERR_INVALID_ARG;
+    if (k_mixed < 0 || k_mixed > 2) return TQ_ERR_INVALID_ARG;
     if (head_dim != TQ_HEAD_DIM) return TQ_ERR_UNSUPPORTED;
     if (n_q_heads / n_kv_heads > TQ_MAX_GROUP) return TQ_ERR_UNSUPPORTED;
     if (v_bits != 3 && v_bits != 4) return TQ_ERR_UNSUPPORTED;
@@ -283,6 +283,9 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     if (!k_mixed && !two && k_bits != 3 && k_bits != 4) return TQ_ERR_UNSUPPORTED;
     if (!k_mixed && !two && k_bits != v_bits) return TQ_ERR_UNSUPPORTED;   // one kernel per shared width
     if ((k_mixed || two) && rot == TQ_ROT_WHT32) return TQ_ERR_UNSUPPORTED;
+    // tight mixed-rate records: k_bits is the average bits per coordinate
+    const bool tight = k_mixed == 2;
+    if (tight && k_bits != 2 && k_bits != 3) return TQ_ERR_UNSUPPORTED;
     if ((int64_t)batch * n_kv_heads * t_capacity > (int64_t)1 << 40) return TQ_ERR_INVALID_ARG;
     d->head_dim = head_dim;
     d->n_q_heads = n_q_heads;
@@ -290,20 +293,20 @@ tq_status tq_cache_desc_init(tq_cache_desc* d, int32_t head_dim, int32_t n_q_hea
     d->batch = batch;
     d->t_capacity = t_capacity;
     d->rot = rot;
-    d->k_bits = k_mixed ? 0 : k_bits;
+    d->k_bits = k_mixed == 1 ? 0 : k_bits;
     d->v_bits = v_bits;
     d->norm_dtype = norm_dtype;
     d->k_mixed = k_mixed;
     d->group = n_q_heads / n_kv_heads;
-    d->k_code_bytes = k_mixed ? 64 : two ? 16 * k_bits : (k_bits == 3 ? 48 : 64);
+    d->k_code_bytes = tight ? 16 * k_bits : k_mixed ? 64 : two ? 16 * k_bits : (k_bits == 3 ? 48 : 64);
     d->v_code_bytes = v_bits == 3 ? 48 : 64;
     d->k_norm_slots = (k_mixed || rot == TQ_ROT_WHT32) ? 4 : two ? 2 : 1;
     d->v_norm_slots = rot == TQ_ROT_WHT32 ? 4 : 1;
     d->norm_bytes = norm_dtype == TQ_F16 ? 2 : 4;
     // the tile layout (read by the tensor-core decode kernel) for every format it
     // covers: at most 8 query heads per KV head, fp16 norms where a vector has
-    // four (the 32-wide blocks, mixed-rate keys), not two-stage keys
-    const bool tile = d->group <= 8 && !two && !((rot == TQ_ROT_WHT32 || k_mixed) && norm_dtype != TQ_F16);
+    // four (the 32-wide blocks, mixed-rate keys), not two-stage keys or tight records
+    const bool tile = d->group <= 8 && !two && !tight && !((rot == TQ_ROT_WHT32 || k_mixed) && norm_dtype != TQ_F16);
     d->layout = tile ? TQ_LAYOUT_TILE16 : TQ_LAYOUT_NATURAL;
     const int64_t alloc = tile ? ((int64_t)t_capacity + 15) / 16 * 16 : t_capacity;
     if (alloc > 0x7fffffff) return TQ_ERR_INVALID_ARG;
@@ -395,8 +398,12 @@ tq_status tq_params_build(const tq_cache_desc* d, const float* signs, const floa
             // same-width groups in ascending width [Block-GTQ]; block i is
             // coordinates (2i, 2i+1)
             const int32_t* bb = k_block_bits + (size_t)h * 64;
-            for (int i = 0; i < 64; ++i)
+            int spent = 0;
+            for (int i = 0; i < 64; ++i) {
                 if (bb[i] < 1 || bb[i] > 4) return TQ_ERR_INVALID_ARG;
+                spent += bb[i];
+            }
+            if (d->k_mixed == 2 && spent != 64 * d->k_bits) return TQ_ERR_INVALID_ARG;   // fills the tight record
             float* kmat = kmat_all + (size_t)h * 128 * 128;
             int pos = 0;
             p.k_nseg = 4;

@@ -57,9 +57,12 @@ enum tq_fmt : int {
     TQ_FMT_MIX4 = 4,   // runtime segments, one code per nibble (64 B)
     TQ_FMT_QJ1 = 5,    // two-stage keys, k_bits 1: 128 sign bits (16 B)
     TQ_FMT_QJ2 = 6,    // two-stage keys, k_bits 2: 128 one-bit codes + 128 sign bits (32 B)
+    TQ_FMT_MXT2 = 7,   // mixed-rate keys, tight records, 2 bits on average (32 B)
+    TQ_FMT_MXT3 = 8,   // mixed-rate keys, tight records, 3 bits on average (48 B)
 };
 
 static inline int tq_k_fmt(const tq_cache_desc* d) {
+    if (d->k_mixed == 2) return d->k_bits == 2 ? TQ_FMT_MXT2 : TQ_FMT_MXT3;
     if (d->k_mixed) return TQ_FMT_MIX4;
     if (tq_two_stage(d)) return d->k_bits == 1 ? TQ_FMT_QJ1 : TQ_FMT_QJ2;
     if (d->rot == TQ_ROT_WHT32) return d->k_bits == 3 ? TQ_FMT_BLK3 : TQ_FMT_BLK4;

@@ -30,6 +30,7 @@ struct QuantArgs {
     // per position
     int B, n_new, Hkv, Tcap, t_alloc, tiled, in_dtype, norm_f16, rot, k_mixed;
     int k_two;                   // two-stage keys: k_bits (1 or 2), else 0
+    int k_tight;                 // mixed-rate keys in tight records (natural layout)
     int code_bytes[2], norm_slots[2];
 };
 
@@ -196,6 +197,45 @@ __device__ __forceinline__ void encode_vector(const QuantArgs& a, const VecId& i
     }
     // pack and store (tile layout: the record goes through the warp's staging
     // buffer, once every lane is done reading the staged input)
+    if (mixed && a.k_tight) {
+        // tight record [Block-GTQ, packed cache]: the lane's four codes at their
+        // widths (at most 16 bits) at the bit offset of position 4l, the
+        // exclusive prefix of the lanes' widths; OR-ed into a zeroed staging copy
+        int sh = 0;
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v |= idx[i] << sh;
+            sh += seg_bits[segi[i]];
+        }
+        int off = sh;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int o = __shfl_up_sync(TQ_FULL_MASK, off, m);
+            if (lane >= m) off += o;
+        }
+        off -= sh;
+        uint32_t* st = reinterpret_cast<uint32_t*>(xs);
+        __syncwarp();   // every lane is done with the staged input
+        if (lane < 16) st[lane] = 0u;
+        __syncwarp();
+        const int wi = off >> 5, bs = off & 31;
+        atomicOr(st + wi, v << bs);
+        if (bs + sh > 32) atomicOr(st + wi + 1, v >> (32 - bs));
+        __syncwarp();
+        const size_t pos = (((size_t)b * a.Hkv + h) * a.t_alloc) + slot;
+        uint32_t* out = reinterpret_cast<uint32_t*>(a.codes[0] + pos * a.code_bytes[0]);
+        if (lane < (a.code_bytes[0] >> 2)) out[lane] = st[lane];
+        if (lane < 4) {
+            const size_t ni = pos * 4 + lane;
+            float n = nrm[0];
+#pragma unroll
+            for (int k = 1; k < 4; ++k) n = lane == k ? nrm[k] : n;
+            if (a.norm_f16) static_cast<__half*>(a.norms[0])[ni] = __float2half_rn(n);
+            else static_cast<float*>(a.norms[0])[ni] = n;
+        }
+        return;
+    }
     if (a.tiled) __syncwarp();
     const size_t pos = (((size_t)b * a.Hkv + h) * a.t_alloc) + slot;
     uint8_t* rec = a.tiled ? reinterpret_cast<uint8_t*>(xs)
@@ -1105,6 +1145,7 @@ extern "C" tq_status tq_quantize_append(const tq_cache_desc* d, const tq_cache_p
     a.rot = d->rot;
     a.k_mixed = d->k_mixed;
     a.k_two = tq_two_stage(d) ? d->k_bits : 0;
+    a.k_tight = d->k_mixed == 2;
     a.code_bytes[0] = d->k_code_bytes;
     a.code_bytes[1] = d->v_code_bytes;
     a.norm_slots[0] = d->k_norm_slots;

@@ -67,8 +67,12 @@ def make_setup(tq, wl: W.Workload, inp: W.Inputs, t_capacity: int) -> Setup:
                 flat.append(m[b].ravel())
             mats.append(m)
         flat = np.concatenate(flat)
+    # mixed-rate keys: nibble records (k_mixed 1), or tight records (k_mixed 2, k_bits
+    # the average width)
+    k_mixed = (2 if wl.tight_k else 1) if wl.mixed_k else 0
+    k_bits = (wl.avg_bits if wl.tight_k else 0) if wl.mixed_k else wl.k_bits
     desc = tq.tq_cache_desc_init(wl.head_dim, wl.n_q_heads, wl.n_kv_heads, wl.batch, t_capacity, wl.rot,
-                                 0 if wl.mixed_k else wl.k_bits, wl.v_bits, wl.norm_dtype, int(wl.mixed_k))
+                                 k_bits, wl.v_bits, wl.norm_dtype, k_mixed)
     blob = tq.tq_params_build(desc, signs=inp.signs, quats=inp.quats,
                               k_block_bits=block_bits, k_group_mats=flat if wl.mixed_k else None)
     specs = O.head_specs(wl, inp, block_bits, mats)

@@ -52,6 +52,10 @@ def _workload(name):
         "llama8b_g16": W.llama8b_decode().with_(n_kv_heads=2),
         "block32_f32": W.block32(3).with_(norm_dtype=W.F32),
         "mixed_f32": W.mixed_rate_long().with_(norm_dtype=W.F32),
+        # mixed-rate keys in tight records: 3 bits on average (48 B), and 2 bits
+        # with four query heads per KV head (32 B)
+        "mixed_tight": W.mixed_rate_long().with_(tight_k=True),
+        "mixed_tight2": W.mixed_rate_long().with_(tight_k=True, avg_bits=2, n_q_heads=8),
     }[name]
 
 
@@ -66,11 +70,13 @@ SMALL = {  # (batch, T) element-wise cases: several tiles and a ragged tail
     "llama8b_g16": (2, 333),
     "block32_f32": (2, 333),
     "mixed_f32": (1, 600),
+    "mixed_tight": (1, 700),
+    "mixed_tight2": (2, 600),
 }
 # TQ_LAYOUT_TILE16 caches (tensor-core decode kernel)
 TILED = ["tiny", "llama8b", "block32_tq3", "block32_tq4", "so4", "mixed", "mixed_g4"]
 # TQ_LAYOUT_NATURAL caches (CUDA-core decode kernels)
-NATURAL = ["llama8b_g16", "block32_f32", "mixed_f32"]
+NATURAL = ["llama8b_g16", "block32_f32", "mixed_f32", "mixed_tight", "mixed_tight2"]
 
 
 def _encode_on_gpu(tq, name, B, T, cap_extra=5, seq_lens=None):
@@ -551,6 +557,7 @@ FULL = {
     "so4_32k": (W.so4_wht(seq_len=32768), [(0, 0), (0, 3)]),
     "mixed_131k": (W.mixed_rate_long(131072), [(0, 0), (0, 1)]),
     "mixed_524k": (W.mixed_rate_long(524288), [(0, 1)]),
+    "mixed_tight_131k": (W.mixed_rate_long(131072).with_(tight_k=True), [(0, 0)]),
 }
 
 
