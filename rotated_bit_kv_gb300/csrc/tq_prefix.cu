@@ -256,11 +256,8 @@ __global__ void __launch_bounds__(kPThr) prefix_attend(PrefixArgs a) {
 constexpr int kTW = 8;
 constexpr int kTThr = kTW * 32;
 
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
-    return pack_h2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-}
-
-// N fp16 words (2N elements) of the input from element `elem` (16-byte aligned)
+// N 16-bit pair words (2N elements) of the input from element `elem` (16-byte
+// aligned): fp32 rounded to fp16 pairs; fp16 and bf16 words as they are
 template <int DT, int N>
 __device__ __forceinline__ void load_words(const void* base, size_t elem, uint32_t (&w)[N]) {
     if constexpr (DT == TQ_F32) {
@@ -277,10 +274,6 @@ __device__ __forceinline__ void load_words(const void* base, size_t elem, uint32
         for (int i = 0; i < N / 4; ++i) {
             const uint4 x = __ldg(p + i);
             w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
-        }
-        if constexpr (DT == TQ_BF16) {
-#pragma unroll
-            for (int i = 0; i < N; ++i) w[i] = bf2_to_h2(w[i]);
         }
     }
 }

@@ -481,31 +481,6 @@ __global__ void __launch_bounds__(kWarps * 32) tq_quantize_kernel(QuantArgs a) {
 // strides 8 .. 64 cross lanes of the half; 3-bit codes of four lanes are the
 // three words of a 32-coordinate group.  Same steps and results as encode_vector.
 
-__device__ __forceinline__ void load8(const void* base, size_t elem, int dtype, float v[8]) {
-    if (dtype == TQ_F32) {
-        const float4 x = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
-        const float4 y = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem + 4);
-        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-    } else if (dtype == TQ_F16) {
-        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __half*>(base) + elem);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            v[2 * i] = f.x;
-            v[2 * i + 1] = f.y;
-        }
-    } else {
-        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-}
-
 // Walsh-Hadamard butterflies over 8 * LANES coordinates held 8 per lane
 template <int LANES>
 __device__ __forceinline__ void wht8(float v[8]) {
