@@ -77,7 +77,7 @@ def _plens(B, P):
     return p
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama8b", "so4", "mixed", "llama8b_g16", "block32_f32"])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "so4", "mixed", "llama8b_g16", "block32_f32", "mixed_tight"])
 def test_prefix_plus_packed(tq, name):
     B, _ = SMALL[name]
     _run(tq, name, 300, _plens(B, 300), lambda L, T: L)

@@ -229,3 +229,43 @@ def test_decode_empty_and_clamped(tq):
     assert not o[0].any()
     assert int(cache.status.item()) & tq.TQ_DEV_SEQ_OVER_MAX
     _check(tq, st, cache, {k: v for k, v in encs.items() if k[0] > 0}, [0, 150, 200], 160)
+
+
+def test_prefix_plus_two_stage(tq):
+    """Unquantised fp16 tokens plus a cache with two-stage keys
+    (tq_decode_attention_prefix): the packed part's estimated scores and the
+    unquantised part's exact ones, merged by log-sum-exp (each part's state from
+    the oracle's functions)."""
+    B, T, P = 2, 300, 96
+    st = _setup(tq, _workload(2, batch=B, n_kv_heads=2, n_q_heads=8), T)
+    cache = tq.PackedKVCache(st.desc, st.blob)
+    encs = _upload(tq, st, cache, T)
+    rng = np.random.default_rng([3, 0x5046])
+    Kp = (rng.standard_normal((B, P, 2, 128)) * 2.0).astype(np.float16)
+    Vp = rng.standard_normal((B, P, 2, 128)).astype(np.float16)
+    plens, lens = np.array([P, 40], np.int32), np.array([T, 123], np.int32)
+    q = to_torch_input(torch, st.inp.q, st.wl.in_dtype)
+    out = cache.decode_prefix(q, torch.from_numpy(lens).cuda(), T, torch.from_numpy(Kp).cuda(),
+                              torch.from_numpy(Vp).cuda(), torch.from_numpy(plens).cuda(), P)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0
+    o = out.cpu().numpy()
+    G = st.wl.group
+    errs, scales = [], []
+    for (b, h), (idx, sb, nr, ev) in encs.items():
+        qh = W.as_float64(st.inp.q[b, h * G:(h + 1) * G], st.wl.in_dtype)
+        L = int(lens[b])
+        s = O.qjl_scores(qh, idx[:L], sb[:L], nr[:L].astype(np.float64), st.qspecs[h]) / np.sqrt(128.0)
+        m1 = s.max(axis=1)
+        p = np.exp(s - m1[:, None])
+        vt = O.dequantize_rotated(ev.idx[:L], ev.norms[:L].astype(np.float64), st.vspecs[h])
+        o1, l1 = (p @ vt) @ st.vspecs[h].R, p.sum(axis=1)
+        n = int(plens[b])
+        m2, l2, o2 = O.part_state(qh, Kp[b, :n, h].astype(np.float64), Vp[b, :n, h].astype(np.float64))
+        M = np.maximum(m1, m2)
+        w1, w2 = np.exp(m1 - M), np.exp(m2 - M)
+        ref = (w1[:, None] * o1 + w2[:, None] * o2) / (w1 * l1 + w2 * l2)[:, None]
+        e, sc = att_error(o[b, h * G:(h + 1) * G], ref)
+        errs.append(e)
+        scales.append(sc)
+    assert max(errs) <= ATT_TOL * max(scales), (max(errs), max(scales))
