@@ -507,7 +507,7 @@ def library_setup(tq, wl, inp, t_capacity):
     """Descriptor and parameter blob through the library alone.  Mixed-rate keys:
     block energies and the greedy allocation from the library's own entry
     points, one seeded Haar matrix per non-empty same-width group (ascending
-    width) of each KV head."""
+    width) of each KV head.  Two-stage keys: one seeded projection per KV head."""
     block_bits = mats = None
     if wl.mixed_k:
         G = wl.group
@@ -526,6 +526,8 @@ def library_setup(tq, wl, inp, t_capacity):
         mats = np.concatenate(flat)
     k_mixed = (2 if wl.tight_k else 1) if wl.mixed_k else 0
     k_bits = (wl.avg_bits if wl.tight_k else 0) if wl.mixed_k else wl.k_bits
+    if not wl.mixed_k and wl.k_bits in (1, 2):   # two-stage keys: the projections
+        mats = np.stack([W.two_stage_projection(wl.head_dim, wl.seed, h) for h in range(wl.n_kv_heads)])
     desc = tq.tq_cache_desc_init(wl.head_dim, wl.n_q_heads, wl.n_kv_heads, wl.batch, t_capacity, wl.rot,
                                  k_bits, wl.v_bits, wl.norm_dtype, k_mixed)
     blob = tq.tq_params_build(desc, signs=inp.signs, quats=inp.quats, k_block_bits=block_bits, k_group_mats=mats)
@@ -602,8 +604,9 @@ def run_sweep(args):
 def run_crossover(args):
     """Token- against dimension-parallel V accumulation on the caches that use those
     kernels (natural layout: 16 query heads per KV head, fp32 norms with mixed-rate
-    keys or with 32-wide blocks): decode time of each kernel over a range of lengths (one
-    cache per workload filled to its longest length, the same launches as the sweep)."""
+    keys or with 32-wide blocks, tight mixed-rate records, two-stage keys): decode time of
+    each kernel over a range of lengths (one cache per workload filled to its longest
+    length, the same launches as the sweep)."""
     import torch
 
     import rotated_bit_kv_gb300 as tq
@@ -614,7 +617,11 @@ def run_crossover(args):
     lengths = [64, 128, 256, 384, 512, 768, 1024, 2048, 4096]
     cases = [W.mixed_rate_long(seq_len=max(lengths)).with_(norm_dtype=W.F32),
              W.llama8b_decode(seq_len=max(lengths), batch=8).with_(n_kv_heads=2),
-             W.block32(3, seq_len=max(lengths), batch=8).with_(norm_dtype=W.F32)]
+             W.block32(3, seq_len=max(lengths), batch=8).with_(norm_dtype=W.F32),
+             W.mixed_rate_long(seq_len=max(lengths)).with_(tight_k=True, name="mixed_rate_long_tight"),
+             W.two_stage_keys(2, seq_len=max(lengths), batch=8)]
+    if args.only:
+        cases = [wl for wl in cases if args.only in wl.name]
     print("| workload | B | T | token-parallel us | dimension-parallel us | faster |")
     print("|---|---|---|---|---|---|")
     for wl in cases:
