@@ -196,9 +196,9 @@ int tq_v_crossover(const tq_cache_desc* d) {
         if (v >= 0 && v < (1L << 30)) return (int)v;
     }
     // Measured on GB300 for each natural-layout format (16 query heads per KV
-    // head; fp32 norms with 32-wide blocks; fp32 norms with mixed-rate keys) over
-    // T = 64 .. 4096: dimension-parallel accumulation is as fast or faster at
-    // every length (the pages' T = 512 crossover comes from a GPU without the
+    // head; fp32 norms with 32-wide blocks; fp32 norms with mixed-rate keys; tight
+    // mixed-rate records; two-stage keys) over T = 64 .. 4096: dimension-parallel
+    // accumulation is as fast or faster at every length (the pages' T = 512 crossover comes from a GPU without the
     // key-axis split), so the crossover is 0 for all of them.
     (void)d;
     return 0;
